@@ -1,0 +1,406 @@
+"""Pins of the CPU oracle to facts other than itself.
+
+Each test checks the oracle against a hand-worked example from a fixture
+under tests/golden/ (with its citation), a closed form, an invariant, an
+exhaustive table, or brute force on tiny inputs, chosen so that a plausible
+slip (a dropped term, a wrong sign or index, a transposed operand, a wrong tie
+rule) fails at least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import read_golden
+
+# ----------------------------------------------------------------------------
+# number formats
+# ----------------------------------------------------------------------------
+
+
+def test_e2m1_table_and_roundtrip():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        v = oracle.e2m1_value(c)
+        assert abs(v) == mags[c & 7]
+        assert math.copysign(1.0, v) == (-1.0 if c & 8 else 1.0)
+        assert oracle.e2m1_encode(v) == c          # every code is a fixed point
+    assert oracle.e2m1_encode(7.0) == 7 and oracle.e2m1_encode(-1e9) == 15   # saturation
+    assert oracle.e2m1_encode(-0.2) == 8                                     # signed zero
+
+
+def test_e2m1_ties_to_even_code():
+    # midpoints between neighbouring magnitudes go to the code with bit0 = 0
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for i in range(7):
+        mid = (mags[i] + mags[i + 1]) / 2
+        want = i if i % 2 == 0 else i + 1
+        assert oracle.e2m1_encode(mid) == want, mid
+        assert oracle.e2m1_encode(-mid) == 8 | want
+        assert oracle.e2m1_encode(np.nextafter(np.float32(mid), np.float32(10))) == i + 1
+        assert oracle.e2m1_encode(np.nextafter(np.float32(mid), np.float32(-1))) == i
+
+
+def test_e4m3_known_values():
+    # OCP 8-bit floating point (E4M3 "FN"): max 448, min normal 2^-6, min subnormal 2^-9
+    assert oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert oracle.e4m3_value(0x38) == 1.0
+    assert oracle.e4m3_value(0x77) == 240.0
+    assert oracle.e4m3_value(0xFE) == -448.0
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+    # 127 finite non-negative codes, strictly increasing
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    assert all(a < b for a, b in zip(vals, vals[1:]))
+
+
+def test_e4m3_roundtrip_ties_and_saturation():
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c
+    vals = [oracle.e4m3_value(c) for c in range(0x7F)]
+    for c in range(0x7E):
+        mid = (vals[c] + vals[c + 1]) / 2   # exactly representable in fp32
+        assert np.float32(mid) == mid
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(mid) == want
+    assert oracle.e4m3_encode(449.0) == 0x7E and oracle.e4m3_encode(1e30) == 0x7E
+    assert oracle.e4m3_encode(-1e30) == 0xFE
+    assert oracle.e4m3_encode(2.0 ** -11) == 0x00      # below half the min subnormal
+    assert oracle.e4m3_encode(-(2.0 ** -11)) == 0x80   # signed zero
+
+
+def test_e8m0_values():
+    assert oracle.e8m0_value(127) == 1.0
+    assert oracle.e8m0_value(120) == 2.0 ** -7
+    assert oracle.e8m0_value(0) == 2.0 ** -127
+    assert math.isnan(oracle.e8m0_value(255))
+
+
+def _bf16_exact(v):
+    """Round v to 8 significant bits with ties to even, in exact rationals."""
+    f = Fraction(v)
+    if f == 0:
+        return 0.0
+    e = math.floor(math.log2(abs(v)))
+    q = Fraction(2) ** (e - 7)
+    n = f / q
+    fl = math.floor(n)
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return float(fl * q)
+
+
+def test_bf16_rounding_brute_force():
+    rng = np.random.default_rng(7)
+    vals = list(rng.standard_normal(300) * 10.0 ** rng.integers(-5, 5, 300))
+    vals += [1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 255.5, 257.0, 100.0]
+    for v in vals:
+        bits = oracle.bf16_from_f64(float(v))
+        assert oracle.bf16_value(bits) == _bf16_exact(float(v)), v
+
+
+# ----------------------------------------------------------------------------
+# quantisers: worked examples
+# ----------------------------------------------------------------------------
+
+
+def test_nvfp4_worked_block():
+    g = read_golden("nvfp4_block_roundtrip.txt")
+    v = np.array([float(s) for s in g["values"]], np.float32)[None, :]
+    codes, sf, glob = oracle.nvfp4_quantize(v)
+    assert glob[0] == float(g["global"][0])
+    assert [f"{b:02X}" for b in sf[0]] == g["scales_hex"]
+    nib = []
+    for b in codes[0]:
+        nib += [b & 15, b >> 4]                 # low nibble holds the lower index
+    assert [f"{q:X}" for q in nib] == g["codes_hex"]
+    dec = oracle.nvfp4_decode(codes, sf, glob)[0]
+    want = [float(s) for s in g["decoded"]]
+    assert list(dec) == want
+    assert math.copysign(1.0, dec[26]) == -1.0  # -0.1 -> -0
+
+
+def test_mxfp8_worked_blocks():
+    g = read_golden("mxfp8_block_roundtrip.txt")
+    a = np.array([float(s) for s in g["blockA_values"]], np.float32)
+    codes, sf = oracle.mxfp8_quantize(a[None, :])
+    assert f"{sf[0, 0]:02X}" == g["blockA_scale_hex"][0]
+    assert [f"{c:02X}" for c in codes[0]] == g["blockA_codes_hex"]
+    dec = oracle.mxfp8_decode(codes, sf)[0]
+    assert dec[0] == 3.0 and dec[1] == 1.0 and dec[2] == -1.0 and dec[3] == 40 / 128 and dec[4] == 2.0
+    b = np.array([float(s) for s in g["blockB_values"]], np.float32)[None, :]
+    c0, s0 = oracle.mxfp8_quantize(b, mode=0)
+    c1, s1 = oracle.mxfp8_quantize(b, mode=1)
+    assert f"{s0[0, 0]:02X}" == g["blockB_mode0_scale_hex"][0] and f"{c0[0, 0]:02X}" == g["blockB_mode0_code0_hex"][0]
+    assert f"{s1[0, 0]:02X}" == g["blockB_mode1_scale_hex"][0] and f"{c1[0, 0]:02X}" == g["blockB_mode1_code0_hex"][0]
+
+
+def test_zero_blocks():
+    z = np.zeros((2, 64), np.float32)
+    codes, sf, g = oracle.nvfp4_quantize(z)
+    assert not codes.any() and not sf.any() and (g == 1.0).all()
+    codes, sf = oracle.mxfp8_quantize(z)
+    assert not codes.any() and not sf.any()
+
+
+def test_nvfp4_global_granularity():
+    # per row: each row's max element decodes back to itself (6 * 448 * g = amax)
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal((5, 64)) * np.array([[1e-3], [1], [7], [300], [0.02]])).astype(np.float32)
+    codes, sf, g = oracle.nvfp4_quantize(v)
+    dec = oracle.nvfp4_decode(codes, sf, g)
+    for r in range(5):
+        i = np.argmax(np.abs(v[r]))
+        assert abs(dec[r, i] - v[r, i]) <= 1e-6 * abs(v[r, i])
+        assert np.isclose(g[r], np.abs(v[r]).max() / 2688.0, rtol=1e-6)
+    # per tensor: one global from the whole matrix
+    codes, sf, gt = oracle.nvfp4_quantize(v, per_tensor=True)
+    assert gt.shape == (1,) and np.isclose(gt[0], np.abs(v).max() / 2688.0, rtol=1e-6)
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
+def test_quantiser_self_consistency_and_error_bound(fmt):
+    rng = np.random.default_rng(11)
+    v = (rng.standard_normal((16, 256)) * rng.uniform(0.01, 50, (16, 1))).astype(np.float32)
+    q = oracle.quantize(fmt, v)
+    dec = oracle.decode(fmt, *q)
+    # re-quantising the decoded values returns the same codes
+    q2 = oracle.quantize(fmt, dec.astype(np.float32))
+    assert np.array_equal(q[0], q2[0]) and np.array_equal(q[1], q2[1])
+    # error bound: half a grid step of the block's scale (element grids have
+    # at most 1 mantissa bit (E2M1) or 3 bits (E4M3)); saturation only in
+    # mode-0 MXFP8 blocks whose max lies in (448, 512) * X
+    bs = 16 if fmt == "nvfp4" else 32
+    for r in range(16):
+        for b in range(256 // bs):
+            blk = v[r, b * bs:(b + 1) * bs].astype(np.float64)
+            d = dec[r, b * bs:(b + 1) * bs]
+            amax = np.abs(blk).max()
+            if fmt == "nvfp4":
+                tol = amax / 6 * 1.0 * 1.07 + 1e-30     # step <= 2 at top binade of [0,6], /6 scale, +E4M3 scale error
+                assert np.all(np.abs(blk - d) <= tol)
+            else:
+                X = 2.0 ** (math.floor(math.log2(amax)) - 8)
+                err = np.abs(blk - d)
+                sat = np.abs(blk) > 448 * X
+                assert np.all(err[~sat] <= np.abs(blk[~sat]) * 2 ** -4 + X * 2 ** -9 / 2 + 1e-30)
+                assert np.all(np.abs(d[sat]) == 448 * X)
+
+
+# ----------------------------------------------------------------------------
+# router
+# ----------------------------------------------------------------------------
+
+
+def test_router_worked_example():
+    g = read_golden("router_4expert_top2.txt")
+    for case in ("case1", "case2"):
+        logits = np.array([[float(s) for s in g[case + "_logits"]]])
+        bias = np.array([float(s) for s in g[case + "_bias"]], np.float32)
+        idx, w, keys = oracle.router_select(logits, bias, 2)
+        assert list(idx[0]) == [int(s) for s in g[case + "_idx"]]
+        assert np.allclose(w[0], [float(s) for s in g[case + "_w"]], rtol=0, atol=1e-7)
+
+
+def test_router_logits_one_hot_and_brute_force():
+    # one-hot x picks a column of W_r exactly
+    H, E = 32, 6
+    rng = np.random.default_rng(5)
+    wr = rng.standard_normal((E, H)).astype(np.float32)
+    wr_b = (wr.view(np.uint32) >> 16).astype(np.uint16)
+    x = np.zeros((1, H), np.float32); x[0, 3] = 1.0
+    x_b = (x.view(np.uint32) >> 16).astype(np.uint16)
+    logits, absdot = oracle.router_logits(x_b, wr_b)
+    assert np.array_equal(logits[0], oracle.bf16_bits_to_f32(wr_b)[:, 3].astype(np.float64))
+    # brute force against a library matmul on tiny random inputs
+    x = rng.standard_normal((7, H)).astype(np.float32)
+    x_b = (x.view(np.uint32) >> 16).astype(np.uint16)
+    logits, absdot = oracle.router_logits(x_b, wr_b)
+    X = oracle.bf16_bits_to_f32(x_b).astype(np.float64)
+    W = oracle.bf16_bits_to_f32(wr_b).astype(np.float64)
+    assert np.allclose(logits, X @ W.T, rtol=1e-13, atol=1e-13)
+    assert np.allclose(absdot, np.abs(X) @ np.abs(W).T, rtol=1e-13)
+
+
+def test_router_select_brute_force_and_invariants():
+    rng = np.random.default_rng(9)
+    T, E, k = 50, 12, 3
+    logits = rng.standard_normal((T, E))
+    bias = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    idx, w, keys = oracle.router_select(logits, bias, k)
+    s = 1.0 / (1.0 + np.exp(-logits))
+    key = s + bias.astype(np.float64)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-key[t, e], e))[:k]
+        assert list(idx[t]) == order
+        assert np.allclose(w[t], s[t, order] / s[t, order].sum(), rtol=1e-14)
+    tie_idx, tie_w, _ = oracle.router_select(np.zeros((1, E)), np.zeros(E, np.float32), k)
+    assert list(tie_idx[0]) == list(range(k)) and np.allclose(tie_w, 1.0 / k)
+    assert np.allclose(w.sum(1), 1.0, atol=1e-12)
+    assert all(len(set(r)) == k for r in idx)          # distinct experts per token
+    idx2, w2, _ = oracle.router_select(logits, bias, k, routed_scale=2.5)
+    assert np.array_equal(idx, idx2) and np.allclose(w2, 2.5 * w)
+    # k = E: every expert, weights = normalised sigmoid of all
+    idx3, w3, _ = oracle.router_select(logits[:3], bias, E)
+    assert all(sorted(r) == list(range(E)) for r in idx3)
+
+
+# ----------------------------------------------------------------------------
+# dispatch and combine
+# ----------------------------------------------------------------------------
+
+
+def test_dispatch_invariants():
+    rng = np.random.default_rng(2)
+    T, E, k = 40, 9, 3
+    idx = np.array([rng.choice(E, k, replace=False) for _ in range(T)], np.int32)
+    d = oracle.dispatch(idx, E)
+    assert d["counts"].sum() == T * k
+    assert np.array_equal(d["counts"], np.bincount(idx.ravel(), minlength=E))
+    assert d["offsets"][0] == 0 and np.array_equal(np.diff(d["offsets"]), d["counts"])
+    perm = d["perm"]
+    assert sorted(perm) == list(range(T * k))                      # a permutation of pair ids
+    e_of = idx.ravel()[perm]
+    t_of = perm // k
+    assert all((e_of[i], t_of[i]) < (e_of[i + 1], t_of[i + 1]) for i in range(T * k - 1))
+    assert np.array_equal(d["pair_pos"].ravel()[perm], np.arange(T * k))   # pair_pos o perm = id
+    assert np.bincount(t_of, minlength=T).tolist() == [k] * T             # every token k times
+    # k = E: every expert sees all T tokens in order
+    full = np.tile(np.arange(E, dtype=np.int32), (5, 1))
+    d2 = oracle.dispatch(full, E)
+    assert (d2["counts"] == 5).all()
+
+
+def test_combine_one_hot_returns_weights():
+    rng = np.random.default_rng(4)
+    T, E, k = 6, 5, 2
+    idx = np.array([rng.choice(E, k, replace=False) for _ in range(T)], np.int32)
+    w = rng.uniform(0.1, 1.0, (T, k))
+    d = oracle.dispatch(idx, E)
+    H = T * k
+    y = np.zeros((T * k, H))
+    for p in range(T * k):
+        y[p, d["perm"][p]] = 1.0                # row p marks its own pair id
+    out = oracle.combine(w, d["pair_pos"], y)
+    for t in range(T):
+        for j in range(k):
+            assert out[t, t * k + j] == w[t, j]
+    assert np.count_nonzero(out) == T * k
+
+
+# ----------------------------------------------------------------------------
+# expert FFN
+# ----------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
+def test_ffn_closed_form_capped_saturation(fmt):
+    # a = e_0; W_gate[:,0] = +1e6, W_up[:,0] = -1e6 -> cap g = +10, cap u = -10,
+    # h = 10 * sigmoid(10) * -10 = -99.9955 -> bf16 -100.  NVFP4 holds it
+    # (block max -> 6 * 448 * g = 100); MXFP8 with X = 2^(6-8) maps 400 to the
+    # tie 384/416 -> 384, i.e. -96.  So y = hq * rowsum(W_down).
+    H, F = 64, 96
+    a = np.zeros((1, H)); a[0, 0] = 1.0
+    Wg = np.zeros((F, H)); Wg[:, 0] = 1e6
+    Wu = np.zeros((F, H)); Wu[:, 0] = -1e6
+    Wd = np.tile((np.arange(H) + 1.0)[:, None] / F, (1, F))
+    res = oracle.expert_ffn(fmt, Wg, Wu, Wd, a, cap=10.0)
+    assert (oracle.bf16_bits_to_f32(res["h_bf16"]) == -100.0).all()
+    hq = -100.0 if fmt == "nvfp4" else -96.0
+    assert np.allclose(res["y"][0], hq * (np.arange(H) + 1.0), rtol=1e-6)
+    # gate and up swapped gives silu(-10) * 10 = -4.54e-3 instead
+    res2 = oracle.expert_ffn(fmt, Wu, Wg, Wd, a, cap=10.0)
+    assert abs(oracle.bf16_bits_to_f32(res2["h_bf16"])[0, 0] - (-10 / (1 + math.exp(10)) * 10)) < 1e-4
+
+
+def test_ffn_zero_gate_gives_zero():
+    H, F = 32, 64
+    rng = np.random.default_rng(1)
+    a = rng.standard_normal((2, H))
+    res = oracle.expert_ffn("nvfp4", np.zeros((F, H)), rng.standard_normal((F, H)),
+                            rng.standard_normal((H, F)), a)
+    assert not res["y"].any()                   # silu(0) = 0
+
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "mxfp8"])
+def test_ffn_brute_force_tiny(fmt):
+    # E = 1, k = 1: one quantised FFN, checked with library matmuls; also the
+    # uncapped case (c = 0) reduces to plain SwiGLU.
+    H, F, n = 64, 96, 3
+    rng = np.random.default_rng(8)
+    Wg, Wu = rng.standard_normal((F, H)) / 8, rng.standard_normal((F, H)) / 8
+    Wd = rng.standard_normal((H, F)) / 10
+    a = rng.standard_normal((n, H))
+    for cap in (10.0, 0.0, 0.5):
+        res = oracle.expert_ffn(fmt, Wg, Wu, Wd, a, cap=cap)
+        g, u = a @ Wg.T, a @ Wu.T
+        if cap > 0:
+            g, u = cap * np.tanh(g / cap), cap * np.tanh(u / cap)
+        h = g / (1 + np.exp(-g)) * u
+        hb = oracle.bf16_bits_to_f32(res["h_bf16"]).astype(np.float64)
+        assert np.allclose(hb, h, rtol=2 ** -8, atol=1e-30)
+        q = oracle.quantize(fmt, hb.astype(np.float32))
+        assert np.array_equal(q[0], res["hq_codes"]) and np.array_equal(q[1], res["hq_sf"])
+        hdec = oracle.decode(fmt, *q)
+        assert np.allclose(res["y"], hdec @ Wd.T, rtol=1e-12, atol=1e-12)
+
+
+def test_moe_layer_tiny_pipeline_consistency():
+    # the assembled layer on the tiny workload: y of every pair equals the
+    # single-expert FFN, and out is the weighted sum in slot order
+    w = synth.WORKLOADS["tiny_mxfp8"]
+    res = oracle.moe_layer(w)
+    T, k, H = w["T"], w["k"], w["H"]
+    assert res["out"].shape == (T, H)
+    d = res["dispatch"]
+    for t in range(T):
+        acc = np.zeros(H)
+        for j in range(k):
+            acc += res["route"]["w"][t, j] * res["y"][d["pair_pos"][t, j]]
+        assert np.array_equal(acc, res["out"][t])
+    assert np.isfinite(res["out"]).all() and np.abs(res["out"]).max() > 0
+
+
+# ----------------------------------------------------------------------------
+# byte counts of the two encodings against the checkpoint sizes on the pages
+# ----------------------------------------------------------------------------
+
+
+def test_checkpoint_bytes_cross_check():
+    g = read_golden("checkpoint_bytes.txt")
+    L, L4, E = int(g["layers"][0]), int(g["nvfp4_layers"][0]), int(g["experts"][0])
+    H, F = int(g["hidden"][0]), int(g["ffn"][0])
+    total = float(g["total_params"][0])
+    tol = float(g["rel_tol"][0])
+    v = np.random.default_rng(0).standard_normal((4, 256)).astype(np.float32)
+    c4, s4, g4 = oracle.nvfp4_quantize(v, per_tensor=True)
+    c8, s8 = oracle.mxfp8_quantize(v)
+    b4 = (c4.nbytes + s4.nbytes) / v.size       # bytes per parameter
+    b8 = (c8.nbytes + s8.nbytes) / v.size
+    per_expert = 3 * H * F
+    expert_params = L * E * per_expert
+    rest_gb = (total - expert_params) * 2 / 1e9  # everything else in BF16
+    mixed = (L4 * E * per_expert * b4 + (L - L4) * E * per_expert * b8) / 1e9 + rest_gb
+    mx = L * E * per_expert * b8 / 1e9 + rest_gb
+    assert abs(mixed / float(g["ckpt_mixed_gb"][0]) - 1) < tol
+    assert abs(mx / float(g["ckpt_mxfp8_gb"][0]) - 1) < tol
+
+
+# ----------------------------------------------------------------------------
+# the seeded generator (not the method, but both sides rely on it)
+# ----------------------------------------------------------------------------
+
+
+def test_generator_moments_and_bounds():
+    z = synth.normals(123, synth.T_X, 0, 200000).astype(np.float64)
+    assert abs(z.mean()) < 0.01 and abs(z.var() - 1.0) < 0.01
+    assert np.abs(z).max() <= 6.0
+    assert np.array_equal(z, synth.normals(123, synth.T_X, 0, 200000))   # deterministic
+    w = synth.WORKLOADS["decode192_mxfp8_outliers"]
+    flags = synth.outlier_flags(w)
+    assert flags.sum() == 2

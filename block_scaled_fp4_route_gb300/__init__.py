@@ -1,0 +1,189 @@
+"""Routed block-scaled MoE layer for GB300 — Python binding of libmoe.so.
+
+Thin ctypes marshalling over the C ABI in include/moe.h: every function here
+has the name of its C entry point, takes torch tensors (device memory) and
+passes their pointers and the current CUDA stream.  All arithmetic runs in the
+library's CUDA kernels; there is no fallback path: if libmoe.so cannot be
+built or loaded, importing the binding's functions raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+FMT_NVFP4, FMT_MXFP8 = 0, 1
+SCALES_ROWMAJOR, SCALES_TILED = 0, 1
+
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
+          4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_ARCH", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_DEVICE_TIMEOUT"}
+
+EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+            "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
+            "moe_status_string"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
+                ("F", ctypes.c_int), ("fmt", ctypes.c_int), ("swiglu_cap", ctypes.c_float),
+                ("mx_scale_mode", ctypes.c_int), ("bias_in_weights", ctypes.c_int),
+                ("routed_scale", ctypes.c_float)]
+
+
+class moe_qweight(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("global_scale", ctypes.c_void_p)]
+
+
+_LAYOUT_FIELDS = ["status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "pair_pos", "bitmap",
+                  "seg_start", "tiles", "n_row_tiles", "xq_codes", "xq_scales", "xq_global", "h_bf16", "hq_codes",
+                  "hq_scales", "hq_global", "y_perm", "total"]
+
+
+class moe_ws_layout(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int64)] + [(f, ctypes.c_size_t) for f in _LAYOUT_FIELDS]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """Build (if stale) and load libmoe.so; raises if that is not possible."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+            cfgp = ctypes.POINTER(moe_config)
+            qwp = ctypes.POINTER(moe_qweight)
+            L.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(sz)]
+            L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
+            L.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
+            L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, sz, P]
+            L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
+            L.moe_forward.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, sz, P]
+            L.moe_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64, i64, i64, ctypes.c_int,
+                                       P, P, P, P]
+            L.moe_pack_scales.argtypes = [P, i64, i64, P, P]
+            L.moe_poll_device_status.argtypes = [P, P]
+            L.moe_workspace_layout.argtypes = [cfgp, ctypes.POINTER(moe_ws_layout)]
+            L.moe_status_string.argtypes = [ctypes.c_int]
+            L.moe_status_string.restype = ctypes.c_char_p
+            for n in EXPORTED[:-1]:
+                getattr(L, n).restype = ctypes.c_int
+            _lib = L
+        return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise MoeError(fn, st)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def make_config(T, H, E, k, F, fmt, swiglu_cap=10.0, mx_scale_mode=0, bias_in_weights=0, routed_scale=1.0):
+    if isinstance(fmt, str):
+        fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
+    return moe_config(T, H, E, k, F, fmt, swiglu_cap, mx_scale_mode, bias_in_weights, routed_scale)
+
+
+def qweight(codes, scales, global_scale=None) -> moe_qweight:
+    return moe_qweight(_ptr(codes), _ptr(scales), _ptr(global_scale))
+
+
+# ----------------------------------------------------------------------------
+# entry points (names of the C ABI)
+# ----------------------------------------------------------------------------
+
+def moe_workspace_size(cfg: moe_config) -> int:
+    n = ctypes.c_size_t(0)
+    _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def moe_workspace_layout(cfg: moe_config) -> dict:
+    L = moe_ws_layout()
+    _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)))
+    return {f: getattr(L, f) for f in ["R"] + _LAYOUT_FIELDS}
+
+
+def moe_route(cfg, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
+    _check("moe_route", lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
+                                        _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None):
+    _check("moe_dispatch", lib().moe_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
+                                              _ptr(perm), _ptr(pair_pos), _ptr(ws), ws.numel() * ws.element_size(),
+                                              _stream(stream)))
+
+
+def moe_expert_ffn(cfg, x, topk_idx, offsets, perm, pair_pos, gate, up, down, y_perm, ws, stream=None):
+    _check("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(offsets),
+                                                  _ptr(perm), _ptr(pair_pos), ctypes.byref(gate), ctypes.byref(up),
+                                                  ctypes.byref(down), _ptr(y_perm), _ptr(ws),
+                                                  ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_combine(cfg, y_perm, topk_w, pair_pos, out, stream=None):
+    _check("moe_combine", lib().moe_combine(ctypes.byref(cfg), _ptr(y_perm), _ptr(topk_w), _ptr(pair_pos),
+                                            _ptr(out), _stream(stream)))
+
+
+def moe_forward(cfg, x, w_router, bias, gate, up, down, out, ws, stream=None):
+    _check("moe_forward", lib().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
+                                            ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), _ptr(out),
+                                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_quantize(fmt, src, codes, scales, global_scale=None, group_rows=0, layout=SCALES_TILED, mx_scale_mode=0,
+                 stream=None):
+    """src: fp32 or bf16 [rows, cols] (torch, on the device)."""
+    import torch
+    if isinstance(fmt, str):
+        fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
+    rows, cols = src.shape[-2] if src.dim() > 1 else 1, src.shape[-1]
+    rows = src.numel() // cols
+    _check("moe_quantize", lib().moe_quantize(fmt, mx_scale_mode, int(src.dtype == torch.float32), _ptr(src), rows,
+                                              cols, group_rows, layout, _ptr(codes), _ptr(scales),
+                                              _ptr(global_scale), _stream(stream)))
+
+
+def moe_pack_scales(rowmajor, rows, scale_cols, tiled, stream=None):
+    _check("moe_pack_scales", lib().moe_pack_scales(_ptr(rowmajor), rows, scale_cols, _ptr(tiled), _stream(stream)))
+
+
+def moe_poll_device_status(ws, stream=None) -> int:
+    """Synchronises the stream; returns the status code (0 = no timeout)."""
+    return int(lib().moe_poll_device_status(_ptr(ws), _stream(stream)))
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()

@@ -1,0 +1,421 @@
+// C ABI of the MoE layer (include/moe.h): argument validation, workspace
+// layout, TMA descriptors, and the chaining of the kernels on the caller's
+// stream.  Allocates no device memory.
+#include <mutex>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DevInfo {
+  bool probed = false;
+  bool ok = false;
+  int sms = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_mu;
+
+moe_status device_check(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.probed) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.ok = (major == 10 && minor == 3);
+    d.probed = true;
+  }
+  if (!d.ok) return MOE_ERR_ARCH;
+  if (sms) *sms = d.sms;
+  return MOE_OK;
+}
+
+moe_status check_cfg(const moe_config* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->fmt != MOE_FMT_NVFP4 && c->fmt != MOE_FMT_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->T > kMaxT || c->E < 1 || c->E > kMaxE || c->k < 1 || c->k > kMaxK || c->k > c->E)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int q = c->fmt == MOE_FMT_NVFP4 ? 256 : 128;  // one 128-byte TMA box of codes along K
+  if (c->H < q || c->F < q || c->H % q != 0 || c->F % q != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((int64_t)c->T * c->k > (1 << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!(c->swiglu_cap >= 0.0f)) return MOE_ERR_INVALID_ARG;
+  if (c->mx_scale_mode != 0 && c->mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status check_qw(const moe_config* c, const moe_qweight* w) {
+  if (!w || !w->codes || !w->scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->codes) || !aligned16(w->scales)) return MOE_ERR_MISALIGNED;
+  if (c->fmt == MOE_FMT_NVFP4) {
+    if (!w->global_scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w->global_scale)) return MOE_ERR_MISALIGNED;
+  }
+  return MOE_OK;
+}
+
+moe_status check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(p)) return MOE_ERR_MISALIGNED;
+  }
+  return MOE_OK;
+}
+
+moe_status check_ws(const moe_config* c, const void* ws, size_t bytes) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_MISALIGNED;
+  moe_ws_layout L;
+  ws_layout(*c, &L);
+  if (bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+// --- TMA descriptors ---------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D u8 tensor [rows, row_bytes] with 128-byte swizzle, box 128 bytes x box_rows.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+// Expert FFN after the tile plan exists in the workspace.
+moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
+                    const int32_t* perm, const int32_t* pair_pos, const moe_qweight* gate, const moe_qweight* up,
+                    const moe_qweight* down, float* y, void* ws, cudaStream_t st) {
+  moe_ws_layout L;
+  ws_layout(c, &L);
+  const int64_t R = L.R;
+  uint8_t* xq = at<uint8_t>(ws, L.xq_codes);
+  uint8_t* xs = at<uint8_t>(ws, L.xq_scales);
+  float* xg = at<float>(ws, L.xq_global);
+  __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h_bf16);
+  uint8_t* hq = at<uint8_t>(ws, L.hq_codes);
+  uint8_t* hs = at<uint8_t>(ws, L.hq_scales);
+  float* hg = at<float>(ws, L.hq_global);
+  const int32_t* seg = at<int32_t>(ws, L.seg_start);
+  const RowTile* tiles = at<RowTile>(ws, L.tiles);
+  const int32_t* nrt = at<int32_t>(ws, L.n_row_tiles);
+  uint32_t* status = at<uint32_t>(ws, L.status);
+
+  cudaError_t e = launch_quant_x(c, x, idx, offsets, pair_pos, seg, xq, xs, xg, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  const int64_t hb = code_bytes(c.fmt, c.H), fb = code_bytes(c.fmt, c.F);
+  CUtensorMap mg, mu, md, mx, mh;
+  if (!make_map(&mg, gate->codes, (int64_t)c.E * c.F, hb, 128) ||
+      !make_map(&mu, up->codes, (int64_t)c.E * c.F, hb, 128) ||
+      !make_map(&md, down->codes, (int64_t)c.E * c.H, fb, 128) || !make_map(&mx, xq, R, hb, 16) ||
+      !make_map(&mh, hq, R, fb, 16))
+    return MOE_ERR_CUDA;
+
+  GemmLaunch g1{};
+  g1.cfg = &c;
+  g1.gated = true;
+  g1.tmA0 = &mg;
+  g1.tmA1 = &mu;
+  g1.tmB = &mx;
+  g1.sfA0 = (const uint8_t*)gate->scales;
+  g1.sfA1 = (const uint8_t*)up->scales;
+  g1.sfB = xs;
+  g1.gA0 = gate->global_scale;
+  g1.gA1 = up->global_scale;
+  g1.gB = xg;
+  g1.tiles = tiles;
+  g1.n_row_tiles = nrt;
+  g1.NA = c.F;
+  g1.K = c.H;
+  g1.h_out = h;
+  g1.status = status;
+  g1.num_sms = sms;
+  if (launch_gemm(g1, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmLaunch g2{};
+  g2.cfg = &c;
+  g2.gated = false;
+  g2.tmA0 = &md;
+  g2.tmA1 = &md;
+  g2.tmB = &mh;
+  g2.sfA0 = (const uint8_t*)down->scales;
+  g2.sfB = hs;
+  g2.gA0 = down->global_scale;
+  g2.gB = hg;
+  g2.tiles = tiles;
+  g2.n_row_tiles = nrt;
+  g2.NA = c.H;
+  g2.K = c.F;
+  g2.y_out = y;
+  g2.status = status;
+  g2.num_sms = sms;
+  if (launch_gemm(g2, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+void ws_layout(const moe_config& c, moe_ws_layout* L) {
+  const int64_t T = c.T, E = c.E, P = T * c.k, R = padded_rows(c), W = (T + 31) / 32;
+  const int bs = block_elems(c.fmt);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 1024);
+    return o;
+  };
+  L->R = R;
+  L->status = take(256);
+  L->logits = take((size_t)router_splits(c) * T * E * 4);
+  L->topk_idx = take(P * 4);
+  L->topk_w = take(P * 4);
+  L->counts = take(E * 4);
+  L->offsets = take((E + 1) * 4);
+  L->perm = take(P * 4);
+  L->pair_pos = take(P * 4);
+  L->bitmap = take(E * W * 4);
+  L->seg_start = take((E + 1) * 4);
+  L->tiles = take(max_row_tiles(c) * sizeof(RowTile));
+  L->n_row_tiles = take(16);
+  L->xq_codes = take(R * code_bytes(c.fmt, c.H));
+  L->xq_scales = take(R * (c.H / bs));
+  L->xq_global = take(R * 4);
+  L->h_bf16 = take(R * c.F * 2);
+  L->hq_codes = take(R * code_bytes(c.fmt, c.F));
+  L->hq_scales = take(R * (c.F / bs));
+  L->hq_global = take(R * 4);
+  L->y_perm = take(P * c.H * 4);
+  L->total = off;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_ws_layout L;
+  ws_layout(*cfg, &L);
+  *bytes = L.total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_layout(const moe_config* cfg, moe_ws_layout* layout) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!layout) return MOE_ERR_INVALID_ARG;
+  ws_layout(*cfg, layout);
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_config* cfg, const void* x_dev, const void* w_router_dev, const float* bias_dev,
+                     int32_t* topk_idx_dev, float* topk_w_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK) s = check_ptrs({x_dev, w_router_dev, bias_dev, topk_idx_dev, topk_w_dev});
+  if (s == MOE_OK) s = check_ws(cfg, ws_dev, ws_bytes);
+  if (s == MOE_OK) s = device_check(nullptr);
+  if (s != MOE_OK) return s;
+  moe_ws_layout L;
+  ws_layout(*cfg, &L);
+  return cuda_status(launch_router(*cfg, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
+                                   at<float>(ws_dev, L.logits), topk_idx_dev, topk_w_dev, (cudaStream_t)stream));
+}
+
+moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int32_t* counts_dev, int32_t* offsets_dev,
+                        int32_t* perm_dev, int32_t* pair_pos_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK) s = check_ptrs({topk_idx_dev, counts_dev, offsets_dev, perm_dev, pair_pos_dev});
+  if (s == MOE_OK) s = check_ws(cfg, ws_dev, ws_bytes);
+  if (s == MOE_OK) s = device_check(nullptr);
+  if (s != MOE_OK) return s;
+  moe_ws_layout L;
+  ws_layout(*cfg, &L);
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
+  if (launch_dispatch(*cfg, topk_idx_dev, counts_dev, offsets_dev, perm_dev, pair_pos_dev, bm, st) != cudaSuccess ||
+      launch_scan_plan(*cfg, counts_dev, nullptr, offsets_dev, at<int32_t>(ws_dev, L.seg_start),
+                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.n_row_tiles), nullptr, st) != cudaSuccess ||
+      launch_dispatch_scatter(*cfg, topk_idx_dev, bm, offsets_dev, perm_dev, pair_pos_dev, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
+                          const int32_t* offsets_dev, const int32_t* perm_dev, const int32_t* pair_pos_dev,
+                          const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down, float* y_perm_dev,
+                          void* ws_dev, size_t ws_bytes, void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK) s = check_ptrs({x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, y_perm_dev});
+  if (s == MOE_OK) s = check_qw(cfg, gate);
+  if (s == MOE_OK) s = check_qw(cfg, up);
+  if (s == MOE_OK) s = check_qw(cfg, down);
+  if (s == MOE_OK) s = check_ws(cfg, ws_dev, ws_bytes);
+  int sms = 0;
+  if (s == MOE_OK) s = device_check(&sms);
+  if (s != MOE_OK) return s;
+  moe_ws_layout L;
+  ws_layout(*cfg, &L);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (launch_scan_plan(*cfg, nullptr, offsets_dev, nullptr, at<int32_t>(ws_dev, L.seg_start),
+                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.n_row_tiles),
+                       at<uint32_t>(ws_dev, L.status), st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return ffn_core(*cfg, sms, (const __nv_bfloat16*)x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, gate, up,
+                  down, y_perm_dev, ws_dev, st);
+}
+
+moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const float* topk_w_dev,
+                       const int32_t* pair_pos_dev, void* out_dev, void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK) s = check_ptrs({y_perm_dev, topk_w_dev, pair_pos_dev, out_dev});
+  if (s == MOE_OK) s = device_check(nullptr);
+  if (s != MOE_OK) return s;
+  return cuda_status(
+      launch_combine(*cfg, y_perm_dev, topk_w_dev, pair_pos_dev, (__nv_bfloat16*)out_dev, (cudaStream_t)stream));
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev, const float* bias_dev,
+                       const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down, void* out_dev,
+                       void* ws_dev, size_t ws_bytes, void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK) s = check_ptrs({x_dev, w_router_dev, bias_dev, out_dev});
+  if (s == MOE_OK) s = check_qw(cfg, gate);
+  if (s == MOE_OK) s = check_qw(cfg, up);
+  if (s == MOE_OK) s = check_qw(cfg, down);
+  if (s == MOE_OK) s = check_ws(cfg, ws_dev, ws_bytes);
+  int sms = 0;
+  if (s == MOE_OK) s = device_check(&sms);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  moe_ws_layout L;
+  ws_layout(c, &L);
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* idx = at<int32_t>(ws_dev, L.topk_idx);
+  float* w = at<float>(ws_dev, L.topk_w);
+  int32_t* counts = at<int32_t>(ws_dev, L.counts);
+  int32_t* offsets = at<int32_t>(ws_dev, L.offsets);
+  int32_t* perm = at<int32_t>(ws_dev, L.perm);
+  int32_t* pair_pos = at<int32_t>(ws_dev, L.pair_pos);
+  uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
+  float* y = at<float>(ws_dev, L.y_perm);
+  if (launch_router(c, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
+                    at<float>(ws_dev, L.logits), idx, w, st) != cudaSuccess ||
+      launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st) != cudaSuccess ||
+      launch_scan_plan(c, counts, nullptr, offsets, at<int32_t>(ws_dev, L.seg_start), at<RowTile>(ws_dev, L.tiles),
+                       at<int32_t>(ws_dev, L.n_row_tiles), at<uint32_t>(ws_dev, L.status), st) != cudaSuccess ||
+      launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st));
+}
+
+moe_status moe_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32, const void* src_dev, int64_t rows,
+                        int64_t cols, int64_t group_rows, moe_scale_layout layout, void* codes_dev, void* scales_dev,
+                        float* global_dev, void* stream) {
+  if (fmt != MOE_FMT_NVFP4 && fmt != MOE_FMT_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (mx_scale_mode != 0 && mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;
+  if (layout != MOE_SCALES_ROWMAJOR && layout != MOE_SCALES_TILED) return MOE_ERR_INVALID_ARG;
+  const int bs = fmt == MOE_FMT_NVFP4 ? 16 : 32;
+  if (rows < 1 || rows > (int64_t)INT32_MAX || cols < bs || cols % bs != 0 || cols > (1 << 20))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (src_is_fp32 ? (cols % 4) : (cols % 8)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (layout == MOE_SCALES_TILED && (rows % 128 != 0 || (cols / bs) % 4 != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (fmt == MOE_FMT_NVFP4) {
+    if (group_rows < 0 || (group_rows > 0 && rows % group_rows != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    moe_status s = check_ptrs({src_dev, codes_dev, scales_dev, global_dev});
+    if (s != MOE_OK) return s;
+  } else {
+    moe_status s = check_ptrs({src_dev, codes_dev, scales_dev});
+    if (s != MOE_OK) return s;
+  }
+  moe_status s = device_check(nullptr);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_quantize(fmt, mx_scale_mode, src_is_fp32, src_dev, rows, cols, group_rows, layout,
+                                     (uint8_t*)codes_dev, (uint8_t*)scales_dev, global_dev, nullptr,
+                                     (cudaStream_t)stream));
+}
+
+moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64_t scale_cols, void* tiled_dev, void* stream) {
+  if (rows < 1 || rows % 128 != 0 || scale_cols < 4 || scale_cols % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status s = check_ptrs({rowmajor_dev, tiled_dev});
+  if (s == MOE_OK) s = device_check(nullptr);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_pack_scales((const uint8_t*)rowmajor_dev, rows, scale_cols, (uint8_t*)tiled_dev,
+                                        (cudaStream_t)stream));
+}
+
+moe_status moe_poll_device_status(void* ws_dev, void* stream) {
+  if (!ws_dev) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws_dev, sizeof(v), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    if (cudaMemsetAsync(ws_dev, 0, sizeof(v), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_ERR_DEVICE_TIMEOUT;
+  }
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait ran out";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

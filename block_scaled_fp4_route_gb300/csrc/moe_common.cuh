@@ -1,0 +1,273 @@
+// Shared device helpers of the MoE library: PTX wrappers for mbarrier, TMA
+// (cp.async.bulk[.tensor]) and the 5th-generation tensor core (tcgen05), the
+// block-scale TILED layout, and bit-exact E2M1 / E4M3 / E8M0 encoders.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// ----------------------------------------------------------------------------
+// status word bits written by kernels whose bounded waits ran out
+// ----------------------------------------------------------------------------
+enum : uint32_t {
+  ST_TIMEOUT_PRODUCER = 1u << 0,
+  ST_TIMEOUT_MMA = 1u << 1,
+  ST_TIMEOUT_EPILOGUE = 1u << 2,
+  ST_TIMEOUT_DRAIN = 1u << 3,
+};
+
+// ----------------------------------------------------------------------------
+// TILED block-scale layout (see moe.h): 512-byte atoms of 128 rows x 4 scale
+// columns; inside an atom row r sits at lane r%32, 4-byte word (r/32)%4.
+// ----------------------------------------------------------------------------
+__host__ __device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t c, int64_t C) {
+  return ((r >> 7) * (C >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
+}
+
+// ----------------------------------------------------------------------------
+// number formats (round to nearest even, saturate to the largest finite,
+// the sign bit follows the input also for zero)
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ float exp2i(int n) {  // 2^n, n in [-127, 127], exact
+  return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ uint32_t e2m1_encode(float v) {
+  uint32_t sign = (__float_as_uint(v) >> 31) << 3;
+  float a = fabsf(v);
+  uint32_t q;
+  if (a <= 0.25f) q = 0;        // midpoint 0.25 goes to code 0 (even)
+  else if (a < 0.75f) q = 1;    // 0.5
+  else if (a <= 1.25f) q = 2;   // 1.0 (0.75 and 1.25 are ties to code 2)
+  else if (a < 1.75f) q = 3;    // 1.5
+  else if (a <= 2.5f) q = 4;    // 2.0 (1.75, 2.5 ties to code 4)
+  else if (a < 3.5f) q = 5;     // 3.0
+  else if (a <= 5.0f) q = 6;    // 4.0 (3.5, 5 ties to code 6)
+  else q = 7;                   // 6.0, saturating (also NaN)
+  return sign | q;
+}
+
+__device__ __forceinline__ uint32_t e4m3_encode(float v) {
+  uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
+  float a = fabsf(v);
+  if (!(a < 448.0f)) return sign | 0x7Eu;
+  int e = (int)(__float_as_uint(a) >> 23) - 127;
+  if (e < -6) {  // E4M3 subnormal range: quantum 2^-9
+    uint32_t q = __float2uint_rn(__fmul_rn(a, 512.0f));
+    return sign | q;  // q == 8 encodes the smallest normal 0x08
+  }
+  uint32_t m = __float2uint_rn(__fmul_rn(a, exp2i(3 - e)));  // in [8, 16]
+  if (m == 16) { m = 8; e += 1; }
+  return sign | ((uint32_t)(e + 7) << 3) | (m - 8);
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  uint32_t e = (c >> 3) & 15, m = c & 7;
+  float v = (e == 0) ? (float)m * 0.001953125f : __uint_as_float(((e + 120) << 23) | (m << 20));
+  return (c & 0x80u) ? -v : v;
+}
+
+// floor(log2 a) for a finite a > 0, exact from the bits.
+__device__ __forceinline__ int ilog2_floor(float a) {
+  uint32_t b = __float_as_uint(a);
+  int ef = (int)(b >> 23);
+  if (ef > 0) return ef - 127;
+  uint32_t m = b & 0x7FFFFFu;
+  return (31 - __clz(m)) - 149;
+}
+
+__device__ __forceinline__ int ilog2_ceil(float a) {
+  uint32_t b = __float_as_uint(a);
+  int ef = (int)(b >> 23);
+  uint32_t m = b & 0x7FFFFFu;
+  if (ef > 0) return ef - 127 + (m != 0);
+  int p = 31 - __clz(m);
+  return p - 149 + (m != (1u << p));
+}
+
+// E8M0 scale byte of one MXFP8 block with absolute maximum amax_b > 0.
+__device__ __forceinline__ uint32_t mx_scale_code(float amax_b, int mode) {
+  int e = (mode == 0) ? ilog2_floor(amax_b) - 8 : ilog2_ceil(__fdiv_rn(amax_b, 448.0f));
+  int s = e + 127;
+  s = s < 0 ? 0 : (s > 254 ? 254 : s);
+  return (uint32_t)s;
+}
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete, for at most `limit` cycles.
+// Returns false (and raises *abort, ORs `code` into *status) if it ran out or
+// if another role has already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status, uint32_t code, long long limit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > limit) {
+        *abort_flag = 1;
+        atomicOr(status, code);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2D tiled TMA load into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"((uint64_t)src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// --- tcgen05 ---------------------------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread
+// has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+// Copy 32 rows x 16 bytes of shared memory into TMEM lanes 0..31 (replicated
+// to all four lane quadrants), 4 columns starting at `taddr`.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D(tmem) (+)= A(smem) * B(smem)^T with NVFP4 operands (E2M1, UE4M3 scale per
+// 16 elements, K = 64 per instruction).
+__device__ __forceinline__ void mma_nvfp4(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
+          d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// Same for MXFP8 operands (E4M3, UE8M0 scale per 32 elements, K = 32).
+__device__ __forceinline__ void mma_mxfp8(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(
+          d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns of TMEM into registers.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major, 128-byte swizzle,
+// rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: next 8-row group
+  d |= (uint64_t)1 << 46;            // descriptor version
+  d |= (uint64_t)2 << 61;            // SWIZZLE_128B
+  return d;
+}
+// Descriptor of a 512-byte scale atom (32 rows x 16 bytes, no swizzle) for
+// tcgen05.cp.  Only one 16-byte column, so both byte offsets may be 128.
+__device__ __forceinline__ uint64_t sdesc_atom(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128 >> 4) << 16;
+  d |= (uint64_t)(128 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptors (M = 128, K-major A and B, dense).
+__device__ __forceinline__ uint32_t idesc_nvfp4(uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (0u << 23) | ((128u >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_mxfp8(uint32_t N, uint32_t sf_id) {
+  return (sf_id << 4) | (0u << 7) | (0u << 10) | ((N >> 3) << 17) | (1u << 23) | ((128u >> 4) << 24) |
+         (sf_id << 29);
+}
+
+}  // namespace moe

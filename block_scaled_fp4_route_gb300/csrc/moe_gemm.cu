@@ -1,0 +1,323 @@
+// Persistent grouped expert GEMM on block-scaled tensor cores (tcgen05).
+//
+// TokenSpeed page on Inkling 2 Small (section on serving on NVIDIA
+// Blackwell): the expert GEMMs run directly on block-scaled tensor cores.
+// Cookbook page, MegaMoE paragraph: the two expert GEMMs with the capped
+// SwiGLU between them.  Both formats of the checkpoint are covered: NVFP4
+// (kind::mxf4nvf4, E2M1 x E2M1 with UE4M3 scales per 16) and MXFP8
+// (kind::mxf8f6f4, E4M3 x E4M3 with UE8M0 scales per 32).
+//
+// Tile = 128 weight rows (MMA M) x up to 128 token rows of one expert (MMA N,
+// rounded up to 16) x the full K, "swap-AB": the weights fill M so that a
+// decode batch with one or two tokens per expert wastes no weight bytes.
+//   GEMM1 (gated):  A0 = W_gate rows, A1 = W_up rows (two accumulators),
+//                   epilogue h = bf16(silu(cap g) * cap u)
+//   GEMM2:          A0 = W_down rows, epilogue y = acc * g_w * g_h (fp32)
+// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
+// warp 2 = TMEM allocator, warps 4..7 = epilogue (TMEM lane quadrants 0..3).
+// Every mbarrier wait is bounded; a wait that runs out sets a status bit in
+// global memory and every role leaves its loop, waits for its own copies in
+// flight, and the CTA frees its TMEM.
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+
+template <int FMT, bool GATED>
+struct Cfg {
+  static constexpr int NA = GATED ? 2 : 1;
+  static constexpr int STAGES = GATED ? 4 : 6;
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = 128 * 128;
+  static constexpr int SF_ATOMS = FMT == MOE_FMT_NVFP4 ? 4 : 1;  // 512-byte atoms per operand per stage
+  static constexpr int SF_BYTES = SF_ATOMS * 512;
+  static constexpr int RAW_STAGE = NA * A_BYTES + B_BYTES + (NA + 1) * SF_BYTES;
+  static constexpr int STAGE_BYTES = (RAW_STAGE + 1023) / 1024 * 1024;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int ELEMS_PER_STAGE = FMT == MOE_FMT_NVFP4 ? 256 : 128;  // 128 bytes of codes
+  static constexpr int BLOCK = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  static constexpr int ACC_COLS = 128;
+  static constexpr int SF_COLS_OP = SF_ATOMS * 4;
+  static constexpr int SF_COLS_STAGE = (NA + 1) * SF_COLS_OP;
+  static constexpr int TMEM_SF = NA * ACC_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(TMEM_SF + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(16 * STAGES + 40 <= BAR_BYTES, "barrier area");
+};
+
+struct GemmArgs {
+  const uint8_t* sfA0;
+  const uint8_t* sfA1;
+  const uint8_t* sfB;
+  const float* gA0;
+  const float* gA1;
+  const float* gB;
+  const RowTile* tiles;
+  const int32_t* n_row_tiles;
+  int NA;  // weight rows per expert (= output features; also the output row stride)
+  int K;   // reduction length in elements
+  float cap;
+  __nv_bfloat16* h_out;
+  float* y_out;
+  uint32_t* status;
+  long long limit;
+};
+
+template <int FMT, bool GATED>
+__global__ void __launch_bounds__(256, 1)
+    k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+               const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+  using C = Cfg<FMT, GATED>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tmem_full = empty + C::STAGES;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain = tmem_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA0);
+    if (GATED) prefetch_tmap(&tmA1);
+    prefetch_tmap(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int MT = a.NA / 128;
+  const int total = (*a.n_row_tiles) * MT;
+  const int KB = a.K / C::ELEMS_PER_STAGE;
+  const int64_t atoms_per_rowblock = (a.K / C::BLOCK) / 4;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arming
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const RowTile rt = a.tiles[t / MT];
+        const int mt = t % MT;
+        const int N = (rt.n_valid + 15) & ~15;
+        const int arow = rt.e * a.NA + mt * 128;
+        const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_rowblock * 512;
+        const uint8_t* sfa1 = GATED ? a.sfA1 + (int64_t)(arow >> 7) * atoms_per_rowblock * 512 : nullptr;
+        const uint8_t* sfb = a.sfB + (int64_t)(rt.row >> 7) * atoms_per_rowblock * 512;
+        const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sbase = smem + stage * C::STAGE_BYTES;
+          uint8_t* sB = sbase + C::NA * C::A_BYTES;
+          uint8_t* sSF = sB + C::B_BYTES;
+          mbar_expect_tx(&full[stage], bytes);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(sbase, &tmA0, &full[stage], kb * 128, arow);
+          if (GATED) tma_load_2d(sbase + C::A_BYTES, &tmA1, &full[stage], kb * 128, arow);
+          for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
+          bulk_load(sSF, sfa0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          if (GATED) bulk_load(sSF + C::SF_BYTES, sfa1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          bulk_load(sSF + C::NA * C::SF_BYTES, sfb + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        // wait (bounded) for the copies this thread put in flight
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (!((armed >> s) & 1u)) continue;
+          uint32_t par = (armed_par >> s) & 1u;
+          long long t0 = clock64();
+          while (!mbar_try_wait(&full[s], par) && clock64() - t0 < a.limit) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        const RowTile rt = a.tiles[t / MT];
+        const uint32_t N = (uint32_t)((rt.n_valid + 15) & ~15);
+        if (!mbar_wait(tmem_empty, acc_phase ^ 1, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* sbase = smem + stage * C::STAGE_BYTES;
+          uint8_t* sB = sbase + C::NA * C::A_BYTES;
+          uint8_t* sSF = sB + C::B_BYTES;
+          const uint32_t sf_t = tmem + C::TMEM_SF + stage * C::SF_COLS_STAGE;
+#pragma unroll
+          for (int op = 0; op < C::NA + 1; ++op)
+#pragma unroll
+            for (int at = 0; at < C::SF_ATOMS; ++at)
+              tc_cp_32x128b_x4(sf_t + op * C::SF_COLS_OP + at * 4,
+                               sdesc_atom(smem_u32(sSF + op * C::SF_BYTES + at * 512)));
+          const uint64_t da0 = sdesc_sw128(smem_u32(sbase));
+          const uint64_t da1 = sdesc_sw128(smem_u32(sbase + C::A_BYTES));
+          const uint64_t db = sdesc_sw128(smem_u32(sB));
+          const uint32_t sfb_t = sf_t + C::NA * C::SF_COLS_OP;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint32_t accum = (kb | s) != 0;
+            const uint64_t koff = (uint64_t)((s * 32) >> 4);
+            if constexpr (FMT == MOE_FMT_NVFP4) {
+              const uint32_t id = idesc_nvfp4(N);
+              mma_nvfp4(tmem, da0 + koff, db + koff, id, sf_t + 4 * s, sfb_t + 4 * s, accum);
+              if constexpr (GATED)
+                mma_nvfp4(tmem + C::ACC_COLS, da1 + koff, db + koff, id, sf_t + C::SF_COLS_OP + 4 * s, sfb_t + 4 * s,
+                          accum);
+            } else {
+              const uint32_t id = idesc_mxfp8(N, (uint32_t)s);
+              mma_mxfp8(tmem, da0 + koff, db + koff, id, sf_t, sfb_t, accum);
+              if constexpr (GATED) mma_mxfp8(tmem + C::ACC_COLS, da1 + koff, db + koff, id, sf_t + C::SF_COLS_OP, sfb_t, accum);
+            }
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tmem_full);
+        acc_phase ^= 1;
+      }
+      // every tcgen05 operation of this thread has completed before TMEM is freed
+      tc_commit(drain);
+      long long t0 = clock64();
+      while (!mbar_try_wait(drain, 0) && clock64() - t0 < a.limit) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      if (!mbar_wait(tmem_full, acc_phase, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
+      tc_fence_after();
+      const RowTile rt = a.tiles[t / MT];
+      const int mt = t % MT;
+      const int f = mt * 128 + q * 32 + lane;
+      float sA0 = 1.0f, sA1 = 1.0f;
+      if constexpr (FMT == MOE_FMT_NVFP4) {
+        sA0 = a.gA0[rt.e];
+        if constexpr (GATED) sA1 = a.gA1[rt.e];
+      }
+      for (int c0 = 0; c0 < rt.n_valid; c0 += 16) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(tq + c0, r0);
+        if constexpr (GATED) tmem_ld16(tq + C::ACC_COLS + c0, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = c0 + j;
+          if (n < rt.n_valid) {
+            const int64_t row = (int64_t)rt.row + n;
+            float gb = 1.0f;
+            if constexpr (FMT == MOE_FMT_NVFP4) gb = a.gB[row];
+            if constexpr (GATED) {
+              float g = __uint_as_float(r0[j]) * (sA0 * gb);
+              float u = __uint_as_float(r1[j]) * (sA1 * gb);
+              if (a.cap > 0.0f) {
+                g = a.cap * tanhf(g / a.cap);
+                u = a.cap * tanhf(u / a.cap);
+              }
+              const float h = g / (1.0f + expf(-g)) * u;
+              a.h_out[row * a.NA + f] = __float2bfloat16_rn(h);
+            } else {
+              a.y_out[(int64_t)(rt.canon + n) * a.NA + f] = __uint_as_float(r0[j]) * (sA0 * gb);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      acc_phase ^= 1;
+    }
+  }
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int FMT, bool GATED>
+cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st) {
+  using C = Cfg<FMT, GATED>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  GemmArgs a;
+  a.sfA0 = g.sfA0;
+  a.sfA1 = g.sfA1;
+  a.sfB = g.sfB;
+  a.gA0 = g.gA0;
+  a.gA1 = g.gA1;
+  a.gB = g.gB;
+  a.tiles = g.tiles;
+  a.n_row_tiles = g.n_row_tiles;
+  a.NA = g.NA;
+  a.K = g.K;
+  a.cap = g.cfg->swiglu_cap;
+  a.h_out = g.h_out;
+  a.y_out = g.y_out;
+  a.status = g.status;
+  a.limit = 4000000000LL;  // ~2 s of SM clock
+  k_moe_gemm<FMT, GATED><<<g.num_sms, 256, C::SMEM, st>>>(*g.tmA0, GATED ? *g.tmA1 : *g.tmA0, *g.tmB, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st) {
+  if (g.cfg->fmt == MOE_FMT_NVFP4) return g.gated ? launch_t<MOE_FMT_NVFP4, true>(g, st) : launch_t<MOE_FMT_NVFP4, false>(g, st);
+  return g.gated ? launch_t<MOE_FMT_MXFP8, true>(g, st) : launch_t<MOE_FMT_MXFP8, false>(g, st);
+}
+
+}  // namespace moe

@@ -1,0 +1,96 @@
+// Internal (non-ABI) declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// One block of up to 128 consecutive rows of one expert in padded row order.
+struct RowTile {
+  int e;        // expert
+  int row;      // first padded row (multiple of 128)
+  int n_valid;  // valid rows in the tile (1..128)
+  int canon;    // first canonical pair position (offsets[e] + 128*i)
+};
+
+constexpr int kTileRows = 128;     // rows of A (weights) per MMA tile, and max rows of B
+constexpr int kMaxE = 1024;
+constexpr int kMaxT = 65536;
+constexpr int kMaxK = 32;
+
+inline int block_elems(moe_format f) { return f == MOE_FMT_NVFP4 ? 16 : 32; }
+inline int64_t code_bytes(moe_format f, int64_t K) { return f == MOE_FMT_NVFP4 ? K / 2 : K; }
+
+// Padded row capacity of the expert-grouped activation buffers.
+inline int64_t padded_rows(const moe_config& c) {
+  int64_t P = (int64_t)c.T * c.k;
+  return ((P + 127) / 128 + c.E) * 128;
+}
+inline int64_t max_row_tiles(const moe_config& c) { return padded_rows(c) / 128; }
+
+void ws_layout(const moe_config& c, moe_ws_layout* L);
+
+// --- launches (all return cudaGetLastError() of their launches) -------------
+cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr,
+                          const float* bias, float* logits, int32_t* idx, float* w, cudaStream_t st);
+
+int router_splits(const moe_config& c);
+
+// bitmap [E, ceil(T/32)] and counts [E]
+cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st);
+cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
+                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st);
+// counts (or offsets_in when counts == nullptr) -> offsets_out (optional),
+// seg_start [E+1], tiles, n_row_tiles; zeroes *status when given
+cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
+                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* n_row_tiles,
+                             uint32_t* status, cudaStream_t st);
+
+cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx,
+                           const int32_t* offsets, const int32_t* pair_pos, const int32_t* seg_start,
+                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st);
+
+cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx,
+                           const int32_t* offsets, const int32_t* perm, const int32_t* seg_start,
+                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st);
+
+cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows,
+                            int64_t cols, int64_t group_rows, moe_scale_layout layout, uint8_t* codes,
+                            uint8_t* scales, float* glob, float* amax_scratch, cudaStream_t st);
+
+cudaError_t launch_pack_scales(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst, cudaStream_t st);
+
+struct GemmLaunch {
+  const moe_config* cfg;
+  bool gated;          // GEMM1 (gate+up, SwiGLU epilogue) vs GEMM2 (down)
+  const CUtensorMap* tmA0;
+  const CUtensorMap* tmA1;
+  const CUtensorMap* tmB;
+  const uint8_t* sfA0;
+  const uint8_t* sfA1;
+  const uint8_t* sfB;
+  const float* gA0;
+  const float* gA1;
+  const float* gB;
+  const RowTile* tiles;
+  const int32_t* n_row_tiles;
+  int NA;              // rows of A per expert
+  int K;               // reduction length (elements)
+  __nv_bfloat16* h_out;   // gated: [R, F]
+  float* y_out;           // down:  [P, H]
+  uint32_t* status;
+  int num_sms;
+};
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
+
+cudaError_t launch_combine(const moe_config& c, const float* y, const float* w, const int32_t* pair_pos,
+                           __nv_bfloat16* out, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,332 @@
+// Block quantisers: NVFP4 (E2M1 codes, E4M3 scale per 16, fp32 global) and
+// MXFP8 (E4M3 codes, E8M0 scale per 32).  Every arithmetic step is a single
+// correctly rounded fp32 operation (__fdiv_rn / __fmul_rn), so the codes are
+// reproducible bit for bit.
+//
+// Three uses:
+//   - x:   one token row per CTA, written to each of its k expert-grouped rows
+//          (the GEMM1 B operand).  The activation is quantised once per token,
+//          over the full hidden width, as the NVFP4 activation scales of an
+//          expert must span its whole input (cookbook, Parallelism paragraph).
+//   - h:   one pair row per CTA (the GEMM2 B operand), global over F.
+//   - API: moe_quantize (weights with one global per expert matrix).
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kQThreads = 256;
+
+__device__ __forceinline__ void load_block_bf16(const __nv_bfloat16* p, int n, float* v) {
+  const uint4* q = reinterpret_cast<const uint4*>(p);
+  for (int i = 0; i < n / 8; ++i) {
+    uint4 u = q[i];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    for (int j = 0; j < 4; ++j) {
+      v[i * 8 + 2 * j] = __uint_as_float(w[j] << 16);
+      v[i * 8 + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+__device__ __forceinline__ void load_block_f32(const float* p, int n, float* v) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+  for (int i = 0; i < n / 4; ++i) {
+    float4 f = q[i];
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+}
+
+template <typename Src>
+__device__ __forceinline__ void load_block(const Src* p, int n, float* v);
+template <>
+__device__ __forceinline__ void load_block<__nv_bfloat16>(const __nv_bfloat16* p, int n, float* v) {
+  load_block_bf16(p, n, v);
+}
+template <>
+__device__ __forceinline__ void load_block<float>(const float* p, int n, float* v) {
+  load_block_f32(p, n, v);
+}
+
+// NVFP4 block of 16: returns the scale byte, writes 8 code bytes.
+__device__ __forceinline__ uint32_t nvfp4_block(const float* v, float G, uint2* codes_out) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  float t = __fdiv_rn(amax, 6.0f);
+  t = __fmul_rn(t, G);
+  uint32_t sb = e4m3_encode(t);
+  uint32_t lo = 0, hi = 0;
+  if (sb != 0) {
+    float inv = __fdiv_rn(G, e4m3_value(sb));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) lo |= e2m1_encode(__fmul_rn(v[i], inv)) << (4 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hi |= e2m1_encode(__fmul_rn(v[8 + i], inv)) << (4 * i);
+  }
+  *codes_out = make_uint2(lo, hi);
+  return sb;
+}
+
+// MXFP8 block of 32: returns the E8M0 byte, writes 32 code bytes.
+__device__ __forceinline__ uint32_t mxfp8_block(const float* v, int mode, uint4* codes_out) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  uint32_t s = 0;
+  if (amax != 0.0f) {
+    s = mx_scale_code(amax, mode);
+    float mul = exp2i(127 - (int)s);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i / 4] |= e4m3_encode(__fmul_rn(v[i], mul)) << (8 * (i % 4));
+  }
+  codes_out[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  codes_out[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return s;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float m = 0.0f;
+  for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+template <typename Src>
+__device__ float row_absmax(const Src* row, int K, float* red) {
+  float m = 0.0f;
+  for (int i = threadIdx.x; i < K; i += blockDim.x) {
+    float v;
+    if constexpr (sizeof(Src) == 2) v = __bfloat162float(row[i]);
+    else v = row[i];
+    m = fmaxf(m, fabsf(v));
+  }
+  return block_max(m, red);
+}
+
+__device__ __forceinline__ float nvfp4_G(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(2688.0f, amax); }
+
+// Quantise one row (K elements) to up to `ndst` destination rows.
+template <int FMT, typename Src>
+__device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst, const int64_t* dst_rows,
+                          uint8_t* codes, uint8_t* scales, bool tiled, int64_t scale_cols) {
+  constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  const int nb = K / BS;
+  const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) {
+    float v[BS];
+    load_block<Src>(row + (int64_t)b * BS, BS, v);
+    if constexpr (FMT == MOE_FMT_NVFP4) {
+      uint2 c;
+      uint32_t s = nvfp4_block(v, G, &c);
+      for (int d = 0; d < ndst; ++d) {
+        int64_t r = dst_rows[d];
+        *reinterpret_cast<uint2*>(codes + r * cbytes + (int64_t)b * 8) = c;
+        scales[tiled ? tiled_scale_offset(r, b, scale_cols) : r * scale_cols + b] = (uint8_t)s;
+      }
+    } else {
+      uint4 c[2];
+      uint32_t s = mxfp8_block(v, mx_mode, c);
+      for (int d = 0; d < ndst; ++d) {
+        int64_t r = dst_rows[d];
+        uint4* o = reinterpret_cast<uint4*>(codes + r * cbytes + (int64_t)b * 32);
+        o[0] = c[0];
+        o[1] = c[1];
+        scales[tiled ? tiled_scale_offset(r, b, scale_cols) : r * scale_cols + b] = (uint8_t)s;
+      }
+    }
+  }
+}
+
+// x: one CTA per token; written to the k expert-grouped rows of the token.
+template <int FMT>
+__global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __restrict__ x, int H, int k,
+                                                       int mx_mode, const int32_t* __restrict__ idx,
+                                                       const int32_t* __restrict__ offsets,
+                                                       const int32_t* __restrict__ pair_pos,
+                                                       const int32_t* __restrict__ seg_start, uint8_t* codes,
+                                                       uint8_t* scales, float* glob) {
+  __shared__ float red[32];
+  __shared__ int64_t dst[kMaxK];
+  const int t = blockIdx.x;
+  const __nv_bfloat16* row = x + (int64_t)t * H;
+  if (threadIdx.x < k) {
+    int pid = t * k + threadIdx.x;
+    int e = idx[pid];
+    dst[threadIdx.x] = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
+  }
+  float G = 1.0f;
+  if constexpr (FMT == MOE_FMT_NVFP4) G = nvfp4_G(row_absmax(row, H, red));
+  __syncthreads();
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (threadIdx.x < k) glob[dst[threadIdx.x]] = __fdiv_rn(1.0f, G);
+  }
+  quant_row<FMT>(row, H, G, mx_mode, k, dst, codes, scales, true, H / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+}
+
+// h: one CTA per canonical pair position p; row = its padded row.
+template <int FMT>
+__global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __restrict__ h, int F, int mx_mode,
+                                                       const int32_t* __restrict__ idx,
+                                                       const int32_t* __restrict__ offsets,
+                                                       const int32_t* __restrict__ perm,
+                                                       const int32_t* __restrict__ seg_start, uint8_t* codes,
+                                                       uint8_t* scales, float* glob) {
+  __shared__ float red[32];
+  __shared__ int64_t dst[1];
+  const int p = blockIdx.x;
+  const int e = idx[perm[p]];
+  const int64_t r = (int64_t)seg_start[e] + (p - offsets[e]);
+  const __nv_bfloat16* row = h + r * F;
+  if (threadIdx.x == 0) dst[0] = r;
+  float G = 1.0f;
+  if constexpr (FMT == MOE_FMT_NVFP4) G = nvfp4_G(row_absmax(row, F, red));
+  __syncthreads();
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (threadIdx.x == 0) glob[r] = __fdiv_rn(1.0f, G);
+  }
+  quant_row<FMT>(row, F, G, mx_mode, 1, dst, codes, scales, true, F / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+}
+
+// --- general API quantiser -------------------------------------------------
+__global__ void k_zero_f32(float* p, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0.0f;
+}
+
+// Per-group absolute maximum, accumulated as float bits (non-negative floats
+// order like their unsigned bit patterns).
+template <typename Src>
+__global__ void k_group_amax(const Src* __restrict__ src, int64_t cols, int64_t group_rows, int64_t chunk,
+                             float* amax) {
+  __shared__ float red[32];
+  const int64_t g = blockIdx.y;
+  const int64_t n = group_rows * cols;
+  const Src* base = src + g * n;
+  int64_t lo = (int64_t)blockIdx.x * chunk, hi = lo + chunk < n ? lo + chunk : n;
+  float m = 0.0f;
+  for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    float v;
+    if constexpr (sizeof(Src) == 2) v = __bfloat162float(base[i]);
+    else v = base[i];
+    m = fmaxf(m, fabsf(v));
+  }
+  m = block_max(m, red);
+  if (threadIdx.x == 0 && m > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(amax + g), __float_as_uint(m));
+}
+
+template <int FMT, typename Src>
+__global__ void __launch_bounds__(kQThreads) k_quantize_rows(const Src* __restrict__ src, int64_t cols,
+                                                             int64_t group_rows, int mx_mode, bool tiled,
+                                                             uint8_t* codes, uint8_t* scales,
+                                                             const float* group_amax, float* glob_rows) {
+  __shared__ float red[32];
+  __shared__ int64_t dst[1];
+  const int64_t r = blockIdx.x;
+  const Src* row = src + r * cols;
+  if (threadIdx.x == 0) dst[0] = r;
+  float G = 1.0f;
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (group_rows > 0) G = nvfp4_G(group_amax[r / group_rows]);
+    else G = nvfp4_G(row_absmax(row, (int)cols, red));
+  }
+  __syncthreads();
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (group_rows == 0 && threadIdx.x == 0) glob_rows[r] = __fdiv_rn(1.0f, G);
+  }
+  quant_row<FMT, Src>(row, (int)cols, G, mx_mode, 1, dst, codes, scales, tiled,
+                      cols / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+}
+
+__global__ void k_finalize_groups(float* glob, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    glob[i] = __fdiv_rn(1.0f, nvfp4_G(glob[i]));
+}
+
+__global__ void k_pack_scales(const uint8_t* __restrict__ src, int64_t rows, int64_t cols, uint8_t* dst) {
+  int64_t n = rows * cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = i / cols, c = i % cols;
+    dst[tiled_scale_offset(r, c, cols)] = src[i];
+  }
+}
+
+int grid_1d(int64_t n, int threads) {
+  int64_t g = (n + threads - 1) / threads;
+  if (g > 152 * 32) g = 152 * 32;
+  return g < 1 ? 1 : (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
+                           const int32_t* pair_pos, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
+                           float* glob, cudaStream_t st) {
+  if (c.fmt == MOE_FMT_NVFP4)
+    k_quant_x<MOE_FMT_NVFP4><<<c.T, kQThreads, 0, st>>>(x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
+                                                         seg_start, codes, scales, glob);
+  else
+    k_quant_x<MOE_FMT_MXFP8><<<c.T, kQThreads, 0, st>>>(x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
+                                                         seg_start, codes, scales, glob);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx, const int32_t* offsets,
+                           const int32_t* perm, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
+                           float* glob, cudaStream_t st) {
+  int P = c.T * c.k;
+  if (c.fmt == MOE_FMT_NVFP4)
+    k_quant_h<MOE_FMT_NVFP4><<<P, kQThreads, 0, st>>>(h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
+                                                       codes, scales, glob);
+  else
+    k_quant_h<MOE_FMT_MXFP8><<<P, kQThreads, 0, st>>>(h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
+                                                       codes, scales, glob);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,
+                            int64_t group_rows, moe_scale_layout layout, uint8_t* codes, uint8_t* scales,
+                            float* glob, float* /*unused*/, cudaStream_t st) {
+  bool tiled = layout == MOE_SCALES_TILED;
+  bool nv = fmt == MOE_FMT_NVFP4;
+  if (nv && group_rows > 0) {
+    int64_t ng = rows / group_rows;
+    int64_t n = group_rows * cols;
+    int64_t chunk = 1 << 16;
+    int64_t nchunks = (n + chunk - 1) / chunk;
+    k_zero_f32<<<grid_1d(ng, 256), 256, 0, st>>>(glob, ng);
+    dim3 grid((unsigned)nchunks, (unsigned)ng);
+    if (src_fp32) k_group_amax<float><<<grid, 256, 0, st>>>((const float*)src, cols, group_rows, chunk, glob);
+    else k_group_amax<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)src, cols, group_rows, chunk, glob);
+  }
+  dim3 grid((unsigned)rows);
+  if (nv) {
+    if (src_fp32)
+      k_quantize_rows<MOE_FMT_NVFP4, float><<<grid, kQThreads, 0, st>>>((const float*)src, cols, group_rows, mx_mode,
+                                                                       tiled, codes, scales, glob, glob);
+    else
+      k_quantize_rows<MOE_FMT_NVFP4, __nv_bfloat16><<<grid, kQThreads, 0, st>>>(
+          (const __nv_bfloat16*)src, cols, group_rows, mx_mode, tiled, codes, scales, glob, glob);
+    if (group_rows > 0) k_finalize_groups<<<grid_1d(rows / group_rows, 256), 256, 0, st>>>(glob, rows / group_rows);
+  } else {
+    if (src_fp32)
+      k_quantize_rows<MOE_FMT_MXFP8, float><<<grid, kQThreads, 0, st>>>((const float*)src, cols, 0, mx_mode, tiled,
+                                                                       codes, scales, nullptr, nullptr);
+    else
+      k_quantize_rows<MOE_FMT_MXFP8, __nv_bfloat16><<<grid, kQThreads, 0, st>>>(
+          (const __nv_bfloat16*)src, cols, 0, mx_mode, tiled, codes, scales, nullptr, nullptr);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_scales(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst, cudaStream_t st) {
+  k_pack_scales<<<grid_1d(rows * cols, 256), 256, 0, st>>>(src, rows, cols, dst);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

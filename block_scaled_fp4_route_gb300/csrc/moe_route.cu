@@ -1,0 +1,247 @@
+// Fused router: logits GEMM, sigmoid, additive bias, top-k, normalisation
+// (SGLang blog on Inkling 2 Small, Performance section, kernel-fusion bullet:
+// sigmoid, bias and top-k form one router kernel; Miles docs section 1:
+// sigmoid routing over 384 experts, 8 per token).
+//
+// Logits: fp32 on CUDA cores.  Each output sums its bf16 x bf16 products
+// (exact in fp32) in chunks of 32 with plain fp32 adds, and the chunk sums are
+// added with Kahan compensation (within a K split and again across splits).
+// Hence |l_gpu - l| <= (gamma_31 + 3u) * sum_h |x_h w_eh| <= 40u * sum|x w|,
+// u = 2^-24, which the top-k parity check uses to certify near-ties.
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kKC = 64;        // K elements per smem stage
+constexpr int kChunk = 32;     // plain-sum chunk length
+constexpr int kPad = 4;        // fp32 row padding (conflict-free float4 reads)
+
+struct Kahan {
+  float s = 0.0f, c = 0.0f;
+  __device__ __forceinline__ void add(float v) {
+    float y = __fsub_rn(v, c);
+    float t = __fadd_rn(s, y);
+    c = __fsub_rn(__fsub_rn(t, s), y);
+    s = t;
+  }
+};
+
+// CTA tile (16*RM tokens) x (16*RN experts); 256 threads as 16 x 16.
+template <int RM, int RN>
+__global__ void __launch_bounds__(256) k_router_logits(const __nv_bfloat16* __restrict__ x,
+                                                       const __nv_bfloat16* __restrict__ wr, float* __restrict__ part,
+                                                       int T, int H, int E, int k_len) {
+  constexpr int TM = 16 * RM, TE = 16 * RN;
+  extern __shared__ __align__(16) float router_smem[];
+  float(*As)[TM][kKC + kPad] = reinterpret_cast<float(*)[TM][kKC + kPad]>(router_smem);
+  float(*Bs)[TE][kKC + kPad] = reinterpret_cast<float(*)[TE][kKC + kPad]>(router_smem + 2 * TM * (kKC + kPad));
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int e0 = blockIdx.x * TE, t0 = blockIdx.y * TM;
+  const int split = blockIdx.z;
+  const int kbeg = split * k_len;
+  const int nst = k_len / kKC;
+
+  // register staging of one stage: rows x 8 uint4 (8 bf16 each)
+  constexpr int A_VEC = TM * (kKC / 8), B_VEC = TE * (kKC / 8);
+  constexpr int A_PER = (A_VEC + 255) / 256, B_PER = (B_VEC + 255) / 256;
+  uint4 ra[A_PER], rb[B_PER];
+
+  auto gload = [&](int st) {
+    int kk = kbeg + st * kKC;
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+      int v = threadIdx.x + 256 * i;
+      ra[i] = make_uint4(0, 0, 0, 0);
+      if (v < A_VEC) {
+        int r = v >> 3, q = v & 7;
+        if (t0 + r < T) ra[i] = *reinterpret_cast<const uint4*>(x + (int64_t)(t0 + r) * H + kk + 8 * q);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < B_PER; ++i) {
+      int v = threadIdx.x + 256 * i;
+      rb[i] = make_uint4(0, 0, 0, 0);
+      if (v < B_VEC) {
+        int r = v >> 3, q = v & 7;
+        if (e0 + r < E) rb[i] = *reinterpret_cast<const uint4*>(wr + (int64_t)(e0 + r) * H + kk + 8 * q);
+      }
+    }
+  };
+  auto unpack_store = [&](float* dst, uint4 u) {
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    float4 lo = make_float4(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u),
+                            __uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+    float4 hi = make_float4(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u),
+                            __uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+    reinterpret_cast<float4*>(dst)[0] = lo;
+    reinterpret_cast<float4*>(dst)[1] = hi;
+  };
+  auto sstore = [&](int buf) {
+#pragma unroll
+    for (int i = 0; i < A_PER; ++i) {
+      int v = threadIdx.x + 256 * i;
+      if (v < A_VEC) unpack_store(&As[buf][v >> 3][8 * (v & 7)], ra[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < B_PER; ++i) {
+      int v = threadIdx.x + 256 * i;
+      if (v < B_VEC) unpack_store(&Bs[buf][v >> 3][8 * (v & 7)], rb[i]);
+    }
+  };
+
+  Kahan acc[RM][RN];
+  gload(0);
+  sstore(0);
+  __syncthreads();
+  for (int st = 0; st < nst; ++st) {
+    const int buf = st & 1;
+    if (st + 1 < nst) gload(st + 1);
+#pragma unroll
+    for (int ch = 0; ch < kKC / kChunk; ++ch) {
+      float p[RM][RN];
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < RN; ++j) p[i][j] = 0.0f;
+#pragma unroll
+      for (int kq = 0; kq < kChunk; kq += 4) {
+        float4 a[RM], b[RN];
+#pragma unroll
+        for (int i = 0; i < RM; ++i) a[i] = *reinterpret_cast<const float4*>(&As[buf][ty + 16 * i][ch * kChunk + kq]);
+#pragma unroll
+        for (int j = 0; j < RN; ++j) b[j] = *reinterpret_cast<const float4*>(&Bs[buf][tx + 16 * j][ch * kChunk + kq]);
+#pragma unroll
+        for (int i = 0; i < RM; ++i)
+#pragma unroll
+          for (int j = 0; j < RN; ++j) {
+            p[i][j] = __fmaf_rn(a[i].x, b[j].x, p[i][j]);
+            p[i][j] = __fmaf_rn(a[i].y, b[j].y, p[i][j]);
+            p[i][j] = __fmaf_rn(a[i].z, b[j].z, p[i][j]);
+            p[i][j] = __fmaf_rn(a[i].w, b[j].w, p[i][j]);
+          }
+      }
+#pragma unroll
+      for (int i = 0; i < RM; ++i)
+#pragma unroll
+        for (int j = 0; j < RN; ++j) acc[i][j].add(p[i][j]);
+    }
+    if (st + 1 < nst) {
+      sstore(buf ^ 1);
+    }
+    __syncthreads();
+  }
+  float* out = part + (int64_t)split * T * E;
+#pragma unroll
+  for (int i = 0; i < RM; ++i)
+#pragma unroll
+    for (int j = 0; j < RN; ++j) {
+      int t = t0 + ty + 16 * i, e = e0 + tx + 16 * j;
+      if (t < T && e < E) out[(int64_t)t * E + e] = acc[i][j].s;
+    }
+}
+
+// One warp per token: sum the K-split partials, sigmoid, bias, top-k,
+// normalise.  Ties in the key go to the lower expert index.
+__global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ part, int nsplit,
+                                                     const float* __restrict__ bias, int T, int E, int k,
+                                                     int bias_in_weights, float routed_scale,
+                                                     int32_t* __restrict__ idx, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  constexpr int MAXPER = kMaxE / 32;
+  float key[MAXPER], sg[MAXPER];
+  const int per = (E + 31) / 32;
+#pragma unroll
+  for (int i = 0; i < MAXPER; ++i) {
+    key[i] = -INFINITY;
+    sg[i] = 0.0f;
+    int e = lane + 32 * i;
+    if (i < per && e < E) {
+      Kahan l;
+      for (int s = 0; s < nsplit; ++s) l.add(part[((int64_t)s * T + t) * E + e]);
+      float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l.s)));
+      sg[i] = s;
+      key[i] = __fadd_rn(s, bias[e]);
+    }
+  }
+  uint32_t taken = 0;
+  float den = 0.0f;
+  int my_slot_e[kMaxK];
+  float my_num[kMaxK];
+  for (int j = 0; j < k; ++j) {
+    // best untaken entry of this lane
+    float bk = -INFINITY;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < MAXPER; ++i) {
+      int e = lane + 32 * i;
+      if (i < per && e < E && !((taken >> i) & 1u) && key[i] > bk) { bk = key[i]; be = e; }
+    }
+    // warp argmax, ties to the lower expert index
+    for (int o = 16; o > 0; o >>= 1) {
+      float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ok > bk || (ok == bk && oe < be)) { bk = ok; be = oe; }
+    }
+    float num = 0.0f;
+    if ((be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < MAXPER; ++i)
+        if (i == (be >> 5)) {
+          taken |= 1u << i;
+          num = bias_in_weights ? key[i] : sg[i];
+        }
+    }
+    num = __shfl_sync(0xffffffffu, num, be & 31);
+    my_slot_e[j] = be;
+    my_num[j] = num;
+    den = __fadd_rn(den, num);
+  }
+  if (lane == 0) {
+    for (int j = 0; j < k; ++j) {
+      idx[(int64_t)t * k + j] = my_slot_e[j];
+      w[(int64_t)t * k + j] = __fmul_rn(routed_scale, __fdiv_rn(my_num[j], den));
+    }
+  }
+}
+
+constexpr int router_smem_bytes(int rm, int rn) { return 2 * 16 * (rm + rn) * (kKC + kPad) * 4; }
+
+}  // namespace
+
+// Number of K splits of the logits GEMM (also sizes the partials buffer).
+int router_splits(const moe_config& c) {
+  if (c.T > 256) return 1;
+  int s = 8;
+  while (s > 1 && (c.H % (kKC * s)) != 0) s >>= 1;
+  return s;
+}
+
+cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr, const float* bias,
+                          float* logits, int32_t* idx, float* w, cudaStream_t st) {
+  int ns = router_splits(c);
+  int k_len = c.H / ns;
+  if (c.T <= 256) {
+    constexpr int smem = router_smem_bytes(1, 4);
+    dim3 grid((c.E + 63) / 64, (c.T + 15) / 16, ns);
+    k_router_logits<1, 4><<<grid, 256, smem, st>>>(x, wr, logits, c.T, c.H, c.E, k_len);
+  } else {
+    constexpr int smem = router_smem_bytes(4, 4);
+    static bool attr = false;
+    if (!attr) {
+      cudaError_t e = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, ns);
+    k_router_logits<4, 4><<<grid, 256, smem, st>>>(x, wr, logits, c.T, c.H, c.E, k_len);
+  }
+  k_router_topk<<<(c.T + 7) / 8, 256, 0, st>>>(logits, ns, bias, c.T, c.E, c.k, c.bias_in_weights, c.routed_scale,
+                                               idx, w);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,229 @@
+/*
+ * moe.h — C ABI of the routed block-scaled mixture-of-experts layer for
+ * GB300 (sm_103a).
+ *
+ * The layer is the routed MoE of Inkling 2 Small: hidden H = 4608, E = 384
+ * routed experts, top-k = 8, expert FFN width F = 2304, no shared experts,
+ * soft-capped SwiGLU, expert weights in NVFP4 (W4A4) or MXFP8 (W8A8).
+ * Sources (pages on the Inkling 2 Small release):
+ *   [SGL]  "SGLang and Miles Add Day-0 Support for Inkling 2 Small",
+ *          section Performance (MegaMoE and kernel-fusion bullets).
+ *   [CB]   "Inkling-2-Small" SGLang cookbook, section 2 Configuration Tips
+ *          (Checkpoints, Parallelism, MegaMoE paragraphs).
+ *   [TS]   "TML Inkling 2 Small at Day 0" (TokenSpeed), table "What's new"
+ *          (MoE and Checkpoint rows) and section "Serving ... on the
+ *          TokenSpeed stack".
+ *   [MI]   "inkling-2-small" Miles docs, section 1 Model Introduction and
+ *          section 5.3 Rollout and precision.
+ *
+ * Conventions for every call:
+ *   - Pointers named *_dev are device pointers; the caller owns every buffer,
+ *     the workspace and the stream.  The library allocates no device memory
+ *     and keeps no state besides cached device attributes.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, passed as void*).
+ *   - On invalid arguments a call returns a non-zero status and enqueues
+ *     nothing.  Checks: shapes (see moe_config), 16-byte alignment of every
+ *     pointer, workspace size, device compute capability 10.3.
+ *   - A CUDA launch error is returned as MOE_ERR_CUDA.  Device-side bounded
+ *     waits that ran out are recorded in the workspace status word and are
+ *     reported by moe_poll_device_status.
+ *   - Inputs must be finite; NaN/Inf behaviour is unspecified.
+ *   - Row-major everywhere; the reduction (K) dimension is contiguous.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,
+  MOE_ERR_MISALIGNED = 3,
+  MOE_ERR_WORKSPACE_TOO_SMALL = 4,
+  MOE_ERR_ARCH = 5,
+  MOE_ERR_CUDA = 6,
+  MOE_ERR_DEVICE_TIMEOUT = 7
+} moe_status;
+
+/* Expert weight / activation encodings [CB Checkpoints; TS Checkpoint row;
+ * MI 5.3: W4A4 / W8A8]:
+ *   NVFP4: E2M1 codes packed two per byte (low nibble = lower k), one E4M3
+ *          scale per 16 elements along K, one fp32 global decode factor g
+ *          (per expert matrix for weights, per token row for activations):
+ *          value = e2m1(code) * e4m3(scale) * g.
+ *   MXFP8: E4M3 codes, one E8M0 scale per 32 elements along K:
+ *          value = e4m3(code) * 2^(scale - 127). */
+typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP8 = 1 } moe_format;
+
+/* Layout of block-scale bytes.
+ *   ROWMAJOR: scales[r][c], c = k / block, shape [rows, K/block].
+ *   TILED:    the layout the expert GEMMs consume: rows padded to a multiple
+ *             of 128 and scale columns to a multiple of 4; the byte of
+ *             (r, c) sits at
+ *               ((r/128) * (C/4) + c/4) * 512 + (r%32)*16 + ((r/32)%4)*4 + c%4
+ *             with C the (padded) number of scale columns.  Same byte count
+ *             as ROWMAJOR when rows%128 == 0 and C%4 == 0. */
+typedef enum { MOE_SCALES_ROWMAJOR = 0, MOE_SCALES_TILED = 1 } moe_scale_layout;
+
+/* Layer shape and options.
+ *   T tokens (1..65536), H hidden, E experts (1..1024), k experts per token
+ *   (1..min(E,32)), F expert FFN width.  H and F must be multiples of 256 for
+ *   NVFP4 and of 128 for MXFP8.
+ *   swiglu_cap: c in cap(v) = c*tanh(v/c), applied to the gate and up
+ *     pre-activations; 0 disables the cap.  Default 10.  [TS MoE row and MI 1
+ *     call the activation a capped / soft-capped SwiGLU but give neither the
+ *     form nor the constant, so both are this parameter.]
+ *   mx_scale_mode: MXFP8 only.  0 = OCP rule X = 2^(floor(log2 amax) - 8)
+ *     (default; block maxima in (448, 512)*X saturate); 1 = X =
+ *     2^ceil(log2(amax/448)) (never saturates).
+ *   bias_in_weights: 0 (default) = the router bias steers selection only and
+ *     the weights normalise the unbiased sigmoid scores; 1 = weights
+ *     normalise the biased keys.
+ *   routed_scale: multiplies the normalised routing weights (default 1). */
+typedef struct {
+  int T, H, E, k, F;
+  moe_format fmt;
+  float swiglu_cap;
+  int mx_scale_mode;
+  int bias_in_weights;
+  float routed_scale;
+} moe_config;
+
+/* One quantised expert matrix for all E experts (device pointers).
+ *   gate, up: N = F rows, K = H;  down: N = H rows, K = F.
+ *   codes:  NVFP4 u8 [E, N, K/2];  MXFP8 u8 [E, N, K].
+ *   scales: TILED layout over the E*N rows (moe_quantize with
+ *           MOE_SCALES_TILED, or moe_pack_scales from ROWMAJOR).
+ *   global_scale: NVFP4 fp32 [E] decode factors; MXFP8: NULL. */
+typedef struct {
+  const void* codes;
+  const void* scales;
+  const float* global_scale;
+} moe_qweight;
+
+/* Bytes of workspace that moe_route / moe_dispatch / moe_expert_ffn /
+ * moe_forward need for this configuration.  The workspace must be 256-byte
+ * aligned; its contents need no initialisation. */
+MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
+
+/* Fused router [SGL Performance, kernel-fusion bullet: sigmoid, bias and
+ * top-k selection share one kernel; MI 1: sigmoid routing over 384 experts,
+ * 8 per token].
+ *   x_dev        bf16 [T, H] tokens
+ *   w_router_dev bf16 [E, H]
+ *   bias_dev     fp32 [E]
+ *   topk_idx_dev int32 [T, k] (out): experts by descending key = s + bias,
+ *                s = sigmoid(x . w_e); ties go to the lower expert index.
+ *   topk_w_dev   fp32 [T, k] (out): routed_scale * s_j / sum_i s_i.
+ * Logits accumulate in fp32 in chunks of 32 products, the chunk sums
+ * compensated (Kahan): |error| <= 40 * 2^-24 * sum_h |x_h w_eh|. */
+MOE_API moe_status moe_route(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                     const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,
+                     void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Token dispatch [CB MegaMoE: dispatch is a step of the fused unit]: groups
+ * the P = T*k pairs (t, j)
+ * by expert, and within an expert by token.
+ *   topk_idx_dev int32 [T, k]
+ *   counts_dev   int32 [E] (out)     pairs per expert
+ *   offsets_dev  int32 [E+1] (out)   exclusive scan of counts
+ *   perm_dev     int32 [P] (out)     perm[p] = t*k + j, sorted by (e, t)
+ *   pair_pos_dev int32 [T, k] (out)  inverse: pair_pos[t*k + j] = p
+ * Deterministic. */
+MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int32_t* counts_dev,
+                        int32_t* offsets_dev, int32_t* perm_dev, int32_t* pair_pos_dev,
+                        void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Expert FFN of every pair [CB MegaMoE: the fused unit holds the two expert
+ * GEMMs and the capped SwiGLU between them; TS: the expert GEMMs run on
+ * block-scaled tensor cores; SGL kernel-fusion bullet: activation
+ * quantisation lives inside the expert GEMMs; MI 5.3: W4A4 / W8A8]:
+ *   a   = quantise(x_t) per token over the full H (NVFP4: per-row global)
+ *   g,u = W_gate,e a , W_up,e a          (tcgen05 block-scaled MMA, fp32)
+ *   h   = bf16( silu(cap g) * cap u )
+ *   y_p = W_down,e quantise(h)           (NVFP4: per-row global over F)
+ *   x_dev        bf16 [T, H]
+ *   topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev: from moe_route /
+ *                moe_dispatch (the tile plan is rebuilt from offsets_dev)
+ *   gate/up/down quantised weights (see moe_qweight)
+ *   y_perm_dev   fp32 [P, H] (out), row p = perm order. */
+MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
+                          const int32_t* offsets_dev, const int32_t* perm_dev,
+                          const int32_t* pair_pos_dev, const moe_qweight* gate,
+                          const moe_qweight* up, const moe_qweight* down, float* y_perm_dev,
+                          void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Weighted combine [CB MegaMoE: the combine ends the fused unit]:
+ *   out[t] = bf16_rne( sum_{j=0..k-1} topk_w[t,j] * y_perm[pair_pos[t,j]] ),
+ * summed in fp32 in slot order (deterministic).
+ *   y_perm_dev fp32 [P, H]; topk_w_dev fp32 [T, k]; pair_pos_dev int32 [T, k];
+ *   out_dev bf16 [T, H] (out). */
+MOE_API moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const float* topk_w_dev,
+                       const int32_t* pair_pos_dev, void* out_dev, void* stream);
+
+/* The whole layer in one call: moe_route, moe_dispatch, moe_expert_ffn and
+ * moe_combine chained on `stream` with every intermediate in the workspace
+ * [CB MegaMoE: one fused unit per layer; SGL: programmatic dependent
+ * launch between kernels].  out_dev bf16 [T, H]. */
+MOE_API moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                       const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
+                       const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes,
+                       void* stream);
+
+/* Block quantiser [MI 1 and 5.2: weight sync re-encodes experts in the layer's
+ * format and recomputes NVFP4 global scales].  Encodes rows x cols values.
+ *   src_is_fp32: 1 = src fp32, 0 = src bf16.
+ *   group_rows:  NVFP4 global-scale granularity: 0 = one global per row
+ *                (activations); G > 0 = one global per G consecutive rows
+ *                (weights: G = N, one per expert matrix); rows % G == 0.
+ *                Ignored for MXFP8.
+ *   codes_dev:   NVFP4 u8 [rows, cols/2]; MXFP8 u8 [rows, cols].
+ *   scales_dev:  ROWMAJOR [rows, cols/bs] or TILED (rows % 128 == 0 and
+ *                (cols/bs) % 4 == 0 required).
+ *   global_dev:  NVFP4 fp32 [rows] or [rows/G]; MXFP8: NULL.
+ * NVFP4 steps (fp32, each rounded to nearest): G = 2688/amax (1 if amax = 0),
+ * g = 1/G, scale = E4M3((amax_b/6)*G), code = E2M1(v * (G/scale)).
+ * MXFP8: scale as mx_scale_mode, code = E4M3(v * 2^(127 - scale)).
+ * Conversions round to nearest even and saturate; zero keeps its sign. */
+MOE_API moe_status moe_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32, const void* src_dev,
+                        int64_t rows, int64_t cols, int64_t group_rows, moe_scale_layout layout,
+                        void* codes_dev, void* scales_dev, float* global_dev, void* stream);
+
+/* ROWMAJOR -> TILED scale re-layout (rows % 128 == 0, scale columns % 4 == 0). */
+MOE_API moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64_t scale_cols, void* tiled_dev,
+                           void* stream);
+
+/* Synchronises `stream`, reads and clears the workspace status word.
+ * Returns MOE_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out. */
+MOE_API moe_status moe_poll_device_status(void* ws_dev, void* stream);
+
+/* Byte offsets of the layer's intermediates inside the workspace, for
+ * inspection by tests (all buffers in padded expert-row order: each expert's
+ * rows start at a multiple of 128).  R = padded row capacity. */
+typedef struct {
+  int64_t R;
+  size_t status, logits, topk_idx, topk_w, counts, offsets, perm, pair_pos, bitmap, seg_start,
+      tiles, n_row_tiles, xq_codes, xq_scales, xq_global, h_bf16, hq_codes, hq_scales, hq_global,
+      y_perm, total;
+} moe_ws_layout;
+MOE_API moe_status moe_workspace_layout(const moe_config* cfg, moe_ws_layout* layout);
+
+MOE_API const char* moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -9,8 +9,9 @@
  * What it computes, and where each step comes from (pages on the model
  * release of Inkling 2 Small):
  *   - "SGLang and Miles Add Day-0 Support for Inkling 2 Small", section
- *     Performance, kernel-fusion bullet: the router is sigmoid, bias, top-k;
- *     quantisation is folded into the expert GEMMs.
+ *     Performance, kernel-fusion bullet: one router kernel does the sigmoid,
+ *     the bias and the top-k; activation quantisation sits inside the expert
+ *     GEMMs.
  *   - "Inkling-2-Small" (SGLang cookbook), section 2 Configuration Tips,
  *     MegaMoE paragraph: the fused unit is dispatch, both expert GEMMs, the
  *     capped SwiGLU and the combine; Parallelism paragraph: NVFP4 activation
@@ -258,9 +259,9 @@ void orc_mxfp8_decode(const uint8_t* codes, const uint8_t* sf, int64_t rows, int
 }
 
 /* ======================================================================== */
-/* O2. Router.  SGLang blog, Performance, kernel-fusion bullet ("sigmoid,   */
-/* bias and top-k"); Miles docs section 1 ("sigmoid-routed MoE", 384 routed */
-/* experts at top-8).  Readings: logits l = x . W_r (fp64 over the bf16      */
+/* O2. Router.  SGLang blog, Performance, kernel-fusion bullet (sigmoid,    */
+/* bias and top-k in that order); Miles docs section 1 (sigmoid routing,   */
+/* 384 routed experts, 8 per token).  Readings: l = x . W_r (fp64 over the  */
 /* inputs); s = 1 / (1 + exp(-l)); the bias is added after the sigmoid and   */
 /* steers selection only: key = s + b; top-k by key descending, ties to the */
 /* lower expert index; slots j = 0..k-1 in that order; weights              */
@@ -321,7 +322,7 @@ void orc_router_select(int64_t T, int64_t E, int64_t k, const double* logits, co
 }
 
 /* ======================================================================== */
-/* O3. Dispatch (cookbook, MegaMoE paragraph: "dispatch").  Pairs (t, j)    */
+/* O3. Dispatch (cookbook, MegaMoE paragraph: dispatch step).  Pairs (t, j) */
 /* with expert e = idx[t,j] are listed grouped by expert ascending and, in  */
 /* an expert, by token ascending.  counts[e], offsets = exclusive scan      */
 /* (E+1 entries), perm[p] = t*k + j, pair_pos[t*k + j] = p.                 */
@@ -346,8 +347,9 @@ void orc_dispatch(int64_t T, int64_t E, int64_t k, const int32_t* idx, int32_t* 
 
 /* ======================================================================== */
 /* O6. Expert FFN of one expert over n pairs (cookbook MegaMoE paragraph:   */
-/* both expert GEMMs and the capped SwiGLU; TokenSpeed table: capped        */
-/* SwiGLU; Miles section 1: soft-capped SwiGLU; Miles 5.3: W4A4 / W8A8).    */
+/* the two expert GEMMs with the capped SwiGLU between them; TokenSpeed     */
+/* table and Miles section 1 name the capped / soft-capped SwiGLU; Miles    */
+/* 5.3: W4A4 / W8A8 activation quantisation).                               */
 /*   g = W_gate a, u = W_up a          (fp64 over decoded operands)         */
 /*   cap(v) = c * tanh(v / c)  (c = 0: no cap)   [reading: form and c]       */
 /*   h = silu(cap g) * cap u = cap g / (1 + exp(-cap g)) * cap u             */
@@ -412,7 +414,7 @@ void orc_expert_ffn(int fmt /*0 nvfp4, 1 mxfp8*/, int64_t H, int64_t F, double c
 }
 
 /* ======================================================================== */
-/* O7. Combine (cookbook MegaMoE paragraph: "the combine").                 */
+/* O7. Combine (cookbook MegaMoE paragraph: the combine step).             */
 /*   out[t] = sum_j w[t,j] * y[pair_pos[t,j]]   (fp64, slot order)          */
 /* ======================================================================== */
 

@@ -1,0 +1,118 @@
+"""Host-side tests of the C ABI: the library builds, loads and exports every
+entry point include/moe.h declares; argument validation returns the
+documented status codes before anything is enqueued (no GPU needed: the
+pointers below are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_fp4_route_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_layer_calls():
+    names = declared_functions()
+    for n in ["moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward", "moe_workspace_size",
+              "moe_quantize", "moe_poll_device_status", "moe_status_string"]:
+        assert n in names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    L = moe.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), n
+        assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value
+    assert sorted(declared_functions()) == sorted(moe.EXPORTED)
+
+
+def test_status_strings():
+    for s in range(8):
+        assert moe.moe_status_string(s)
+
+
+def cfg(**kw):
+    base = dict(T=64, H=4608, E=384, k=8, F=2304, fmt="nvfp4")
+    base.update(kw)
+    return moe.make_config(**base)
+
+
+def test_workspace_size_and_layout():
+    c = cfg()
+    n = moe.moe_workspace_size(c)
+    L = moe.moe_workspace_layout(c)
+    assert L["total"] == n
+    offs = [L[f] for f in ["status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "pair_pos",
+                           "bitmap", "seg_start", "tiles", "n_row_tiles", "xq_codes", "xq_scales", "xq_global",
+                           "h_bf16", "hq_codes", "hq_scales", "hq_global", "y_perm", "total"]]
+    assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
+    # padded rows: one 128-row block per expert on top of the pairs
+    assert L["R"] == ((64 * 8 + 127) // 128 + 384) * 128
+    assert L["hq_codes"] - L["h_bf16"] >= L["R"] * 2304 * 2
+    # larger T needs no less workspace
+    assert moe.moe_workspace_size(cfg(T=4096)) > n
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(T=0), 2), (dict(T=70000), 2), (dict(k=0), 2), (dict(k=33), 2), (dict(E=4, k=8), 2),
+    (dict(E=2000), 2), (dict(H=4608 + 128), 2), (dict(F=128), 2), (dict(fmt="mxfp8", F=128 + 64), 2),
+    (dict(swiglu_cap=-1.0), 1), (dict(mx_scale_mode=2), 1),
+])
+def test_config_validation(kw, status):
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_workspace_size(cfg(**kw))
+    assert ei.value.status == status
+
+
+class FakeTensor:
+    """Stands in for a device tensor: an address and a size, never dereferenced."""
+
+    def __init__(self, addr, nbytes=1 << 40):
+        self.addr, self.nbytes = addr, nbytes
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+def test_argument_validation_without_a_device():
+    c = cfg()
+    ok = FakeTensor(0x10000)
+    mis = FakeTensor(0x10008)
+    ws = FakeTensor(0x100000)
+    with pytest.raises(moe.MoeError) as ei:   # null pointer
+        moe.moe_route(c, ok, ok, 0, ok, ok, ws, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(moe.MoeError) as ei:   # misaligned pointer
+        moe.moe_route(c, mis, ok, ok, ok, ok, ws, stream=0)
+    assert ei.value.status == 3
+    with pytest.raises(moe.MoeError) as ei:   # workspace too small
+        moe.moe_route(c, ok, ok, ok, ok, ok, FakeTensor(0x100000, 1024), stream=0)
+    assert ei.value.status == 4
+    with pytest.raises(moe.MoeError) as ei:   # workspace not 256-byte aligned
+        moe.moe_route(c, ok, ok, ok, ok, ok, FakeTensor(0x100010), stream=0)
+    assert ei.value.status == 3
+    qw = moe.qweight(0x20000, 0x30000, None)   # NVFP4 needs globals
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(c, ok, ok, ok, qw, qw, qw, ok, ws, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(moe.MoeError) as ei:   # tiled scales need rows % 128 == 0
+        moe.lib()
+        st = moe.lib().moe_quantize(0, 0, 1, 0x10000, 100, 256, 0, 1, 0x20000, 0x30000, 0x40000, 0)
+        moe._check("moe_quantize", st)
+    assert ei.value.status == 2
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_pack_scales(ok, 100, 16, ok, stream=0)
+    assert ei.value.status == 2

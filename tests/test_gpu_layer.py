@@ -1,0 +1,177 @@
+"""The whole layer on the GPU (moe_forward and the staged calls) against the
+oracle.  Small shapes are compared on every token; the full-size seeded
+workloads, in the launch configuration the benchmark times, on all routing /
+dispatch / activation-code results and on the output rows of a seeded token
+sample (the oracle regenerates the touched experts itself)."""
+import numpy as np
+import pytest
+
+import oracle
+import parity
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+import block_scaled_fp4_route_gb300 as moe  # noqa: E402
+from synth.gpu_workload import GpuWorkload, untile_scales  # noqa: E402
+
+U = dict(outlier_frac=0.0, bias="uniform")
+SMALL = {
+    "tiny_mxfp8": "tiny_mxfp8",
+    "tiny_nvfp4": dict(T=8, H=256, E=16, k=2, F=256, fmt="nvfp4", seed=10, **U),
+    "ragged_mxfp8": dict(T=37, H=256, E=8, k=3, F=128, fmt="mxfp8", seed=11, **U),
+    "multitile_nvfp4": dict(T=300, H=256, E=2, k=1, F=256, fmt="nvfp4", seed=12, **U),
+    "multitile_mxfp8": dict(T=290, H=384, E=3, k=2, F=256, fmt="mxfp8", seed=15, **U),
+    "k_eq_E_mxfp8": dict(T=5, H=256, E=4, k=4, F=128, fmt="mxfp8", seed=13, **U),
+    "one_token_nvfp4": dict(T=1, H=512, E=16, k=4, F=256, fmt="nvfp4", seed=14, **U),
+}
+
+
+def padded_rows_of(r, tokens, k):
+    """Padded expert-grouped row of every (token, slot) of the sample."""
+    idx, pp, off, seg = r["idx"], r["pair_pos"], r["offsets"], r["seg_start"]
+    rows = np.empty((len(tokens), k), np.int64)
+    for i, t in enumerate(tokens):
+        for j in range(k):
+            e = idx[t, j]
+            rows[i, j] = seg[e] + pp[t, j] - off[e]
+    return rows
+
+
+def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=False, route_all=True):
+    w, T, k, E, H, F = gw.w, gw.w["T"], gw.w["k"], gw.w["E"], gw.w["H"], gw.w["F"]
+    out = gw.forward()
+    assert moe.moe_poll_device_status(gw.ws) == 0
+    gpu_out = parity.bf16_to_f64(out)
+    r = gw.routing()
+    if tokens is None:
+        tokens = np.arange(T)
+    tokens = np.asarray(tokens, np.int64)
+    stats = {}
+
+    # routing: all tokens (or the sample), near-ties certified against the bound
+    rows_r = np.arange(T) if route_all else tokens
+    x_r = synth.x_rows(w, rows_r)
+    ro = oracle.route(x_r, synth.router_weight(w), synth.router_bias(w), k)
+    ties_all = parity.check_topk(r["idx"][rows_r], ro["idx"], ro["keys"], ro["absdot"])
+    stats["near_ties"] = len(ties_all)
+    same = [i for i in range(len(rows_r)) if i not in ties_all]
+    assert np.abs(r["w"][rows_r][same] - ro["w"][same]).max() <= parity.W_TOL
+
+    # dispatch of the GPU's own indices: bit-exact
+    d = oracle.dispatch(r["idx"], E)
+    for key in ("counts", "offsets", "perm", "pair_pos"):
+        assert np.array_equal(r[key].ravel(), d[key].ravel()), key
+
+    # activation codes of the sample at every expert-grouped row: bit-exact
+    xq = oracle.quantize_x(w, synth.x_rows(w, tokens), mx_mode)
+    prow = padded_rows_of(r, tokens, k)
+    R = gw.layout["R"]
+    nv = w["fmt"] == "nvfp4"
+    cb, bs = (H // 2, 16) if nv else (H, 32)
+    codes = gw.ws_view("xq_codes", torch.uint8, R * cb).view(R, cb)
+    scales = gw.ws_view("xq_scales", torch.uint8, R * (H // bs)).cpu().numpy()
+    gcodes = codes[torch.from_numpy(prow.ravel()).cuda()].cpu().numpy().reshape(len(tokens), k, cb)
+    gsc = untile_scales(scales, R, H // bs)[prow.ravel()].reshape(len(tokens), k, H // bs)
+    for j in range(k):
+        assert np.array_equal(gcodes[:, j], xq[0])
+        assert np.array_equal(gsc[:, j], xq[1])
+    if nv:
+        gg = gw.ws_view("xq_global", torch.float32, R).cpu().numpy()[prow]
+        for j in range(k):
+            assert np.array_equal(gg[:, j].view(np.uint32), xq[2].view(np.uint32))
+
+    # the layer on the sample, with the GPU's choice on certified near-ties
+    pos = {int(t): i for i, t in enumerate(rows_r)}
+    override = {i: ties_all[pos[int(t)]] for i, t in enumerate(tokens) if pos.get(int(t)) in ties_all}
+    res = oracle.moe_layer(w, tokens, idx_override=override, cap=cap, mx_mode=mx_mode, keep_pairs=check_h)
+    if out_rowwise:
+        stats["literal"] = parity.out_error(gpu_out[tokens], res["out"])[0] / parity.out_error(
+            gpu_out[tokens], res["out"])[1]
+        stats["rowwise"] = parity.check_output_rowwise(gpu_out[tokens], res["out"])
+    else:
+        stats["err_over_rms"] = parity.check_output(gpu_out[tokens], res["out"])
+
+    if check_h:
+        # h = bf16(silu(cap g) cap u): near-exact (GEMM accumulation order differs)
+        hbuf = gw.ws_view("h_bf16", torch.int16, R * F).view(R, F)
+        flips, total = 0, 0
+        od = res["dispatch"]
+        for e, pr in res["pairs"].items():
+            lo, hi = od["offsets"][e], od["offsets"][e + 1]
+            pids = od["perm"][lo:hi]
+            grow = prow[pids // k, pids % k]
+            gh = hbuf[torch.from_numpy(grow).cuda()].cpu().numpy().view(np.uint16)
+            flips += int((gh != pr["h_bf16"]).sum())
+            total += gh.size
+        stats["h_flip_rate"] = flips / max(total, 1)
+        assert stats["h_flip_rate"] < 0.01
+    return stats
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_small_layer_all_tokens(name):
+    gw = GpuWorkload(SMALL[name], torch)
+    st = check_layer(gw)
+    print(name, st)
+
+
+def test_small_layer_uncapped_and_mx_round_up():
+    gw = GpuWorkload("tiny_mxfp8", torch, cap=0.0, mx_scale_mode=1)
+    print(check_layer(gw, cap=0.0, mx_mode=1))
+    gw = GpuWorkload(SMALL["tiny_nvfp4"], torch, cap=0.0)
+    print(check_layer(gw, cap=0.0))
+
+
+def test_staged_calls_equal_forward():
+    gw = GpuWorkload(SMALL["ragged_mxfp8"], torch)
+    ref = gw.forward().clone()
+    c, T, k, E, H = gw.cfg, gw.w["T"], gw.w["k"], gw.w["E"], gw.w["H"]
+    dev = "cuda"
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, k), dtype=torch.float32, device=dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    perm = torch.empty(T * k, dtype=torch.int32, device=dev)
+    pp = torch.empty((T, k), dtype=torch.int32, device=dev)
+    y = torch.empty((T * k, H), dtype=torch.float32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty_like(gw.ws)
+    moe.moe_route(c, gw.x, gw.w_router, gw.bias, idx, wts, ws)
+    moe.moe_dispatch(c, idx, counts, offsets, perm, pp, ws)
+    moe.moe_expert_ffn(c, gw.x, idx, offsets, perm, pp, gw.qw["gate"], gw.qw["up"], gw.qw["down"], y, ws)
+    moe.moe_combine(c, y, wts, pp, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    # deterministic across runs
+    again = gw.forward()
+    assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
+
+
+def sample_tokens(w, n, extra=()):
+    rng = np.random.default_rng(1000 + w["seed"])
+    toks = set(int(t) for t in extra)
+    toks.add(0)
+    toks.add(w["T"] - 1)
+    while len(toks) < n:
+        toks.add(int(rng.integers(0, w["T"])))
+    return np.array(sorted(toks))
+
+
+FULL = ["decode64_nvfp4", "decode192_mxfp8_outliers", "prefill4096_nvfp4", "prefill16384_mxfp8_zipf"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    w = synth.WORKLOADS[name]
+    gw = GpuWorkload(name, torch)
+    extra = []
+    if w["outlier_frac"] > 0:
+        extra = list(np.nonzero(synth.outlier_flags(w))[0])
+    n = 6 if w["T"] > 1000 else 8
+    tokens = sample_tokens(w, n, extra)
+    st = check_layer(gw, tokens, out_rowwise=w["outlier_frac"] > 0, route_all=w["T"] <= 4096)
+    print(name, st)
+    del gw
+    torch.cuda.empty_cache()

@@ -1,0 +1,368 @@
+"""Benchmark of the routed block-scaled MoE layer on GB300.
+
+One step = one moe_forward over one seeded token batch (router, dispatch,
+activation quantisation, GEMM1 + capped SwiGLU, h quantisation, GEMM2,
+combine), inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Multi-GPU: token-sharded replicas (each rank runs its own batch and holds all
+experts; no collective on the data path); value = all ranks' tokens / the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MoE-layer tokens/s & µs/layer; % HBM roofline (decode) / % FP4-FP8 peak (prefill)")
+DEFAULT_WORKLOAD = "decode64_nvfp4"
+UNIT = "tokens/s"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], source="measured")
+    return dict(hbm_gbs=6800.0, source="fallback")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("moe_gemm.cu", "moe_common.cuh"):
+        h.update(open(os.path.join(ROOT, "block_scaled_fp4_route_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes of one launch of each expert GEMM
+# ----------------------------------------------------------------------------
+
+def gemm_bytes(w: dict, n_touched: int):
+    """Algorithmic HBM bytes of GEMM1 (gate+up) and GEMM2 (down) per launch:
+    the encoded weights of the touched experts (each read once), the encoded
+    activations read and the output written."""
+    H, F, P = w["H"], w["F"], w["T"] * w["k"]
+    nv = w["fmt"] == "nvfp4"
+    bpe = 0.5 + 1 / 16 if nv else 1 + 1 / 32          # bytes per element incl. block scales
+    glob = 4 if nv else 0
+    g1 = n_touched * (2 * (F * H * bpe + glob)) + P * (H * bpe + glob) + P * F * 2
+    g2 = n_touched * (H * F * bpe + glob) + P * (F * bpe + glob) + P * H * 4
+    return g1, g2
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.window = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "100", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.p.stdout:
+            self.samples.append((time.time(), [s.strip() for s in line.split(",")]))
+
+    def start(self):
+        self.window = [time.time(), None]
+
+    def stop(self):
+        self.window[1] = time.time()
+        if self.p:
+            time.sleep(0.25)
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+
+    def summary(self):
+        if not self.p:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        t0, t1 = self.window
+        rows = [r for (t, r) in self.samples if t0 <= t <= t1 + 0.1]
+        if not rows:   # timed region shorter than the sampling period: nearest samples
+            rows = [r for (t, r) in self.samples if t0 - 0.3 <= t <= t1 + 0.3]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+class OracleSample:
+    """The oracle as it stands on a bounded sample of a workload: given the
+    inputs and the encoded experts (prepared outside the timing), one call
+    routes the sample tokens, dispatches them, runs every (token, expert) pair
+    through the quantised FFN (weights decoded on the fly) and combines."""
+
+    def __init__(self, w: dict, n_tokens: int, max_pairs=None):
+        import oracle
+        import synth
+        self.oracle, self.w = oracle, w
+        rng = np.random.default_rng(77)
+        self.tokens = np.sort(rng.choice(w["T"], size=min(n_tokens, w["T"]), replace=False))
+        self.inputs = (synth.x_rows(w, self.tokens), synth.router_weight(w), synth.router_bias(w))
+        self.max_pairs = max_pairs
+        res = oracle.route(self.inputs[0], self.inputs[1], self.inputs[2], w["k"])
+        order = oracle.dispatch(res["idx"], w["E"])
+        P = len(self.tokens) * w["k"] if max_pairs is None else max_pairs
+        experts = sorted(set(int(e) for e in res["idx"].ravel()[order["perm"][:P]]))
+        self.cache = {e: oracle.quantized_expert(w, e) for e in experts}
+        self.pairs = P
+
+    def run(self):
+        return self.oracle.moe_layer(self.w, self.tokens, inputs=self.inputs, expert_cache=self.cache,
+                                     max_pairs=self.max_pairs)
+
+    def tokens_per_call(self) -> float:
+        return self.pairs / self.w["k"]
+
+
+def cpu_cores() -> int:
+    import oracle
+    return oracle.num_threads()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    # size one step so that warmup + steps take about two minutes of CPU
+    probe = OracleSample(w, 1, max_pairs=1)
+    t0 = time.perf_counter()
+    probe.run()
+    t_pair = time.perf_counter() - t0
+    n_pairs = int(max(1, min(w["k"], 120.0 / max(1, args.steps + args.warmup) / max(t_pair, 1e-6))))
+    samp = OracleSample(w, 1, max_pairs=n_pairs)
+    for _ in range(args.warmup):
+        samp.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        samp.run()
+    dt = time.perf_counter() - t0
+    value = samp.tokens_per_call() * args.steps / dt
+    cores = cpu_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": args.workload, **{k: w[k] for k in ("T", "H", "E", "k", "F", "fmt")}},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"per step: routing of 1 token of {args.workload} and {n_pairs} of its "
+                                       f"{w['k']} expert FFN pairs (weights decoded in fp64), counted as "
+                                       f"{n_pairs}/{w['k']} token"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    import block_scaled_fp4_route_gb300 as moe
+    import synth
+    from synth.gpu_workload import GpuWorkload
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+
+    w = synth.WORKLOADS[args.workload]
+    T, k = w["T"], w["k"]
+    gw = GpuWorkload(args.workload, torch)
+    st = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        gw.forward()
+    torch.cuda.synchronize()
+    status = moe.moe_poll_device_status(gw.ws)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warmup")
+    counts = gw.routing()["counts"]
+    n_touched = int((counts > 0).sum())
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_index = int(vis.split(",")[local]) if vis else local
+    clocks = ClockSampler(gpu_index)
+    time.sleep(0.3)
+
+    # ---- timed region: K steps, inputs resident (touched expert weights >> L2) ----
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(st)
+    for _ in range(args.steps):
+        gw.forward()
+    end.record(st)
+    torch.cuda.synchronize()
+    clocks.stop()
+    barrier()
+    ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+    launches_per_step = 10
+
+    # ---- per-stage device times (events between the stages, same stream) ----
+    n_prof = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(n_prof)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(st)
+    for i in range(n_prof):
+        moe.moe_forward_profiled(gw.cfg, gw.x, gw.w_router, gw.bias, gw.qw["gate"], gw.qw["up"], gw.qw["down"],
+                                 gw.out, gw.ws, evs[i])
+    torch.cuda.synchronize()
+    stage_ms = {n: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs]))
+                for i, n in enumerate(moe.STAGE_NAMES)}
+
+    # ---- end to end through host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        x_host = gw.x.cpu().pin_memory()
+        out_host = torch.empty_like(gw.out, device="cpu").pin_memory()
+        x_dev = torch.empty_like(gw.x)
+        n_e2e = min(args.steps, 500)
+        for _ in range(3):
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_forward(gw.cfg, x_dev, gw.w_router, gw.bias, gw.qw["gate"], gw.qw["up"], gw.qw["down"],
+                            gw.out, gw.ws)
+            out_host.copy_(gw.out, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            x_dev.copy_(x_host, non_blocking=True)
+            moe.moe_forward(gw.cfg, x_dev, gw.w_router, gw.bias, gw.qw["gate"], gw.qw["up"], gw.qw["down"],
+                            gw.out, gw.ws)
+            out_host.copy_(gw.out, non_blocking=True)
+            st.synchronize()
+        dt = time.perf_counter() - t0
+        if dist:
+            t = torch.tensor([dt], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * T * n_e2e / dt, "unit": UNIT, "h2d_bytes_per_step": int(gw.x.numel() * 2),
+               "d2h_bytes_per_step": int(gw.out.numel() * 2), "steps": n_e2e}
+
+    # ---- roofline of the dominant kernel (GEMM1: gate/up + SwiGLU) ----
+    pk = peaks()
+    g1_bytes, g2_bytes = gemm_bytes(w, n_touched)
+    g1_ms = stage_ms["gemm1_gate_up_swiglu"]
+    achieved = g1_bytes / (g1_ms / 1e3) / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        tr = json.load(open(TRAFFIC_FILE))
+        ent = tr.get(args.workload, {}).get("gemm1")
+        if ent and tr.get("source_sha") == kernel_source_sha():
+            traffic = ent
+    roofline = {"bound": "hbm", "kernel": "gemm1_gate_up_swiglu", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                "peak_source": pk["source"], "algorithmic_bytes": g1_bytes,
+                "gemm2": {"achieved": g2_bytes / (stage_ms["gemm2_down"] / 1e3) / 1e9,
+                          "frac": g2_bytes / (stage_ms["gemm2_down"] / 1e3) / 1e9 / pk["hbm_gbs"],
+                          "algorithmic_bytes": g2_bytes}}
+    layer_bytes = g1_bytes + g2_bytes + w["E"] * w["H"] * 2 + T * w["H"] * 4
+    layer = {"us_per_layer": ms_per_step * 1e3, "alg_bytes": layer_bytes,
+             "hbm_frac_whole_layer": layer_bytes / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"],
+             "stage_ms": stage_ms}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        samp = OracleSample(w, 8)
+        t0 = time.perf_counter()
+        samp.run()
+        dt = time.perf_counter() - t0
+        cpu = {"value": samp.tokens_per_call() / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"8 tokens of {args.workload} through the whole layer ({samp.pairs} expert pairs, "
+                         f"{len(samp.cache)} experts decoded on the fly), {dt:.2f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": w["fmt"], "data": "synthetic",
+                "config": {"workload": args.workload, "T": T, "H": w["H"], "E": w["E"], "k": k, "F": w["F"],
+                           "fmt": w["fmt"], "touched_experts": n_touched, "parallelism": f"replicas{world}",
+                           "l2": f"inputs larger than L2: {layer_bytes / 1e9:.2f} GB of touched expert weights "
+                                 f"per step against a 129 MB L2; no flush"},
+                "layer": layer, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clocks.summary(), "gpu_launches": launches_per_step * args.steps}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -21,7 +21,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_ARCH", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_DEVICE_TIMEOUT"}
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
-            "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
+            "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
             "moe_status_string"]
 
 
@@ -71,6 +71,8 @@ def lib():
             L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, sz, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
             L.moe_forward.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, sz, P]
+            L.moe_forward_profiled.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, sz, P,
+                                               ctypes.POINTER(ctypes.c_void_p)]
             L.moe_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64, i64, i64, ctypes.c_int,
                                        P, P, P, P]
             L.moe_pack_scales.argtypes = [P, i64, i64, P, P]
@@ -161,6 +163,18 @@ def moe_forward(cfg, x, w_router, bias, gate, up, down, out, ws, stream=None):
     _check("moe_forward", lib().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
                                             ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), _ptr(out),
                                             _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+NUM_STAGES = 7
+STAGE_NAMES = ["router", "dispatch", "quant_x", "gemm1_gate_up_swiglu", "quant_h", "gemm2_down", "combine"]
+
+
+def moe_forward_profiled(cfg, x, w_router, bias, gate, up, down, out, ws, events, stream=None):
+    """events: NUM_STAGES + 1 torch.cuda.Event objects (created with timing)."""
+    arr = (ctypes.c_void_p * (NUM_STAGES + 1))(*[e.cuda_event for e in events])
+    _check("moe_forward_profiled", lib().moe_forward_profiled(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), ctypes.byref(gate), ctypes.byref(up),
+        ctypes.byref(down), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream), arr))
 
 
 def moe_quantize(fmt, src, codes, scales, global_scale=None, group_rows=0, layout=SCALES_TILED, mx_scale_mode=0,

@@ -120,10 +120,16 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(ws) + off);
 }
 
-// Expert FFN after the tile plan exists in the workspace.
+void mark(cudaEvent_t* ev, int i, cudaStream_t st) {
+  if (ev) cudaEventRecord(ev[i], st);
+}
+
+// Expert FFN after the tile plan exists in the workspace.  ev (optional)
+// receives the stage boundaries 2..5 (x quantisation, GEMM1, h quantisation,
+// GEMM2).
 moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
                     const int32_t* perm, const int32_t* pair_pos, const moe_qweight* gate, const moe_qweight* up,
-                    const moe_qweight* down, float* y, void* ws, cudaStream_t st) {
+                    const moe_qweight* down, float* y, void* ws, cudaStream_t st, cudaEvent_t* ev = nullptr) {
   moe_ws_layout L;
   ws_layout(c, &L);
   const int64_t R = L.R;
@@ -139,6 +145,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   const int32_t* nrt = at<int32_t>(ws, L.n_row_tiles);
   uint32_t* status = at<uint32_t>(ws, L.status);
 
+  mark(ev, 2, st);
   cudaError_t e = launch_quant_x(c, x, idx, offsets, pair_pos, seg, xq, xs, xg, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
@@ -169,8 +176,10 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g1.h_out = h;
   g1.status = status;
   g1.num_sms = sms;
+  mark(ev, 3, st);
   if (launch_gemm(g1, st) != cudaSuccess) return MOE_ERR_CUDA;
 
+  mark(ev, 4, st);
   if (launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st) != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmLaunch g2{};
@@ -190,6 +199,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g2.y_out = y;
   g2.status = status;
   g2.num_sms = sms;
+  mark(ev, 5, st);
   if (launch_gemm(g2, st) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -319,9 +329,10 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const flo
       launch_combine(*cfg, y_perm_dev, topk_w_dev, pair_pos_dev, (__nv_bfloat16*)out_dev, (cudaStream_t)stream));
 }
 
-moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev, const float* bias_dev,
-                       const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down, void* out_dev,
-                       void* ws_dev, size_t ws_bytes, void* stream) {
+static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                               const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
+                               const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes, void* stream,
+                               cudaEvent_t* ev) {
   moe_status s = check_cfg(cfg);
   if (s == MOE_OK) s = check_ptrs({x_dev, w_router_dev, bias_dev, out_dev});
   if (s == MOE_OK) s = check_qw(cfg, gate);
@@ -343,16 +354,40 @@ moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_r
   int32_t* pair_pos = at<int32_t>(ws_dev, L.pair_pos);
   uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
   float* y = at<float>(ws_dev, L.y_perm);
+  mark(ev, 0, st);
   if (launch_router(c, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                    at<float>(ws_dev, L.logits), idx, w, st) != cudaSuccess ||
-      launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st) != cudaSuccess ||
+                    at<float>(ws_dev, L.logits), idx, w, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  mark(ev, 1, st);
+  if (launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st) != cudaSuccess ||
       launch_scan_plan(c, counts, nullptr, offsets, at<int32_t>(ws_dev, L.seg_start), at<RowTile>(ws_dev, L.tiles),
                        at<int32_t>(ws_dev, L.n_row_tiles), at<uint32_t>(ws_dev, L.status), st) != cudaSuccess ||
       launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st);
+  s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st, ev);
   if (s != MOE_OK) return s;
-  return cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st));
+  mark(ev, 6, st);
+  s = cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st));
+  mark(ev, 7, st);
+  return s;
+}
+
+moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev, const float* bias_dev,
+                       const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down, void* out_dev,
+                       void* ws_dev, size_t ws_bytes, void* stream) {
+  return forward_impl(cfg, x_dev, w_router_dev, bias_dev, gate, up, down, out_dev, ws_dev, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_profiled(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                                const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
+                                const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes, void* stream,
+                                void* const* events) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_NUM_STAGES + 1; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  cudaEvent_t ev[MOE_NUM_STAGES + 1];
+  for (int i = 0; i < MOE_NUM_STAGES + 1; ++i) ev[i] = (cudaEvent_t)events[i];
+  return forward_impl(cfg, x_dev, w_router_dev, bias_dev, gate, up, down, out_dev, ws_dev, ws_bytes, stream, ev);
 }
 
 moe_status moe_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32, const void* src_dev, int64_t rows,

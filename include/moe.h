@@ -182,6 +182,20 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x_dev, const v
                        const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes,
                        void* stream);
 
+/* moe_forward, also recording events[i] (cudaEvent_t handles, created by the
+ * caller) on `stream` at the start of stage i and events[MOE_NUM_STAGES] after
+ * the last, so that the caller can time each stage:
+ *   0 router (logits, top-k)      1 dispatch (bitmap, scan, scatter)
+ *   2 x quantisation              3 GEMM1 gate/up + capped SwiGLU
+ *   4 h quantisation              5 GEMM2 down
+ *   6 combine
+ * Same results as moe_forward. */
+#define MOE_NUM_STAGES 7
+MOE_API moe_status moe_forward_profiled(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                                        const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
+                                        const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes,
+                                        void* stream, void* const* events);
+
 /* Block quantiser [MI 1 and 5.2: weight sync re-encodes experts in the layer's
  * format and recomputes NVFP4 global scales].  Encodes rows x cols values.
  *   src_is_fp32: 1 = src fp32, 0 = src bf16.

@@ -271,12 +271,16 @@ def quantize_x(w: dict, x_bf16: np.ndarray, mx_mode: int = 0):
 
 
 def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mode: int = 0,
-              expert_cache=None, keep_pairs: bool = False):
+              expert_cache=None, keep_pairs: bool = False, inputs=None, max_pairs=None):
     """Run the whole layer for the given token rows (default: all T).
 
     idx_override: optional {token_row_index_in_sample: int32[k]} replacing the
     oracle's own top-k for certified near-tie tokens.
     expert_cache: optional dict e -> quantized_expert(...) to reuse encodings.
+    inputs: optional (x rows of the tokens, W_r, bias) already generated.
+    max_pairs: compute only the first max_pairs (token, slot) pairs of the
+    sample's dispatch order (a bounded sample of the work; the output rows are
+    then partial sums).
     Returns dict with x codes, routing, dispatch (over the sample), y per pair
     and the fp64 output [n, H].
     """
@@ -285,9 +289,12 @@ def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mod
     if tokens is None:
         tokens = np.arange(T)
     tokens = np.asarray(tokens, np.int64)
-    x = synth.x_rows(w, tokens)
-    wr = synth.router_weight(w)
-    bias = synth.router_bias(w)
+    if inputs is None:
+        x = synth.x_rows(w, tokens)
+        wr = synth.router_weight(w)
+        bias = synth.router_bias(w)
+    else:
+        x, wr, bias = inputs
     r = route(x, wr, bias, k)
     idx = r["idx"].copy()
     if idx_override:
@@ -301,8 +308,11 @@ def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mod
     P = len(tokens) * k
     y = np.zeros((P, H), np.float64)
     pairs = {}
+    budget = P if max_pairs is None else int(max_pairs)
     for e in np.nonzero(d["counts"])[0]:
         e = int(e)
+        if d["offsets"][e] >= budget:
+            break
         if expert_cache is not None and e in expert_cache:
             q = expert_cache[e]
         else:
@@ -310,7 +320,7 @@ def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mod
             if expert_cache is not None:
                 expert_cache[e] = q
         dec = decoded_expert(w, q)
-        lo, hi = d["offsets"][e], d["offsets"][e + 1]
+        lo, hi = d["offsets"][e], min(d["offsets"][e + 1], budget)
         pids = d["perm"][lo:hi]
         rows = pids // k
         res = expert_ffn(w["fmt"], dec["gate"], dec["up"], dec["down"], a_all[rows], cap=cap, mx_mode=mx_mode)

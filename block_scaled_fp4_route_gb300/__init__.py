@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
-            "moe_status_string"]
+            "moe_route_noalloc", "moe_status_string"]
 
 
 class MoeError(RuntimeError):
@@ -67,6 +67,7 @@ def lib():
             qwp = ctypes.POINTER(moe_qweight)
             L.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(sz)]
             L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
+            L.moe_route_noalloc.argtypes = [cfgp, P, P, P, P, P, P]
             L.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
             L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, sz, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
@@ -139,6 +140,14 @@ def moe_workspace_layout(cfg: moe_config) -> dict:
 def moe_route(cfg, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
     _check("moe_route", lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
                                         _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_route_noalloc(cfg, x, w_router, bias, topk_idx, topk_w, stream=None):
+    """moe_route without a workspace, for callers that cannot allocate device
+    memory when they route: the library's own fixed scratch is used instead
+    (see include/moe.h for its size limit and the one-time set-up)."""
+    _check("moe_route_noalloc", lib().moe_route_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
+                                                        _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
 
 
 def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None):

@@ -8,6 +8,8 @@
 // added with Kahan compensation (within a K split and again across splits).
 // Hence |l_gpu - l| <= (gamma_31 + 3u) * sum_h |x_h w_eh| <= 40u * sum|x w|,
 // u = 2^-24, which the top-k parity check uses to certify near-ties.
+#include <mutex>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -244,4 +246,83 @@ cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __n
   return cudaGetLastError();
 }
 
+// ----------------------------------------------------------------------------
+// Router without a caller-provided workspace (moe_route_noalloc).
+//
+// Some callers cannot allocate device memory at the point where they route
+// tokens: for example code running inside a captured CUDA graph region, a
+// plugin that has no access to its host framework's allocator, or a runtime
+// that forbids allocation after start-up.  For them the router's only scratch
+// (the fp32 logits partials) lives in a fixed array that the CUDA module
+// reserves when the library is loaded, so the call itself allocates nothing.
+// ----------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchFloats = (size_t)1 << 20;  // 4 MiB of logits partials
+static __device__ __align__(256) float g_route_scratch[kNoAllocScratchFloats];
+
+struct NoAllocDevice {
+  bool ready = false;
+  moe_status status = MOE_OK;
+  float* scratch = nullptr;  // device address of g_route_scratch on that device
+};
+NoAllocDevice g_noalloc[64];
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: look up the device address of
+// the scratch array (the host-side name is only a stand-in for it).
+moe_status noalloc_setup(float** scratch) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      d.status = MOE_ERR_CUDA;
+    } else if (!(major == 10 && minor == 3)) {
+      d.status = MOE_ERR_ARCH;
+    } else {
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_route_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        d.status = MOE_ERR_CUDA;
+      } else {
+        d.scratch = static_cast<float*>(p);
+        d.status = MOE_OK;
+      }
+    }
+    d.ready = true;
+  }
+  *scratch = d.scratch;
+  return d.status;
+}
+
+}  // namespace
+
 }  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                                        const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,
+                                        void* stream) {
+  using namespace moe;
+  size_t ws_bytes = 0;
+  moe_status s = moe_workspace_size(cfg, &ws_bytes);  // validates the configuration
+  if (s != MOE_OK) return s;
+  const void* ptrs[] = {x_dev, w_router_dev, bias_dev, topk_idx_dev, topk_w_dev};
+  for (const void* p : ptrs) {
+    if (!p) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MOE_ERR_MISALIGNED;
+  }
+  const size_t need = (size_t)router_splits(*cfg) * (size_t)cfg->T * (size_t)cfg->E;
+  if (need > kNoAllocScratchFloats) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  float* scratch = nullptr;
+  s = noalloc_setup(&scratch);
+  if (s != MOE_OK) return s;
+  // every logits partial the top-k kernel reads is written first by the
+  // logits kernel of the same call, so nothing needs clearing
+  cudaError_t e = launch_router(*cfg, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
+                                scratch, topk_idx_dev, topk_w_dev, (cudaStream_t)stream);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -133,6 +133,27 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x_dev, const voi
                      const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,
                      void* ws_dev, size_t ws_bytes, void* stream);
 
+/* The router of moe_route for callers that cannot allocate device memory
+ * when they route (inside a captured CUDA graph region, in a plugin without
+ * access to its host framework's allocator, or in a runtime that forbids
+ * allocation after start-up).  The pages have no counterpart: it is an
+ * interface convenience, with the same arguments and results as moe_route
+ * but no workspace.
+ *   Its scratch (the fp32 logits partials) is a fixed 4 MiB array inside the
+ *   library, reserved on every device that loads the library until the
+ *   process exits.  Configurations whose partials do not fit return
+ *   MOE_ERR_WORKSPACE_TOO_SMALL: splits * T * E <= 2^20 floats, where splits
+ *   is 8 (or the largest power of two <= 8 with H % (64*splits) == 0) for
+ *   T <= 256 and 1 above; e.g. up to T = 256 at E = 384, H = 4608.
+ *   The first call on a device looks up the array's device address; make that
+ *   first call before any stream capture.
+ *   Every call uses the same array: calls that may overlap on the GPU (other
+ *   streams, other threads) race and must be serialised by the caller.  No
+ *   call allocates or frees memory. */
+MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
+                                     const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,
+                                     void* stream);
+
 /* Token dispatch [CB MegaMoE: dispatch is a step of the fused unit]: groups
  * the P = T*k pairs (t, j)
  * by expert, and within an expert by token.

@@ -43,7 +43,7 @@ class moe_qweight(ctypes.Structure):
 
 
 _LAYOUT_FIELDS = ["status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "pair_pos", "bitmap",
-                  "seg_start", "tiles", "n_row_tiles", "xq_codes", "xq_scales", "xq_global", "h_bf16", "hq_codes",
+                  "seg_start", "tiles", "rt_base", "xq_codes", "xq_scales", "xq_global", "h_bf16", "hq_codes",
                   "hq_scales", "hq_global", "y_perm", "total"]
 
 

@@ -142,7 +142,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   float* hg = at<float>(ws, L.hq_global);
   const int32_t* seg = at<int32_t>(ws, L.seg_start);
   const RowTile* tiles = at<RowTile>(ws, L.tiles);
-  const int32_t* nrt = at<int32_t>(ws, L.n_row_tiles);
+  const int32_t* rtb = at<int32_t>(ws, L.rt_base);
   uint32_t* status = at<uint32_t>(ws, L.status);
 
   mark(ev, 2, st);
@@ -170,7 +170,8 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g1.gA1 = up->global_scale;
   g1.gB = xg;
   g1.tiles = tiles;
-  g1.n_row_tiles = nrt;
+  g1.rt_base = rtb;
+  g1.E = c.E;
   g1.NA = c.F;
   g1.K = c.H;
   g1.h_out = h;
@@ -189,11 +190,14 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g2.tmA1 = &md;
   g2.tmB = &mh;
   g2.sfA0 = (const uint8_t*)down->scales;
+  g2.sfA1 = (const uint8_t*)down->scales;
   g2.sfB = hs;
   g2.gA0 = down->global_scale;
+  g2.gA1 = down->global_scale;
   g2.gB = hg;
   g2.tiles = tiles;
-  g2.n_row_tiles = nrt;
+  g2.rt_base = rtb;
+  g2.E = c.E;
   g2.NA = c.H;
   g2.K = c.F;
   g2.y_out = y;
@@ -227,13 +231,13 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
   L->bitmap = take(E * W * 4);
   L->seg_start = take((E + 1) * 4);
   L->tiles = take(max_row_tiles(c) * sizeof(RowTile));
-  L->n_row_tiles = take(16);
+  L->rt_base = take((E + 1) * 4);
   L->xq_codes = take(R * code_bytes(c.fmt, c.H));
-  L->xq_scales = take(R * (c.H / bs));
+  L->xq_scales = take(act_scale_bytes(R, c.H / bs));
   L->xq_global = take(R * 4);
   L->h_bf16 = take(R * c.F * 2);
   L->hq_codes = take(R * code_bytes(c.fmt, c.F));
-  L->hq_scales = take(R * (c.F / bs));
+  L->hq_scales = take(act_scale_bytes(R, c.F / bs));
   L->hq_global = take(R * 4);
   L->y_perm = take(P * c.H * 4);
   L->total = off;
@@ -289,7 +293,7 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int3
   uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
   if (launch_dispatch(*cfg, topk_idx_dev, counts_dev, offsets_dev, perm_dev, pair_pos_dev, bm, st) != cudaSuccess ||
       launch_scan_plan(*cfg, counts_dev, nullptr, offsets_dev, at<int32_t>(ws_dev, L.seg_start),
-                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.n_row_tiles), nullptr, st) != cudaSuccess ||
+                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.rt_base), nullptr, st) != cudaSuccess ||
       launch_dispatch_scatter(*cfg, topk_idx_dev, bm, offsets_dev, perm_dev, pair_pos_dev, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -312,7 +316,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_
   ws_layout(*cfg, &L);
   cudaStream_t st = (cudaStream_t)stream;
   if (launch_scan_plan(*cfg, nullptr, offsets_dev, nullptr, at<int32_t>(ws_dev, L.seg_start),
-                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.n_row_tiles),
+                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.rt_base),
                        at<uint32_t>(ws_dev, L.status), st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return ffn_core(*cfg, sms, (const __nv_bfloat16*)x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, gate, up,
@@ -361,7 +365,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   mark(ev, 1, st);
   if (launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st) != cudaSuccess ||
       launch_scan_plan(c, counts, nullptr, offsets, at<int32_t>(ws_dev, L.seg_start), at<RowTile>(ws_dev, L.tiles),
-                       at<int32_t>(ws_dev, L.n_row_tiles), at<uint32_t>(ws_dev, L.status), st) != cudaSuccess ||
+                       at<int32_t>(ws_dev, L.rt_base), at<uint32_t>(ws_dev, L.status), st) != cudaSuccess ||
       launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st, ev);

@@ -7,7 +7,7 @@
 //   1. one CTA per expert builds the expert's token bitmap in shared memory
 //      from topk_idx and counts its pairs;
 //   2. one CTA scans counts -> offsets, padded segment starts (each expert's
-//      rows begin at a multiple of 128) and the list of 128-row tiles;
+//      rows begin at a multiple of kNT) and the list of kNT-row tiles;
 //   3. one CTA per expert ranks its tokens from the bitmap (popcount prefix)
 //      and writes perm / pair_pos.
 #include "moe_common.cuh"
@@ -79,7 +79,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* sh) {
 __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ counts,
                                                     const int32_t* __restrict__ offsets_in, int E,
                                                     int32_t* __restrict__ offsets_out, int32_t* __restrict__ seg_start,
-                                                    RowTile* __restrict__ tiles, int32_t* __restrict__ n_row_tiles,
+                                                    RowTile* __restrict__ tiles, int32_t* __restrict__ rt_base,
                                                     uint32_t* __restrict__ status) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
@@ -92,25 +92,26 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
     if (e < E) offsets_out[e] = off;
     if (e == 0) offsets_out[E] = tot;
   }
-  int padded = (c + 127) & ~127;
+  int nrt = (c + kNT - 1) / kNT;
+  int padded = nrt * kNT;
   int ptot;
   int seg = block_exclusive_scan(padded, &ptot, sh);
   if (e < E) seg_start[e] = seg;
   if (e == 0) seg_start[E] = ptot;
-  int nrt = (c + 127) >> 7;
   int rtot;
   int rt0 = block_exclusive_scan(nrt, &rtot, sh);
   if (e < E) {
+    rt_base[e] = rt0;
     for (int i = 0; i < nrt; ++i) {
       RowTile t;
       t.e = e;
-      t.row = seg + 128 * i;
-      t.n_valid = min(128, c - 128 * i);
-      t.canon = off + 128 * i;
+      t.row = seg + kNT * i;
+      t.n_valid = min(kNT, c - kNT * i);
+      t.canon = off + kNT * i;
       tiles[rt0 + i] = t;
     }
   }
-  if (e == 0) *n_row_tiles = rtot;
+  if (e == 0) rt_base[E] = rtot;
 }
 
 __global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __restrict__ idx, int T, int k,
@@ -160,9 +161,9 @@ cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, con
 }
 
 cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
-                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* n_row_tiles,
+                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
                              uint32_t* status, cudaStream_t st) {
-  k_scan_plan<<<1, 1024, 0, st>>>(counts, offsets_in, c.E, offsets_out, seg_start, tiles, n_row_tiles, status);
+  k_scan_plan<<<1, 1024, 0, st>>>(counts, offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status);
   return cudaGetLastError();
 }
 

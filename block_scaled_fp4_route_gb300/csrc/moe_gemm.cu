@@ -7,17 +7,25 @@
 // (kind::mxf4nvf4, E2M1 x E2M1 with UE4M3 scales per 16) and MXFP8
 // (kind::mxf8f6f4, E4M3 x E4M3 with UE8M0 scales per 32).
 //
-// Tile = 128 weight rows (MMA M) x up to 128 token rows of one expert (MMA N,
-// rounded up to 16) x the full K, "swap-AB": the weights fill M so that a
-// decode batch with one or two tokens per expert wastes no weight bytes.
-//   GEMM1 (gated):  A0 = W_gate rows, A1 = W_up rows (two accumulators),
+// A tile holds two 128-row weight blocks (two MMAs with M = 128 sharing the
+// token operand) x up to kNT = 64 token rows of one expert (MMA N, rounded up
+// to 16) x the full K, "swap-AB": the weights fill M so a decode batch with
+// one or two tokens per expert wastes no weight bytes, and each pipeline
+// stage carries 32 KB of weights.
+//   GEMM1 (gated):  A0 = 128 W_gate rows, A1 = the same 128 W_up rows,
 //                   epilogue h = bf16(silu(cap g) * cap u)
-//   GEMM2:          A0 = W_down rows, epilogue y = acc * g_w * g_h (fp32)
+//   GEMM2:          A0, A1 = 256 consecutive W_down rows,
+//                   epilogue y = acc * g_w * g_h (fp32)
+// Tiles are walked expert by expert, then weight-row block, then token block,
+// so CTAs running side by side share an expert's weights and activations in
+// L2.  The TMEM accumulator is double-buffered: the epilogue of one tile runs
+// while the MMAs of the next one accumulate into the other buffer.
 // Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
 // warp 2 = TMEM allocator, warps 4..7 = epilogue (TMEM lane quadrants 0..3).
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit in
-// global memory and every role leaves its loop, waits for its own copies in
-// flight, and the CTA frees its TMEM.
+// global memory, every role leaves its loop, the producer waits for its own
+// copies in flight, the MMA thread for its tcgen05 operations, and the CTA
+// frees its TMEM.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -26,26 +34,29 @@ namespace {
 
 template <int FMT, bool GATED>
 struct Cfg {
-  static constexpr int NA = GATED ? 2 : 1;
-  static constexpr int STAGES = GATED ? 4 : 6;
+  static constexpr int NA = 2;                              // weight blocks per tile
+  static constexpr int ROWS = GATED ? 128 : 256;            // output features per tile
+  static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 4 : 5;
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BYTES = 128 * 128;
+  static constexpr int B_BYTES = kNT * 128;
   static constexpr int SF_ATOMS = FMT == MOE_FMT_NVFP4 ? 4 : 1;  // 512-byte atoms per operand per stage
   static constexpr int SF_BYTES = SF_ATOMS * 512;
   static constexpr int RAW_STAGE = NA * A_BYTES + B_BYTES + (NA + 1) * SF_BYTES;
   static constexpr int STAGE_BYTES = (RAW_STAGE + 1023) / 1024 * 1024;
   static constexpr int BAR_BYTES = 256;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + 1024;
+  static constexpr int RTB_BYTES = (kMaxE + 1) * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + RTB_BYTES + 1024;
   static constexpr int ELEMS_PER_STAGE = FMT == MOE_FMT_NVFP4 ? 256 : 128;  // 128 bytes of codes
   static constexpr int BLOCK = FMT == MOE_FMT_NVFP4 ? 16 : 32;
-  static constexpr int ACC_COLS = 128;
+  static constexpr int ACC_COLS = kNT;          // one accumulator: 128 lanes x N columns
+  static constexpr int ACC_BUF = NA * ACC_COLS;  // gate (+ up) of one tile
   static constexpr int SF_COLS_OP = SF_ATOMS * 4;
   static constexpr int SF_COLS_STAGE = (NA + 1) * SF_COLS_OP;
-  static constexpr int TMEM_SF = NA * ACC_COLS;
+  static constexpr int TMEM_SF = 2 * ACC_BUF;
   static constexpr int TMEM_COLS = 512;
   static_assert(TMEM_SF + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
-  static_assert(16 * STAGES + 40 <= BAR_BYTES, "barrier area");
+  static_assert(16 * STAGES + 64 <= BAR_BYTES, "barrier area");
 };
 
 struct GemmArgs {
@@ -56,7 +67,8 @@ struct GemmArgs {
   const float* gA1;
   const float* gB;
   const RowTile* tiles;
-  const int32_t* n_row_tiles;
+  const int32_t* rt_base;
+  int E;
   int NA;  // weight rows per expert (= output features; also the output row stride)
   int K;   // reduction length in elements
   float cap;
@@ -65,6 +77,21 @@ struct GemmArgs {
   uint32_t* status;
   long long limit;
 };
+
+// Tile t -> (expert e, weight-row block mt, row tile index rt) in the order
+// expert, mt, token block.  rtb[e] is the first row tile of expert e.
+__device__ __forceinline__ void map_tile(int t, int MT, const int32_t* rtb, int E, int& mt, int& rt) {
+  int lo = 0, hi = E;  // rtb[lo]*MT <= t < rtb[hi]*MT
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (rtb[mid] * MT <= t) lo = mid;
+    else hi = mid;
+  }
+  const int nrt = rtb[lo + 1] - rtb[lo];
+  const int l = t - rtb[lo] * MT;
+  mt = l / nrt;
+  rt = rtb[lo] + l % nrt;
+}
 
 template <int FMT, bool GATED>
 __global__ void __launch_bounds__(256, 1)
@@ -75,11 +102,12 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
   uint64_t* empty = full + C::STAGES;
-  uint64_t* tmem_full = empty + C::STAGES;
-  uint64_t* tmem_empty = tmem_full + 1;
-  uint64_t* drain = tmem_empty + 1;
+  uint64_t* tmem_full = empty + C::STAGES;  // [2]
+  uint64_t* tmem_empty = tmem_full + 2;     // [2]
+  uint64_t* drain = tmem_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_rtb = reinterpret_cast<int32_t*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -87,8 +115,10 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 4);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tmem_full[b], 1);
+      mbar_init(&tmem_empty[b], 4);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -99,18 +129,19 @@ __global__ void __launch_bounds__(256, 1)
   }
   if (threadIdx.x == 32) {
     prefetch_tmap(&tmA0);
-    if (GATED) prefetch_tmap(&tmA1);
+    prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
   }
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = a.rt_base[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const int MT = a.NA / 128;
-  const int total = (*a.n_row_tiles) * MT;
+  const int MT = (a.NA + C::ROWS - 1) / C::ROWS;
+  const int total = s_rtb[a.E] * MT;
   const int KB = a.K / C::ELEMS_PER_STAGE;
-  const int64_t atoms_per_rowblock = (a.K / C::BLOCK) / 4;
+  const int64_t atoms_per_row = (a.K / C::BLOCK) / 4;  // scale atoms per 128 weight rows or per token tile
 
   if (warp == 0) {
     if (lane == 0) {
@@ -120,13 +151,19 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arming
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const RowTile rt = a.tiles[t / MT];
-        const int mt = t % MT;
+        int mt, rti;
+        map_tile(t, MT, s_rtb, a.E, mt, rti);
+        const RowTile rt = a.tiles[rti];
         const int N = (rt.n_valid + 15) & ~15;
-        const int arow = rt.e * a.NA + mt * 128;
-        const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_rowblock * 512;
-        const uint8_t* sfa1 = GATED ? a.sfA1 + (int64_t)(arow >> 7) * atoms_per_rowblock * 512 : nullptr;
-        const uint8_t* sfb = a.sfB + (int64_t)(rt.row >> 7) * atoms_per_rowblock * 512;
+        const int arow = rt.e * a.NA + mt * C::ROWS;
+        // down: the second block of the last tile lies past the expert when
+        // NA % 256 == 128; it then re-reads the first block (never past the
+        // scale buffer) and the epilogue drops its results
+        const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+        const int arow1 = (GATED || !second) ? arow : arow + 128;
+        const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
+        const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
+        const uint8_t* sfb = a.sfB + (int64_t)(rt.row / kNT) * atoms_per_row * 512;
         const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
@@ -140,10 +177,10 @@ __global__ void __launch_bounds__(256, 1)
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           tma_load_2d(sbase, &tmA0, &full[stage], kb * 128, arow);
-          if (GATED) tma_load_2d(sbase + C::A_BYTES, &tmA1, &full[stage], kb * 128, arow);
+          tma_load_2d(sbase + C::A_BYTES, &tmA1, &full[stage], kb * 128, arow1);
           for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
           bulk_load(sSF, sfa0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
-          if (GATED) bulk_load(sSF + C::SF_BYTES, sfa1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          bulk_load(sSF + C::SF_BYTES, sfa1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
           bulk_load(sSF + C::NA * C::SF_BYTES, sfb + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -166,16 +203,22 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
       int stage = 0;
-      uint32_t phase = 0, acc_phase = 0;
+      uint32_t phase = 0;
+      int it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        const RowTile rt = a.tiles[t / MT];
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+        int mt, rti;
+        map_tile(t, MT, s_rtb, a.E, mt, rti);
+        const RowTile rt = a.tiles[rti];
         const uint32_t N = (uint32_t)((rt.n_valid + 15) & ~15);
-        if (!mbar_wait(tmem_empty, acc_phase ^ 1, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
+        const int buf = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(&tmem_empty[buf], use ^ 1, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t acc0 = tmem + buf * C::ACC_BUF;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
             ok = false;
@@ -202,14 +245,13 @@ __global__ void __launch_bounds__(256, 1)
             const uint64_t koff = (uint64_t)((s * 32) >> 4);
             if constexpr (FMT == MOE_FMT_NVFP4) {
               const uint32_t id = idesc_nvfp4(N);
-              mma_nvfp4(tmem, da0 + koff, db + koff, id, sf_t + 4 * s, sfb_t + 4 * s, accum);
-              if constexpr (GATED)
-                mma_nvfp4(tmem + C::ACC_COLS, da1 + koff, db + koff, id, sf_t + C::SF_COLS_OP + 4 * s, sfb_t + 4 * s,
-                          accum);
+              mma_nvfp4(acc0, da0 + koff, db + koff, id, sf_t + 4 * s, sfb_t + 4 * s, accum);
+              mma_nvfp4(acc0 + C::ACC_COLS, da1 + koff, db + koff, id, sf_t + C::SF_COLS_OP + 4 * s, sfb_t + 4 * s,
+                        accum);
             } else {
               const uint32_t id = idesc_mxfp8(N, (uint32_t)s);
-              mma_mxfp8(tmem, da0 + koff, db + koff, id, sf_t, sfb_t, accum);
-              if constexpr (GATED) mma_mxfp8(tmem + C::ACC_COLS, da1 + koff, db + koff, id, sf_t + C::SF_COLS_OP, sfb_t, accum);
+              mma_mxfp8(acc0, da0 + koff, db + koff, id, sf_t, sfb_t, accum);
+              mma_mxfp8(acc0 + C::ACC_COLS, da1 + koff, db + koff, id, sf_t + C::SF_COLS_OP, sfb_t, accum);
             }
           }
           tc_commit(&empty[stage]);
@@ -219,8 +261,7 @@ __global__ void __launch_bounds__(256, 1)
           }
         }
         if (!ok) break;
-        tc_commit(tmem_full);
-        acc_phase ^= 1;
+        tc_commit(&tmem_full[buf]);
       }
       // every tcgen05 operation of this thread has completed before TMEM is freed
       tc_commit(drain);
@@ -232,30 +273,36 @@ __global__ void __launch_bounds__(256, 1)
     // ---------------- epilogue ----------------
     const int q = warp & 3;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
-    uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      if (!mbar_wait(tmem_full, acc_phase, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
-      tc_fence_after();
-      const RowTile rt = a.tiles[t / MT];
-      const int mt = t % MT;
-      const int f = mt * 128 + q * 32 + lane;
-      float sA0 = 1.0f, sA1 = 1.0f;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      int mt, rti;
+      map_tile(t, MT, s_rtb, a.E, mt, rti);
+      const RowTile rt = a.tiles[rti];
+      const int f = mt * C::ROWS + q * 32 + lane;       // feature of accumulator 0 (down: +128 for 1)
+      const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+      float sA0 = 1.0f, sA1 = 1.0f, gb_lo = 1.0f, gb_hi = 1.0f;
       if constexpr (FMT == MOE_FMT_NVFP4) {
         sA0 = a.gA0[rt.e];
-        if constexpr (GATED) sA1 = a.gA1[rt.e];
+        sA1 = a.gA1[rt.e];
+        if (lane < rt.n_valid) gb_lo = a.gB[rt.row + lane];
+        if (32 + lane < rt.n_valid) gb_hi = a.gB[rt.row + 32 + lane];
       }
+      const int buf = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1) & 1u;
+      if (!mbar_wait(&tmem_full[buf], use, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
+      tc_fence_after();
+      const uint32_t tacc = tq + buf * C::ACC_BUF;
       for (int c0 = 0; c0 < rt.n_valid; c0 += 16) {
         uint32_t r0[16], r1[16];
-        tmem_ld16(tq + c0, r0);
-        if constexpr (GATED) tmem_ld16(tq + C::ACC_COLS + c0, r1);
+        tmem_ld16(tacc + c0, r0);
+        tmem_ld16(tacc + C::ACC_COLS + c0, r1);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int n = c0 + j;
+          const float gb = __shfl_sync(0xffffffffu, n < 32 ? gb_lo : gb_hi, n & 31);
           if (n < rt.n_valid) {
             const int64_t row = (int64_t)rt.row + n;
-            float gb = 1.0f;
-            if constexpr (FMT == MOE_FMT_NVFP4) gb = a.gB[row];
             if constexpr (GATED) {
               float g = __uint_as_float(r0[j]) * (sA0 * gb);
               float u = __uint_as_float(r1[j]) * (sA1 * gb);
@@ -266,15 +313,16 @@ __global__ void __launch_bounds__(256, 1)
               const float h = g / (1.0f + expf(-g)) * u;
               a.h_out[row * a.NA + f] = __float2bfloat16_rn(h);
             } else {
-              a.y_out[(int64_t)(rt.canon + n) * a.NA + f] = __uint_as_float(r0[j]) * (sA0 * gb);
+              float* yrow = a.y_out + (int64_t)(rt.canon + n) * a.NA;
+              yrow[f] = __uint_as_float(r0[j]) * (sA0 * gb);
+              if (second) yrow[f + 128] = __uint_as_float(r1[j]) * (sA1 * gb);
             }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty);
-      acc_phase ^= 1;
+      if (lane == 0) mbar_arrive(&tmem_empty[buf]);
     }
   }
   __syncthreads();
@@ -301,7 +349,8 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st) {
   a.gA1 = g.gA1;
   a.gB = g.gB;
   a.tiles = g.tiles;
-  a.n_row_tiles = g.n_row_tiles;
+  a.rt_base = g.rt_base;
+  a.E = g.E;
   a.NA = g.NA;
   a.K = g.K;
   a.cap = g.cfg->swiglu_cap;
@@ -309,7 +358,7 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st) {
   a.y_out = g.y_out;
   a.status = g.status;
   a.limit = 4000000000LL;  // ~2 s of SM clock
-  k_moe_gemm<FMT, GATED><<<g.num_sms, 256, C::SMEM, st>>>(*g.tmA0, GATED ? *g.tmA1 : *g.tmA0, *g.tmB, a);
+  k_moe_gemm<FMT, GATED><<<g.num_sms, 256, C::SMEM, st>>>(*g.tmA0, *g.tmA1, *g.tmB, a);
   return cudaGetLastError();
 }
 

@@ -11,15 +11,19 @@
 
 namespace moe {
 
-// One block of up to 128 consecutive rows of one expert in padded row order.
+// Token rows per expert tile (MMA N <= kNT).  Each expert's rows start at a
+// multiple of kNT in the expert-grouped activation buffers.
+constexpr int kNT = 64;
+
+// One block of up to kNT consecutive rows of one expert in padded row order.
 struct RowTile {
   int e;        // expert
-  int row;      // first padded row (multiple of 128)
-  int n_valid;  // valid rows in the tile (1..128)
-  int canon;    // first canonical pair position (offsets[e] + 128*i)
+  int row;      // first padded row (multiple of kNT)
+  int n_valid;  // valid rows in the tile (1..kNT)
+  int canon;    // first canonical pair position (offsets[e] + kNT*i)
 };
 
-constexpr int kTileRows = 128;     // rows of A (weights) per MMA tile, and max rows of B
+constexpr int kTileRows = 128;     // weight rows (MMA M) per tile
 constexpr int kMaxE = 1024;
 constexpr int kMaxT = 65536;
 constexpr int kMaxK = 32;
@@ -30,9 +34,11 @@ inline int64_t code_bytes(moe_format f, int64_t K) { return f == MOE_FMT_NVFP4 ?
 // Padded row capacity of the expert-grouped activation buffers.
 inline int64_t padded_rows(const moe_config& c) {
   int64_t P = (int64_t)c.T * c.k;
-  return ((P + 127) / 128 + c.E) * 128;
+  return ((P + kNT - 1) / kNT + c.E) * kNT;
 }
-inline int64_t max_row_tiles(const moe_config& c) { return padded_rows(c) / 128; }
+inline int64_t max_row_tiles(const moe_config& c) { return padded_rows(c) / kNT; }
+// Bytes of activation block scales in the per-row-tile atom layout.
+inline int64_t act_scale_bytes(int64_t R, int64_t scale_cols) { return (R / kNT) * (scale_cols / 4) * 512; }
 
 void ws_layout(const moe_config& c, moe_ws_layout* L);
 
@@ -48,9 +54,10 @@ cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* co
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
                                     const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st);
 // counts (or offsets_in when counts == nullptr) -> offsets_out (optional),
-// seg_start [E+1], tiles, n_row_tiles; zeroes *status when given
+// seg_start [E+1], tiles, rt_base [E+1] (first row tile of each expert; the
+// total at E); zeroes *status when given
 cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
-                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* n_row_tiles,
+                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
                              uint32_t* status, cudaStream_t st);
 
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx,
@@ -80,7 +87,8 @@ struct GemmLaunch {
   const float* gA1;
   const float* gB;
   const RowTile* tiles;
-  const int32_t* n_row_tiles;
+  const int32_t* rt_base;
+  int E;
   int NA;              // rows of A per expert
   int K;               // reduction length (elements)
   __nv_bfloat16* h_out;   // gated: [R, F]

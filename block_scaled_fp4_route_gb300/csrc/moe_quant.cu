@@ -112,9 +112,15 @@ __device__ float row_absmax(const Src* row, int K, float* red) {
 __device__ __forceinline__ float nvfp4_G(float amax) { return amax == 0.0f ? 1.0f : __fdiv_rn(2688.0f, amax); }
 
 // Quantise one row (K elements) to up to `ndst` destination rows.
+enum ScaleLayout { SL_ROWMAJOR = 0, SL_TILED = 1, SL_ACT = 2 };
+
+__device__ __forceinline__ int64_t scale_index(int layout, int64_t r, int64_t c, int64_t C) {
+  return layout == SL_TILED ? tiled_scale_offset(r, c, C) : (layout == SL_ACT ? act_scale_offset(r, c, C) : r * C + c);
+}
+
 template <int FMT, typename Src>
 __device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst, const int64_t* dst_rows,
-                          uint8_t* codes, uint8_t* scales, bool tiled, int64_t scale_cols) {
+                          uint8_t* codes, uint8_t* scales, int layout, int64_t scale_cols) {
   constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   const int nb = K / BS;
   const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
@@ -127,7 +133,7 @@ __device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst,
       for (int d = 0; d < ndst; ++d) {
         int64_t r = dst_rows[d];
         *reinterpret_cast<uint2*>(codes + r * cbytes + (int64_t)b * 8) = c;
-        scales[tiled ? tiled_scale_offset(r, b, scale_cols) : r * scale_cols + b] = (uint8_t)s;
+        scales[scale_index(layout, r, b, scale_cols)] = (uint8_t)s;
       }
     } else {
       uint4 c[2];
@@ -137,7 +143,7 @@ __device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst,
         uint4* o = reinterpret_cast<uint4*>(codes + r * cbytes + (int64_t)b * 32);
         o[0] = c[0];
         o[1] = c[1];
-        scales[tiled ? tiled_scale_offset(r, b, scale_cols) : r * scale_cols + b] = (uint8_t)s;
+        scales[scale_index(layout, r, b, scale_cols)] = (uint8_t)s;
       }
     }
   }
@@ -166,7 +172,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
   if constexpr (FMT == MOE_FMT_NVFP4) {
     if (threadIdx.x < k) glob[dst[threadIdx.x]] = __fdiv_rn(1.0f, G);
   }
-  quant_row<FMT>(row, H, G, mx_mode, k, dst, codes, scales, true, H / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+  quant_row<FMT>(row, H, G, mx_mode, k, dst, codes, scales, SL_ACT, H / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
 }
 
 // h: one CTA per canonical pair position p; row = its padded row.
@@ -190,7 +196,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
   if constexpr (FMT == MOE_FMT_NVFP4) {
     if (threadIdx.x == 0) glob[r] = __fdiv_rn(1.0f, G);
   }
-  quant_row<FMT>(row, F, G, mx_mode, 1, dst, codes, scales, true, F / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+  quant_row<FMT>(row, F, G, mx_mode, 1, dst, codes, scales, SL_ACT, F / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
 }
 
 // --- general API quantiser -------------------------------------------------
@@ -239,7 +245,7 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_rows(const Src* __restri
   if constexpr (FMT == MOE_FMT_NVFP4) {
     if (group_rows == 0 && threadIdx.x == 0) glob_rows[r] = __fdiv_rn(1.0f, G);
   }
-  quant_row<FMT, Src>(row, (int)cols, G, mx_mode, 1, dst, codes, scales, tiled,
+  quant_row<FMT, Src>(row, (int)cols, G, mx_mode, 1, dst, codes, scales, tiled ? SL_TILED : SL_ROWMAJOR,
                       cols / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
 }
 

@@ -246,11 +246,14 @@ MOE_API moe_status moe_poll_device_status(void* ws_dev, void* stream);
 
 /* Byte offsets of the layer's intermediates inside the workspace, for
  * inspection by tests (all buffers in padded expert-row order: each expert's
- * rows start at a multiple of 128).  R = padded row capacity. */
+ * rows start at a multiple of 64).  R = padded row capacity.  The activation
+ * block scales (xq_scales, hq_scales) use one 512-byte atom per 64-row tile
+ * and 4 scale columns: row r, column c at
+ *   ((r/64)*(C/4) + c/4)*512 + (r%64%32)*16 + (r%64/32)*4 + c%4. */
 typedef struct {
   int64_t R;
   size_t status, logits, topk_idx, topk_w, counts, offsets, perm, pair_pos, bitmap, seg_start,
-      tiles, n_row_tiles, xq_codes, xq_scales, xq_global, h_bf16, hq_codes, hq_scales, hq_global,
+      tiles, rt_base, xq_codes, xq_scales, xq_global, h_bf16, hq_codes, hq_scales, hq_global,
       y_perm, total;
 } moe_ws_layout;
 MOE_API moe_status moe_workspace_layout(const moe_config* cfg, moe_ws_layout* layout);

@@ -57,6 +57,12 @@ WORKLOADS = {
                               outlier_frac=0.0, bias="uniform"),
     "prefill16384_mxfp8_zipf": dict(T=16384, H=4608, E=384, k=8, F=2304, fmt="mxfp8", seed=4,
                                     outlier_frac=0.0, bias="zipf"),
+    # smaller cases of the same kernels for detailed profiler captures (a few
+    # GB resident, touched weights still far above the L2 size)
+    "profile_decode16_nvfp4_e96": dict(T=16, H=4608, E=96, k=8, F=2304, fmt="nvfp4", seed=21,
+                                       outlier_frac=0.0, bias="uniform"),
+    "profile_prefill2048_mxfp8_e64": dict(T=2048, H=4608, E=64, k=8, F=2304, fmt="mxfp8", seed=22,
+                                          outlier_frac=0.0, bias="uniform"),
 }
 
 

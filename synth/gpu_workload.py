@@ -88,9 +88,11 @@ class GpuWorkload:
                     seg_start=g("seg_start", torch.int32, E + 1))
 
 
-def untile_scales(tiled: np.ndarray, rows: int, cols: int) -> np.ndarray:
-    """TILED scale layout (moe.h) -> row-major [rows, cols]."""
+def untile_scales(tiled: np.ndarray, rows: int, cols: int, tile_rows: int = 128) -> np.ndarray:
+    """Scale atoms (moe.h) -> row-major [rows, cols].  tile_rows = 128 is the
+    TILED weight layout; 64 is the activation layout of the workspace."""
     r = np.arange(rows)[:, None]
     c = np.arange(cols)[None, :]
-    off = ((r >> 7) * (cols >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3)
+    rr = r % tile_rows
+    off = ((r // tile_rows) * (cols >> 2) + (c >> 2)) * 512 + (rr & 31) * 16 + ((rr >> 5) & 3) * 4 + (c & 3)
     return np.asarray(tiled).reshape(-1)[off]

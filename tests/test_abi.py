@@ -50,11 +50,11 @@ def test_workspace_size_and_layout():
     L = moe.moe_workspace_layout(c)
     assert L["total"] == n
     offs = [L[f] for f in ["status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "pair_pos",
-                           "bitmap", "seg_start", "tiles", "n_row_tiles", "xq_codes", "xq_scales", "xq_global",
+                           "bitmap", "seg_start", "tiles", "rt_base", "xq_codes", "xq_scales", "xq_global",
                            "h_bf16", "hq_codes", "hq_scales", "hq_global", "y_perm", "total"]]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
-    # padded rows: one 128-row block per expert on top of the pairs
-    assert L["R"] == ((64 * 8 + 127) // 128 + 384) * 128
+    # padded rows: one 64-row tile per expert on top of the pairs
+    assert L["R"] == ((64 * 8 + 63) // 64 + 384) * 64
     assert L["hq_codes"] - L["h_bf16"] >= L["R"] * 2304 * 2
     # larger T needs no less workspace
     assert moe.moe_workspace_size(cfg(T=4096)) > n

@@ -146,7 +146,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   uint32_t* status = at<uint32_t>(ws, L.status);
 
   mark(ev, 2, st);
-  cudaError_t e = launch_quant_x(c, x, idx, offsets, pair_pos, seg, xq, xs, xg, st);
+  cudaError_t e = launch_quant_x(c, x, idx, offsets, pair_pos, seg, xq, xs, xg, st, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   const int64_t hb = code_bytes(c.fmt, c.H), fb = code_bytes(c.fmt, c.F);
@@ -178,10 +178,10 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g1.status = status;
   g1.num_sms = sms;
   mark(ev, 3, st);
-  if (launch_gemm(g1, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(g1, st, true) != cudaSuccess) return MOE_ERR_CUDA;
 
   mark(ev, 4, st);
-  if (launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st, true) != cudaSuccess) return MOE_ERR_CUDA;
 
   GemmLaunch g2{};
   g2.cfg = &c;
@@ -204,7 +204,26 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g2.status = status;
   g2.num_sms = sms;
   mark(ev, 5, st);
-  if (launch_gemm(g2, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gemm(g2, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+// Dispatch + tile plan into the workspace: one CTA for decode batches,
+// bitmap / scan / scatter kernels otherwise.  `status` (optional) is cleared.
+moe_status dispatch_impl(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets, int32_t* perm,
+                         int32_t* pair_pos, void* ws, uint32_t* status, cudaStream_t st, bool pdl) {
+  moe_ws_layout L;
+  ws_layout(c, &L);
+  int32_t* seg = at<int32_t>(ws, L.seg_start);
+  RowTile* tiles = at<RowTile>(ws, L.tiles);
+  int32_t* rtb = at<int32_t>(ws, L.rt_base);
+  if (dispatch_fits_one_cta(c))
+    return cuda_status(launch_dispatch_small(c, idx, counts, offsets, perm, pair_pos, seg, tiles, rtb, status, st, pdl));
+  uint32_t* bm = at<uint32_t>(ws, L.bitmap);
+  if (launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st, pdl) != cudaSuccess ||
+      launch_scan_plan(c, counts, nullptr, offsets, seg, tiles, rtb, status, st, true) != cudaSuccess ||
+      launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st, true) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -277,7 +296,7 @@ moe_status moe_route(const moe_config* cfg, const void* x_dev, const void* w_rou
   moe_ws_layout L;
   ws_layout(*cfg, &L);
   return cuda_status(launch_router(*cfg, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                                   at<float>(ws_dev, L.logits), topk_idx_dev, topk_w_dev, (cudaStream_t)stream));
+                                   at<float>(ws_dev, L.logits), topk_idx_dev, topk_w_dev, (cudaStream_t)stream, false));
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int32_t* counts_dev, int32_t* offsets_dev,
@@ -290,13 +309,8 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int3
   moe_ws_layout L;
   ws_layout(*cfg, &L);
   cudaStream_t st = (cudaStream_t)stream;
-  uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
-  if (launch_dispatch(*cfg, topk_idx_dev, counts_dev, offsets_dev, perm_dev, pair_pos_dev, bm, st) != cudaSuccess ||
-      launch_scan_plan(*cfg, counts_dev, nullptr, offsets_dev, at<int32_t>(ws_dev, L.seg_start),
-                       at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.rt_base), nullptr, st) != cudaSuccess ||
-      launch_dispatch_scatter(*cfg, topk_idx_dev, bm, offsets_dev, perm_dev, pair_pos_dev, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  return dispatch_impl(*cfg, topk_idx_dev, counts_dev, offsets_dev, perm_dev, pair_pos_dev, ws_dev, nullptr, st,
+                       false);
 }
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
@@ -317,7 +331,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_
   cudaStream_t st = (cudaStream_t)stream;
   if (launch_scan_plan(*cfg, nullptr, offsets_dev, nullptr, at<int32_t>(ws_dev, L.seg_start),
                        at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.rt_base),
-                       at<uint32_t>(ws_dev, L.status), st) != cudaSuccess)
+                       at<uint32_t>(ws_dev, L.status), st, false) != cudaSuccess)
     return MOE_ERR_CUDA;
   return ffn_core(*cfg, sms, (const __nv_bfloat16*)x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, gate, up,
                   down, y_perm_dev, ws_dev, st);
@@ -329,8 +343,8 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const flo
   if (s == MOE_OK) s = check_ptrs({y_perm_dev, topk_w_dev, pair_pos_dev, out_dev});
   if (s == MOE_OK) s = device_check(nullptr);
   if (s != MOE_OK) return s;
-  return cuda_status(
-      launch_combine(*cfg, y_perm_dev, topk_w_dev, pair_pos_dev, (__nv_bfloat16*)out_dev, (cudaStream_t)stream));
+  return cuda_status(launch_combine(*cfg, y_perm_dev, topk_w_dev, pair_pos_dev, (__nv_bfloat16*)out_dev,
+                                    (cudaStream_t)stream, false));
 }
 
 static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
@@ -360,18 +374,16 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   float* y = at<float>(ws_dev, L.y_perm);
   mark(ev, 0, st);
   if (launch_router(c, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                    at<float>(ws_dev, L.logits), idx, w, st) != cudaSuccess)
+                    at<float>(ws_dev, L.logits), idx, w, st, false) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(ev, 1, st);
-  if (launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st) != cudaSuccess ||
-      launch_scan_plan(c, counts, nullptr, offsets, at<int32_t>(ws_dev, L.seg_start), at<RowTile>(ws_dev, L.tiles),
-                       at<int32_t>(ws_dev, L.rt_base), at<uint32_t>(ws_dev, L.status), st) != cudaSuccess ||
-      launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  s = dispatch_impl(c, idx, counts, offsets, perm, pair_pos, ws_dev, at<uint32_t>(ws_dev, L.status), st, true);
+  if (s != MOE_OK) return s;
+  (void)bm;
   s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st, ev);
   if (s != MOE_OK) return s;
   mark(ev, 6, st);
-  s = cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st));
+  s = cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st, true));
   mark(ev, 7, st);
   return s;
 }

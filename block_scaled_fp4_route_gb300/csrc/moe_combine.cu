@@ -13,6 +13,8 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, co
   __shared__ int pos[kMaxK];
   __shared__ float ww[kMaxK];
   const int t = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < k) {
     pos[threadIdx.x] = pair_pos[(int64_t)t * k + threadIdx.x];
     ww[threadIdx.x] = w[(int64_t)t * k + threadIdx.x];
@@ -39,9 +41,8 @@ __global__ void __launch_bounds__(256) k_combine(const float* __restrict__ y, co
 }  // namespace
 
 cudaError_t launch_combine(const moe_config& c, const float* y, const float* w, const int32_t* pair_pos,
-                           __nv_bfloat16* out, cudaStream_t st) {
-  k_combine<<<c.T, 256, 0, st>>>(y, w, pair_pos, c.H, c.k, out);
-  return cudaGetLastError();
+                           __nv_bfloat16* out, cudaStream_t st, bool pdl) {
+  return launch_k(k_combine, dim3(c.T), dim3(256), 0, st, pdl, y, w, pair_pos, c.H, c.k, out);
 }
 
 }  // namespace moe

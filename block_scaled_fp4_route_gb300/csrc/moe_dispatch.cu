@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kDThreads) k_disp_bitmap(const int32_t* __rest
   __shared__ int red[kDThreads / 32];
   const int e = blockIdx.x;
   const int W = (T + 31) / 32;
+  pdl_wait();
+  pdl_trigger();
   for (int i = threadIdx.x; i < W; i += blockDim.x) bm[i] = 0u;
   __syncthreads();
   const int P = T * k;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
                                                     uint32_t* __restrict__ status) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (status && e == 0) *status = 0u;
   int c = 0;
   if (e < E) c = counts ? counts[e] : (offsets_in[e + 1] - offsets_in[e]);
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __res
   const int e = blockIdx.x;
   const int W = (T + 31) / 32;
   const int wpt = (W + blockDim.x - 1) / blockDim.x;
+  pdl_wait();
+  pdl_trigger();
   const int w0 = threadIdx.x * wpt;
   int c = 0;
   for (int i = 0; i < wpt; ++i)
@@ -146,25 +152,114 @@ __global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __res
   }
 }
 
+constexpr int kSmallWords = 12288;  // 48 KB of token bitmaps
+
+// Whole dispatch for small batches in one CTA of 1024 threads: token bitmaps
+// of every expert in shared memory, counts / offsets / segments / tiles by
+// block scans, then each expert's thread ranks its tokens in order.
+__global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos,
+                                                         int32_t* __restrict__ seg_start, RowTile* __restrict__ tiles,
+                                                         int32_t* __restrict__ rt_base, uint32_t* __restrict__ status) {
+  extern __shared__ uint32_t sbm[];  // [E][W]
+  __shared__ int sh[32];
+  const int W = (T + 31) / 32;
+  pdl_wait();
+  pdl_trigger();
+  if (status && threadIdx.x == 0) *status = 0u;
+  for (int i = threadIdx.x; i < E * W; i += blockDim.x) sbm[i] = 0u;
+  __syncthreads();
+  const int P = T * k;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    int t = p / k;
+    atomicOr(&sbm[idx[p] * W + (t >> 5)], 1u << (t & 31));
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  int c = 0;
+  if (e < E)
+    for (int i = 0; i < W; ++i) c += __popc(sbm[e * W + i]);
+  int tot;
+  const int off = block_exclusive_scan(c, &tot, sh);
+  const int nrt = (c + kNT - 1) / kNT;
+  int ptot;
+  const int seg = block_exclusive_scan(nrt * kNT, &ptot, sh);
+  int rtot;
+  const int rt0 = block_exclusive_scan(nrt, &rtot, sh);
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = off;
+    seg_start[e] = seg;
+    rt_base[e] = rt0;
+    for (int i = 0; i < nrt; ++i) {
+      RowTile tl;
+      tl.e = e;
+      tl.row = seg + kNT * i;
+      tl.n_valid = min(kNT, c - kNT * i);
+      tl.canon = off + kNT * i;
+      tiles[rt0 + i] = tl;
+    }
+    int rank = 0;
+    for (int i = 0; i < W; ++i) {
+      uint32_t v = sbm[e * W + i];
+      while (v) {
+        int b = __ffs(v) - 1;
+        v &= v - 1;
+        int t = i * 32 + b;
+        int j = 0;
+        while (j < k && idx[t * k + j] != e) ++j;
+        perm[off + rank] = t * k + j;
+        pair_pos[t * k + j] = off + rank;
+        ++rank;
+      }
+    }
+  }
+  if (e == 0) {
+    offsets[E] = tot;
+    seg_start[E] = ptot;
+    rt_base[E] = rtot;
+  }
+}
+
 }  // namespace
 
+bool dispatch_fits_one_cta(const moe_config& c) {
+  return c.E <= 1024 && (int64_t)c.E * ((c.T + 31) / 32) <= kSmallWords;
+}
+
+cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                  int32_t* perm, int32_t* pair_pos, int32_t* seg_start, RowTile* tiles,
+                                  int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
+  if (!dispatch_fits_one_cta(c)) return cudaErrorNotSupported;
+  const size_t smem = (size_t)c.E * ((c.T + 31) / 32) * 4;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallWords * 4);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_k(k_dispatch_small, dim3(1), dim3(1024), smem, st, pdl, idx, c.T, c.k, c.E, counts, offsets, perm,
+                  pair_pos, seg_start, tiles, rt_base, status);
+}
+
 cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
-                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st) {
-  k_disp_bitmap<<<c.E, kDThreads, 0, st>>>(idx, c.T, c.k, bitmap, counts);
-  return cudaGetLastError();
+                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st, bool pdl) {
+  return launch_k(k_disp_bitmap, dim3(c.E), dim3(kDThreads), 0, st, pdl, idx, c.T, c.k, bitmap, counts);
 }
 
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
-                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st) {
-  k_disp_scatter<<<c.E, kDThreads, 0, st>>>(idx, c.T, c.k, bitmap, offsets, perm, pair_pos);
-  return cudaGetLastError();
+                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st,
+                                    bool pdl) {
+  return launch_k(k_disp_scatter, dim3(c.E), dim3(kDThreads), 0, st, pdl, idx, c.T, c.k, bitmap, offsets, perm,
+                  pair_pos);
 }
 
 cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
                              int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
-                             uint32_t* status, cudaStream_t st) {
-  k_scan_plan<<<1, 1024, 0, st>>>(counts, offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status);
-  return cudaGetLastError();
+                             uint32_t* status, cudaStream_t st, bool pdl) {
+  return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, counts, offsets_in, c.E, offsets_out, seg_start, tiles,
+                  rt_base, status);
 }
 
 }  // namespace moe

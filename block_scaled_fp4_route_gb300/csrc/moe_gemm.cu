@@ -132,6 +132,9 @@ __global__ void __launch_bounds__(256, 1)
     prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
   }
+  // everything above is independent of the previous kernel; from here on
+  // the tile plan and the activations it wrote are read
+  pdl_wait();
   for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = a.rt_base[i];
   tc_fence_before();
   __syncthreads();
@@ -326,6 +329,7 @@ __global__ void __launch_bounds__(256, 1)
     }
   }
   __syncthreads();
+  pdl_trigger();
   if (warp == 2) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -333,7 +337,7 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <int FMT, bool GATED>
-cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st) {
+cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   using C = Cfg<FMT, GATED>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -358,15 +362,15 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st) {
   a.y_out = g.y_out;
   a.status = g.status;
   a.limit = 4000000000LL;  // ~2 s of SM clock
-  k_moe_gemm<FMT, GATED><<<g.num_sms, 256, C::SMEM, st>>>(*g.tmA0, *g.tmA1, *g.tmB, a);
-  return cudaGetLastError();
+  return launch_k(k_moe_gemm<FMT, GATED>, dim3(g.num_sms), dim3(256), C::SMEM, st, pdl, *g.tmA0, *g.tmA1, *g.tmB, a);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st) {
-  if (g.cfg->fmt == MOE_FMT_NVFP4) return g.gated ? launch_t<MOE_FMT_NVFP4, true>(g, st) : launch_t<MOE_FMT_NVFP4, false>(g, st);
-  return g.gated ? launch_t<MOE_FMT_MXFP8, true>(g, st) : launch_t<MOE_FMT_MXFP8, false>(g, st);
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  if (g.cfg->fmt == MOE_FMT_NVFP4)
+    return g.gated ? launch_t<MOE_FMT_NVFP4, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false>(g, st, pdl);
+  return g.gated ? launch_t<MOE_FMT_MXFP8, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false>(g, st, pdl);
 }
 
 }  // namespace moe

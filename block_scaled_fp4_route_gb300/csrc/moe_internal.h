@@ -43,30 +43,40 @@ inline int64_t act_scale_bytes(int64_t R, int64_t scale_cols) { return (R / kNT)
 void ws_layout(const moe_config& c, moe_ws_layout* L);
 
 // --- launches (all return cudaGetLastError() of their launches) -------------
+// Launches after the first of an API call use programmatic dependent launch
+// (`pdl` = true): the kernel may start while its predecessor drains and waits
+// for it on the device.
 cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr,
-                          const float* bias, float* logits, int32_t* idx, float* w, cudaStream_t st);
+                          const float* bias, float* logits, int32_t* idx, float* w, cudaStream_t st, bool pdl);
 
 int router_splits(const moe_config& c);
 
 // bitmap [E, ceil(T/32)] and counts [E]
 cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
-                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st);
+                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st, bool pdl);
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
-                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st);
+                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st,
+                                    bool pdl);
+// Whole dispatch + tile plan in one CTA when the token bitmaps fit in shared
+// memory (decode batches); returns cudaErrorNotSupported otherwise.
+bool dispatch_fits_one_cta(const moe_config& c);
+cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                  int32_t* perm, int32_t* pair_pos, int32_t* seg_start, RowTile* tiles,
+                                  int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl);
 // counts (or offsets_in when counts == nullptr) -> offsets_out (optional),
 // seg_start [E+1], tiles, rt_base [E+1] (first row tile of each expert; the
 // total at E); zeroes *status when given
 cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
                              int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
-                             uint32_t* status, cudaStream_t st);
+                             uint32_t* status, cudaStream_t st, bool pdl);
 
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx,
                            const int32_t* offsets, const int32_t* pair_pos, const int32_t* seg_start,
-                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st);
+                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st, bool pdl);
 
 cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx,
                            const int32_t* offsets, const int32_t* perm, const int32_t* seg_start,
-                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st);
+                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st, bool pdl);
 
 cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows,
                             int64_t cols, int64_t group_rows, moe_scale_layout layout, uint8_t* codes,
@@ -96,9 +106,9 @@ struct GemmLaunch {
   uint32_t* status;
   int num_sms;
 };
-cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st);
+cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st, bool pdl);
 
 cudaError_t launch_combine(const moe_config& c, const float* y, const float* w, const int32_t* pair_pos,
-                           __nv_bfloat16* out, cudaStream_t st);
+                           __nv_bfloat16* out, cudaStream_t st, bool pdl);
 
 }  // namespace moe

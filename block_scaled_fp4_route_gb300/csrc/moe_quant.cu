@@ -161,6 +161,8 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
   __shared__ int64_t dst[kMaxK];
   const int t = blockIdx.x;
   const __nv_bfloat16* row = x + (int64_t)t * H;
+  pdl_wait();
+  pdl_trigger();
   if (threadIdx.x < k) {
     int pid = t * k + threadIdx.x;
     int e = idx[pid];
@@ -186,6 +188,8 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
   __shared__ float red[32];
   __shared__ int64_t dst[1];
   const int p = blockIdx.x;
+  pdl_wait();
+  pdl_trigger();
   const int e = idx[perm[p]];
   const int64_t r = (int64_t)seg_start[e] + (p - offsets[e]);
   const __nv_bfloat16* row = h + r * F;
@@ -272,27 +276,19 @@ int grid_1d(int64_t n, int threads) {
 
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
                            const int32_t* pair_pos, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
-                           float* glob, cudaStream_t st) {
-  if (c.fmt == MOE_FMT_NVFP4)
-    k_quant_x<MOE_FMT_NVFP4><<<c.T, kQThreads, 0, st>>>(x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
-                                                         seg_start, codes, scales, glob);
-  else
-    k_quant_x<MOE_FMT_MXFP8><<<c.T, kQThreads, 0, st>>>(x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
-                                                         seg_start, codes, scales, glob);
-  return cudaGetLastError();
+                           float* glob, cudaStream_t st, bool pdl) {
+  auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_x<MOE_FMT_NVFP4> : k_quant_x<MOE_FMT_MXFP8>;
+  return launch_k(kern, dim3(c.T), dim3(kQThreads), 0, st, pdl, x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
+                  seg_start, codes, scales, glob);
 }
 
 cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx, const int32_t* offsets,
                            const int32_t* perm, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
-                           float* glob, cudaStream_t st) {
+                           float* glob, cudaStream_t st, bool pdl) {
   int P = c.T * c.k;
-  if (c.fmt == MOE_FMT_NVFP4)
-    k_quant_h<MOE_FMT_NVFP4><<<P, kQThreads, 0, st>>>(h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
-                                                       codes, scales, glob);
-  else
-    k_quant_h<MOE_FMT_MXFP8><<<P, kQThreads, 0, st>>>(h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
-                                                       codes, scales, glob);
-  return cudaGetLastError();
+  auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_h<MOE_FMT_NVFP4> : k_quant_h<MOE_FMT_MXFP8>;
+  return launch_k(kern, dim3(P), dim3(kQThreads), 0, st, pdl, h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
+                  codes, scales, glob);
 }
 
 cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,

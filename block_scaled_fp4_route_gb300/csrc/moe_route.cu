@@ -44,6 +44,7 @@ __global__ void __launch_bounds__(256) k_router_logits(const __nv_bfloat16* __re
   const int split = blockIdx.z;
   const int kbeg = split * k_len;
   const int nst = k_len / kKC;
+  pdl_wait();
 
   // register staging of one stage: rows x 8 uint4 (8 bf16 each)
   constexpr int A_VEC = TM * (kKC / 8), B_VEC = TE * (kKC / 8);
@@ -142,70 +143,76 @@ __global__ void __launch_bounds__(256) k_router_logits(const __nv_bfloat16* __re
       int t = t0 + ty + 16 * i, e = e0 + tx + 16 * j;
       if (t < T && e < E) out[(int64_t)t * E + e] = acc[i][j].s;
     }
+  pdl_trigger();
 }
 
-// One warp per token: sum the K-split partials, sigmoid, bias, top-k,
-// normalise.  Ties in the key go to the lower expert index.
-__global__ void __launch_bounds__(256) k_router_topk(const float* __restrict__ part, int nsplit,
-                                                     const float* __restrict__ bias, int T, int E, int k,
-                                                     int bias_in_weights, float routed_scale,
-                                                     int32_t* __restrict__ idx, float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= T) return;
-  constexpr int MAXPER = kMaxE / 32;
-  float key[MAXPER], sg[MAXPER];
-  const int per = (E + 31) / 32;
+constexpr int kMaxSplits = 24;
+
+// One CTA per token, one thread per expert: sum the K-split partials (Kahan,
+// fixed order), sigmoid, bias, then k rounds of a block-wide arg-max; ties in
+// the key go to the lower expert index.
+__global__ void __launch_bounds__(1024) k_router_topk(const float* __restrict__ part, int nsplit,
+                                                      const float* __restrict__ bias, int T, int E, int k,
+                                                      int bias_in_weights, float routed_scale,
+                                                      int32_t* __restrict__ idx, float* __restrict__ w) {
+  __shared__ float s_key[32];
+  __shared__ int s_e[32];
+  __shared__ int s_win[kMaxK];
+  __shared__ float s_num[kMaxK];
+  const int t = blockIdx.x;
+  const int e = threadIdx.x;
+  const int lane = e & 31, warp = e >> 5, nw = blockDim.x >> 5;
+  pdl_wait();
+  pdl_trigger();
+  float key = -INFINITY, sg = 0.0f;
+  if (e < E) {
+    float v[kMaxSplits];
 #pragma unroll
-  for (int i = 0; i < MAXPER; ++i) {
-    key[i] = -INFINITY;
-    sg[i] = 0.0f;
-    int e = lane + 32 * i;
-    if (i < per && e < E) {
-      Kahan l;
-      for (int s = 0; s < nsplit; ++s) l.add(part[((int64_t)s * T + t) * E + e]);
-      float s = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l.s)));
-      sg[i] = s;
-      key[i] = __fadd_rn(s, bias[e]);
-    }
+    for (int s = 0; s < kMaxSplits; ++s) v[s] = s < nsplit ? part[((int64_t)s * T + t) * E + e] : 0.0f;
+    Kahan l;
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      if (s < nsplit) l.add(v[s]);
+    sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l.s)));
+    key = __fadd_rn(sg, bias[e]);
   }
-  uint32_t taken = 0;
-  float den = 0.0f;
-  int my_slot_e[kMaxK];
-  float my_num[kMaxK];
+  bool taken = e >= E;
   for (int j = 0; j < k; ++j) {
-    // best untaken entry of this lane
-    float bk = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < MAXPER; ++i) {
-      int e = lane + 32 * i;
-      if (i < per && e < E && !((taken >> i) & 1u) && key[i] > bk) { bk = key[i]; be = e; }
-    }
-    // warp argmax, ties to the lower expert index
+    float bk = taken ? -INFINITY : key;
+    int be = taken ? 0x7fffffff : e;
     for (int o = 16; o > 0; o >>= 1) {
       float ok = __shfl_xor_sync(0xffffffffu, bk, o);
       int oe = __shfl_xor_sync(0xffffffffu, be, o);
       if (ok > bk || (ok == bk && oe < be)) { bk = ok; be = oe; }
     }
-    float num = 0.0f;
-    if ((be & 31) == lane) {
-#pragma unroll
-      for (int i = 0; i < MAXPER; ++i)
-        if (i == (be >> 5)) {
-          taken |= 1u << i;
-          num = bias_in_weights ? key[i] : sg[i];
-        }
+    if (lane == 0) {
+      s_key[warp] = bk;
+      s_e[warp] = be;
     }
-    num = __shfl_sync(0xffffffffu, num, be & 31);
-    my_slot_e[j] = be;
-    my_num[j] = num;
-    den = __fadd_rn(den, num);
+    __syncthreads();
+    if (warp == 0) {
+      bk = lane < nw ? s_key[lane] : -INFINITY;
+      be = lane < nw ? s_e[lane] : 0x7fffffff;
+      for (int o = 16; o > 0; o >>= 1) {
+        float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ok > bk || (ok == bk && oe < be)) { bk = ok; be = oe; }
+      }
+      if (lane == 0) s_win[j] = be;
+    }
+    __syncthreads();
+    if (e == s_win[j]) {
+      taken = true;
+      s_num[j] = bias_in_weights ? key : sg;
+    }
   }
-  if (lane == 0) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float den = 0.0f;
+    for (int j = 0; j < k; ++j) den = __fadd_rn(den, s_num[j]);
     for (int j = 0; j < k; ++j) {
-      idx[(int64_t)t * k + j] = my_slot_e[j];
-      w[(int64_t)t * k + j] = __fmul_rn(routed_scale, __fdiv_rn(my_num[j], den));
+      idx[(int64_t)t * k + j] = s_win[j];
+      w[(int64_t)t * k + j] = __fmul_rn(routed_scale, __fdiv_rn(s_num[j], den));
     }
   }
 }
@@ -214,36 +221,32 @@ constexpr int router_smem_bytes(int rm, int rn) { return 2 * 16 * (rm + rn) * (k
 
 }  // namespace
 
-// Number of K splits of the logits GEMM (also sizes the partials buffer).
+// Number of K splits of the logits GEMM (also sizes the partials buffer):
+// enough 64x64 output tiles x splits to fill the GPU for decode batches, each
+// split a whole number of 64-element stages.
 int router_splits(const moe_config& c) {
-  if (c.T > 256) return 1;
-  int s = 8;
-  while (s > 1 && (c.H % (kKC * s)) != 0) s >>= 1;
-  return s;
+  int cap = c.T <= 64 ? kMaxSplits : (c.T <= 256 ? 8 : 1);
+  for (int s = cap; s > 1; --s)
+    if (c.H % (kKC * s) == 0) return s;
+  return 1;
 }
 
 cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr, const float* bias,
-                          float* logits, int32_t* idx, float* w, cudaStream_t st) {
-  int ns = router_splits(c);
-  int k_len = c.H / ns;
-  if (c.T <= 256) {
-    constexpr int smem = router_smem_bytes(1, 4);
-    dim3 grid((c.E + 63) / 64, (c.T + 15) / 16, ns);
-    k_router_logits<1, 4><<<grid, 256, smem, st>>>(x, wr, logits, c.T, c.H, c.E, k_len);
-  } else {
-    constexpr int smem = router_smem_bytes(4, 4);
-    static bool attr = false;
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, ns);
-    k_router_logits<4, 4><<<grid, 256, smem, st>>>(x, wr, logits, c.T, c.H, c.E, k_len);
+                          float* logits, int32_t* idx, float* w, cudaStream_t st, bool pdl) {
+  const int ns = router_splits(c);
+  const int k_len = c.H / ns;
+  constexpr int smem = router_smem_bytes(4, 4);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
   }
-  k_router_topk<<<(c.T + 7) / 8, 256, 0, st>>>(logits, ns, bias, c.T, c.E, c.k, c.bias_in_weights, c.routed_scale,
-                                               idx, w);
-  return cudaGetLastError();
+  dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, ns);
+  cudaError_t e = launch_k(k_router_logits<4, 4>, grid, dim3(256), smem, st, pdl, x, wr, logits, c.T, c.H, c.E, k_len);
+  if (e != cudaSuccess) return e;
+  return launch_k(k_router_topk, dim3(c.T), dim3((c.E + 31) / 32 * 32), 0, st, true, (const float*)logits, ns, bias,
+                  c.T, c.E, c.k, c.bias_in_weights, c.routed_scale, idx, w);
 }
 
 // ----------------------------------------------------------------------------
@@ -323,6 +326,6 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev
   // every logits partial the top-k kernel reads is written first by the
   // logits kernel of the same call, so nothing needs clearing
   cudaError_t e = launch_router(*cfg, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                                scratch, topk_idx_dev, topk_w_dev, (cudaStream_t)stream);
+                                scratch, topk_idx_dev, topk_w_dev, (cudaStream_t)stream, false);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

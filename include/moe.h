@@ -143,8 +143,8 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x_dev, const voi
  *   library, reserved on every device that loads the library until the
  *   process exits.  Configurations whose partials do not fit return
  *   MOE_ERR_WORKSPACE_TOO_SMALL: splits * T * E <= 2^20 floats, where splits
- *   is 8 (or the largest power of two <= 8 with H % (64*splits) == 0) for
- *   T <= 256 and 1 above; e.g. up to T = 256 at E = 384, H = 4608.
+ *   is the largest s <= 24 (T <= 64), <= 8 (T <= 256) or 1 (T > 256) with
+ *   H % (64*s) == 0; e.g. every T <= 256 at E = 384, H = 4608.
  *   The first call on a device looks up the array's device address; make that
  *   first call before any stream capture.
  *   Every call uses the same array: calls that may overlap on the GPU (other

@@ -47,6 +47,7 @@ moe_status check_cfg(const moe_config* c) {
     return MOE_ERR_UNSUPPORTED_SHAPE;
   const int q = c->fmt == MOE_FMT_NVFP4 ? 256 : 128;  // one 128-byte TMA box of codes along K
   if (c->H < q || c->F < q || c->H % q != 0 || c->F % q != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (c->H > 16384 || c->F > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;  // activation rows quantised in registers
   if ((int64_t)c->T * c->k > (1 << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->swiglu_cap >= 0.0f)) return MOE_ERR_INVALID_ARG;
   if (c->mx_scale_mode != 0 && c->mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;

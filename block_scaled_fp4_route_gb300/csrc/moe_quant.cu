@@ -149,6 +149,61 @@ __device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst,
   }
 }
 
+// Activation rows (x, h): each thread keeps its blocks of the row in
+// registers, so the row is read once: absolute maximum (NVFP4 global), then
+// the codes.  Rows of up to kRowRounds * kQThreads blocks (16384 elements).
+constexpr int kRowRounds = 2;
+
+template <int FMT>
+__device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
+                                               const int64_t* dst, uint8_t* codes, uint8_t* scales, float* glob,
+                                               float* red) {
+  constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  const int nb = K / BS;
+  const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
+  const int64_t C = nb;
+  float v[kRowRounds][BS];
+  float m = 0.0f;
+#pragma unroll
+  for (int r = 0; r < kRowRounds; ++r) {
+    const int b = threadIdx.x + r * blockDim.x;
+    if (b < nb) {
+      load_block_bf16(row + (int64_t)b * BS, BS, v[r]);
+#pragma unroll
+      for (int i = 0; i < BS; ++i) m = fmaxf(m, fabsf(v[r][i]));
+    }
+  }
+  float G = 1.0f;
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    G = nvfp4_G(block_max(m, red));
+    if (threadIdx.x < ndst) glob[dst[threadIdx.x]] = __fdiv_rn(1.0f, G);
+  }
+#pragma unroll
+  for (int r = 0; r < kRowRounds; ++r) {
+    const int b = threadIdx.x + r * blockDim.x;
+    if (b >= nb) continue;
+    if constexpr (FMT == MOE_FMT_NVFP4) {
+      uint2 c;
+      uint32_t sc = nvfp4_block(v[r], G, &c);
+      for (int d = 0; d < ndst; ++d) {
+        const int64_t rr = dst[d];
+        *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
+        scales[act_scale_offset(rr, b, C)] = (uint8_t)sc;
+      }
+    } else {
+      uint4 c[2];
+      uint32_t sc = mxfp8_block(v[r], mx_mode, c);
+      for (int d = 0; d < ndst; ++d) {
+        const int64_t rr = dst[d];
+        uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
+        o[0] = c[0];
+        o[1] = c[1];
+        scales[act_scale_offset(rr, b, C)] = (uint8_t)sc;
+      }
+    }
+  }
+}
+
 // x: one CTA per token; written to the k expert-grouped rows of the token.
 template <int FMT>
 __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __restrict__ x, int H, int k,
@@ -160,21 +215,15 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
   __shared__ float red[32];
   __shared__ int64_t dst[kMaxK];
   const int t = blockIdx.x;
-  const __nv_bfloat16* row = x + (int64_t)t * H;
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x < k) {
-    int pid = t * k + threadIdx.x;
-    int e = idx[pid];
+    const int pid = t * k + threadIdx.x;
+    const int e = idx[pid];
     dst[threadIdx.x] = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
   }
-  float G = 1.0f;
-  if constexpr (FMT == MOE_FMT_NVFP4) G = nvfp4_G(row_absmax(row, H, red));
   __syncthreads();
-  if constexpr (FMT == MOE_FMT_NVFP4) {
-    if (threadIdx.x < k) glob[dst[threadIdx.x]] = __fdiv_rn(1.0f, G);
-  }
-  quant_row<FMT>(row, H, G, mx_mode, k, dst, codes, scales, SL_ACT, H / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+  quant_row_regs<FMT>(x + (int64_t)t * H, H, mx_mode, k, dst, codes, scales, glob, red);
 }
 
 // h: one CTA per canonical pair position p; row = its padded row.
@@ -190,18 +239,99 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
   const int p = blockIdx.x;
   pdl_wait();
   pdl_trigger();
-  const int e = idx[perm[p]];
-  const int64_t r = (int64_t)seg_start[e] + (p - offsets[e]);
-  const __nv_bfloat16* row = h + r * F;
-  if (threadIdx.x == 0) dst[0] = r;
-  float G = 1.0f;
-  if constexpr (FMT == MOE_FMT_NVFP4) G = nvfp4_G(row_absmax(row, F, red));
-  __syncthreads();
-  if constexpr (FMT == MOE_FMT_NVFP4) {
-    if (threadIdx.x == 0) glob[r] = __fdiv_rn(1.0f, G);
+  if (threadIdx.x == 0) {
+    const int e = idx[perm[p]];
+    dst[0] = (int64_t)seg_start[e] + (p - offsets[e]);
   }
-  quant_row<FMT>(row, F, G, mx_mode, 1, dst, codes, scales, SL_ACT, F / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
+  __syncthreads();
+  quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, codes, scales, glob, red);
 }
+
+// Many short rows (prefill): one warp per row, eight rows per CTA.  Pass 1
+// finds the row maximum (NVFP4 only), pass 2 re-reads the row (now in L1)
+// block by block.  dst_lane: lane d < ndst holds destination row d.
+template <int FMT>
+__device__ __forceinline__ void quant_row_warp(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
+                                               int64_t dst_lane, uint8_t* codes, uint8_t* scales, float* glob) {
+  constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  const int lane = threadIdx.x & 31;
+  const int nb = K / BS;
+  const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
+  float G = 1.0f;
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    float m = 0.0f;
+    const uint4* q = reinterpret_cast<const uint4*>(row);
+    for (int i = lane; i < K / 8; i += 32) {
+      uint4 u = q[i];
+      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    }
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    G = nvfp4_G(m);
+    if (lane < ndst) glob[dst_lane] = __fdiv_rn(1.0f, G);
+  }
+  for (int b = lane; b < nb; b += 32) {
+    float v[BS];
+    load_block_bf16(row + (int64_t)b * BS, BS, v);
+    if constexpr (FMT == MOE_FMT_NVFP4) {
+      uint2 c;
+      const uint32_t sc = nvfp4_block(v, G, &c);
+      for (int d = 0; d < ndst; ++d) {
+        const int64_t rr = __shfl_sync(0xffffffffu, dst_lane, d);
+        *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
+        scales[act_scale_offset(rr, b, nb)] = (uint8_t)sc;
+      }
+    } else {
+      uint4 c[2];
+      const uint32_t sc = mxfp8_block(v, mx_mode, c);
+      for (int d = 0; d < ndst; ++d) {
+        const int64_t rr = __shfl_sync(0xffffffffu, dst_lane, d);
+        uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
+        o[0] = c[0];
+        o[1] = c[1];
+        scales[act_scale_offset(rr, b, nb)] = (uint8_t)sc;
+      }
+    }
+  }
+}
+
+// rows: x tokens (is_h = 0, k destinations each) or h pair positions (is_h = 1).
+template <int FMT>
+__global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __restrict__ src, int rows, int K, int k,
+                                                         int is_h, int mx_mode, const int32_t* __restrict__ idx,
+                                                         const int32_t* __restrict__ offsets,
+                                                         const int32_t* __restrict__ pair_pos,
+                                                         const int32_t* __restrict__ perm,
+                                                         const int32_t* __restrict__ seg_start, uint8_t* codes,
+                                                         uint8_t* scales, float* glob) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  pdl_wait();
+  pdl_trigger();
+  if (r >= rows) return;
+  int64_t dst = 0;
+  const __nv_bfloat16* row;
+  int ndst;
+  if (is_h) {
+    const int e = idx[perm[r]];
+    dst = (int64_t)seg_start[e] + (r - offsets[e]);
+    row = src + dst * K;
+    ndst = 1;
+  } else {
+    if (lane < k) {
+      const int pid = r * k + lane;
+      const int e = idx[pid];
+      dst = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
+    }
+    row = src + (int64_t)r * K;
+    ndst = k;
+  }
+  quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, codes, scales, glob);
+}
+
+constexpr int kWarpRowsFrom = 2048;  // rows from which one warp per row is used
 
 // --- general API quantiser -------------------------------------------------
 __global__ void k_zero_f32(float* p, int64_t n) {
@@ -277,6 +407,11 @@ int grid_1d(int64_t n, int threads) {
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
                            const int32_t* pair_pos, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
                            float* glob, cudaStream_t st, bool pdl) {
+  if (c.T >= kWarpRowsFrom) {
+    auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
+    return launch_k(kw, dim3((c.T + 7) / 8), dim3(256), 0, st, pdl, x, c.T, c.H, c.k, 0, c.mx_scale_mode, idx, offsets,
+                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob);
+  }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_x<MOE_FMT_NVFP4> : k_quant_x<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(c.T), dim3(kQThreads), 0, st, pdl, x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
                   seg_start, codes, scales, glob);
@@ -286,6 +421,11 @@ cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const in
                            const int32_t* perm, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
                            float* glob, cudaStream_t st, bool pdl) {
   int P = c.T * c.k;
+  if (P >= kWarpRowsFrom) {
+    auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
+    return launch_k(kw, dim3((P + 7) / 8), dim3(256), 0, st, pdl, h, P, c.F, c.k, 1, c.mx_scale_mode, idx, offsets,
+                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob);
+  }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_h<MOE_FMT_NVFP4> : k_quant_h<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(P), dim3(kQThreads), 0, st, pdl, h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
                   codes, scales, glob);

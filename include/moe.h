@@ -80,7 +80,7 @@ typedef enum { MOE_SCALES_ROWMAJOR = 0, MOE_SCALES_TILED = 1 } moe_scale_layout;
 /* Layer shape and options.
  *   T tokens (1..65536), H hidden, E experts (1..1024), k experts per token
  *   (1..min(E,32)), F expert FFN width.  H and F must be multiples of 256 for
- *   NVFP4 and of 128 for MXFP8.
+ *   NVFP4 and of 128 for MXFP8, and at most 16384.
  *   swiglu_cap: c in cap(v) = c*tanh(v/c), applied to the gate and up
  *     pre-activations; 0 disables the cap.  Default 10.  [TS MoE row and MI 1
  *     call the activation a capped / soft-capped SwiGLU but give neither the

@@ -153,10 +153,21 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t phase = 0;
       uint32_t armed = 0, armed_par = 0;  // per stage: armed at least once / parity of last arming
       bool ok = true;
+      // the next tile's descriptor is fetched one tile ahead, so no global
+      // load sits between the last stage of a tile and the first of the next
+      int mt = 0, rti = 0;
+      RowTile rt{};
+      if (blockIdx.x < total) {
+        map_tile(blockIdx.x, MT, s_rtb, a.E, mt, rti);
+        rt = a.tiles[rti];
+      }
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-        int mt, rti;
-        map_tile(t, MT, s_rtb, a.E, mt, rti);
-        const RowTile rt = a.tiles[rti];
+        int mt_n = 0, rti_n = 0;
+        RowTile rt_n{};
+        if (t + (int)gridDim.x < total) {
+          map_tile(t + gridDim.x, MT, s_rtb, a.E, mt_n, rti_n);
+          rt_n = a.tiles[rti_n];
+        }
         const int N = (rt.n_valid + 15) & ~15;
         const int arow = rt.e * a.NA + mt * C::ROWS;
         // down: the second block of the last tile lies past the expert when
@@ -190,6 +201,8 @@ __global__ void __launch_bounds__(256, 1)
             phase ^= 1;
           }
         }
+        mt = mt_n;
+        rt = rt_n;
       }
       if (!ok) {
         // wait (bounded) for the copies this thread put in flight
@@ -209,11 +222,19 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      int nv_next = 0;
+      if (blockIdx.x < total) {
+        int mt0, rti0;
+        map_tile(blockIdx.x, MT, s_rtb, a.E, mt0, rti0);
+        nv_next = a.tiles[rti0].n_valid;
+      }
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
-        int mt, rti;
-        map_tile(t, MT, s_rtb, a.E, mt, rti);
-        const RowTile rt = a.tiles[rti];
-        const uint32_t N = (uint32_t)((rt.n_valid + 15) & ~15);
+        const uint32_t N = (uint32_t)((nv_next + 15) & ~15);
+        if (t + (int)gridDim.x < total) {  // fetched one tile ahead
+          int mt_n, rti_n;
+          map_tile(t + gridDim.x, MT, s_rtb, a.E, mt_n, rti_n);
+          nv_next = a.tiles[rti_n].n_valid;
+        }
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(&tmem_empty[buf], use ^ 1, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
-            "moe_route_noalloc", "moe_status_string"]
+            "moe_route_noalloc", "moe_fake_quantize", "moe_selftest_bounded_wait", "moe_status_string"]
 
 
 class MoeError(RuntimeError):
@@ -77,6 +77,8 @@ def lib():
             L.moe_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64, i64, i64, ctypes.c_int,
                                        P, P, P, P]
             L.moe_pack_scales.argtypes = [P, i64, i64, P, P]
+            L.moe_fake_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64, i64, i64, P, P, P]
+            L.moe_selftest_bounded_wait.argtypes = [cfgp, qwp, qwp, P, sz, i64, P]
             L.moe_poll_device_status.argtypes = [P, P]
             L.moe_workspace_layout.argtypes = [cfgp, ctypes.POINTER(moe_ws_layout)]
             L.moe_status_string.argtypes = [ctypes.c_int]
@@ -197,6 +199,24 @@ def moe_quantize(fmt, src, codes, scales, global_scale=None, group_rows=0, layou
     _check("moe_quantize", lib().moe_quantize(fmt, mx_scale_mode, int(src.dtype == torch.float32), _ptr(src), rows,
                                               cols, group_rows, layout, _ptr(codes), _ptr(scales),
                                               _ptr(global_scale), _stream(stream)))
+
+
+def moe_fake_quantize(fmt, src, out, global_scale=None, group_rows=0, mx_scale_mode=0, stream=None):
+    """out (fp32, same shape as src) = decode(encode(src)); straight-through in training."""
+    import torch
+    if isinstance(fmt, str):
+        fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
+    cols = src.shape[-1]
+    rows = src.numel() // cols
+    _check("moe_fake_quantize", lib().moe_fake_quantize(fmt, mx_scale_mode, int(src.dtype == torch.float32), _ptr(src),
+                                                        rows, cols, group_rows, _ptr(out), _ptr(global_scale),
+                                                        _stream(stream)))
+
+
+def moe_selftest_bounded_wait(cfg, gate, up, ws, limit_cycles, stream=None):
+    _check("moe_selftest_bounded_wait", lib().moe_selftest_bounded_wait(
+        ctypes.byref(cfg), ctypes.byref(gate), ctypes.byref(up), _ptr(ws), ws.numel() * ws.element_size(),
+        limit_cycles, _stream(stream)))
 
 
 def moe_pack_scales(rowmajor, rows, scale_cols, tiled, stream=None):

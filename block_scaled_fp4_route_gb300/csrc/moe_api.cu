@@ -442,6 +442,70 @@ moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64_t scale
                                         (cudaStream_t)stream));
 }
 
+moe_status moe_fake_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32, const void* src_dev, int64_t rows,
+                             int64_t cols, int64_t group_rows, float* out_dev, float* global_dev, void* stream) {
+  if (fmt != MOE_FMT_NVFP4 && fmt != MOE_FMT_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (mx_scale_mode != 0 && mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;
+  const int bs = fmt == MOE_FMT_NVFP4 ? 16 : 32;
+  if (rows < 1 || rows > (int64_t)INT32_MAX || cols < bs || cols % bs != 0 || cols > (1 << 20))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (src_is_fp32 ? (cols % 4) : (cols % 8)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  moe_status s;
+  if (fmt == MOE_FMT_NVFP4) {
+    if (group_rows < 0 || (group_rows > 0 && rows % group_rows != 0)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    s = check_ptrs({src_dev, out_dev, global_dev});
+  } else {
+    s = check_ptrs({src_dev, out_dev});
+  }
+  if (s == MOE_OK) s = device_check(nullptr);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_fake_quant(fmt, mx_scale_mode, src_is_fp32, src_dev, rows, cols, group_rows, out_dev,
+                                       global_dev, (cudaStream_t)stream));
+}
+
+moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qweight* gate, const moe_qweight* up,
+                                     void* ws_dev, size_t ws_bytes, int64_t limit_cycles, void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK) s = check_qw(cfg, gate);
+  if (s == MOE_OK) s = check_qw(cfg, up);
+  if (s == MOE_OK) s = check_ws(cfg, ws_dev, ws_bytes);
+  if (s == MOE_OK && (limit_cycles < 1000 || limit_cycles > 4000000000LL)) s = MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  if (s == MOE_OK) s = device_check(&sms);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  moe_ws_layout L;
+  ws_layout(c, &L);
+  const int64_t hb = code_bytes(c.fmt, c.H);
+  CUtensorMap mg, mu, mx;
+  if (!make_map(&mg, gate->codes, (int64_t)c.E * c.F, hb, 128) || !make_map(&mu, up->codes, (int64_t)c.E * c.F, hb, 128) ||
+      !make_map(&mx, at<uint8_t>(ws_dev, L.xq_codes), L.R, hb, 16))
+    return MOE_ERR_CUDA;
+  GemmLaunch g1{};
+  g1.cfg = &c;
+  g1.gated = true;
+  g1.tmA0 = &mg;
+  g1.tmA1 = &mu;
+  g1.tmB = &mx;
+  g1.sfA0 = (const uint8_t*)gate->scales;
+  g1.sfA1 = (const uint8_t*)up->scales;
+  g1.sfB = at<uint8_t>(ws_dev, L.xq_scales);
+  g1.gA0 = gate->global_scale;
+  g1.gA1 = up->global_scale;
+  g1.gB = at<float>(ws_dev, L.xq_global);
+  g1.tiles = at<RowTile>(ws_dev, L.tiles);
+  g1.rt_base = at<int32_t>(ws_dev, L.rt_base);
+  g1.E = c.E;
+  g1.NA = c.F;
+  g1.K = c.H;
+  g1.h_out = at<__nv_bfloat16>(ws_dev, L.h_bf16);
+  g1.status = at<uint32_t>(ws_dev, L.status);
+  g1.num_sms = sms;
+  g1.wait_limit = limit_cycles;
+  g1.withhold_loads = 1;
+  return cuda_status(launch_gemm(g1, (cudaStream_t)stream, false));
+}
+
 moe_status moe_poll_device_status(void* ws_dev, void* stream) {
   if (!ws_dev) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;

@@ -73,6 +73,13 @@ __device__ __forceinline__ uint32_t e4m3_encode(float v) {
   return sign | ((uint32_t)(e + 7) << 3) | (m - 8);
 }
 
+// E2M1 code -> value {0, .5, 1, 1.5, 2, 3, 4, 6} with sign (exact).
+__device__ __forceinline__ float e2m1_value(uint32_t q) {
+  const uint32_t m = q & 7u;
+  const float v = m < 2u ? 0.5f * (float)m : (float)(1u << ((m >> 1) - 1u)) * ((m & 1u) ? 1.5f : 1.0f);
+  return (q & 8u) ? -v : v;
+}
+
 __device__ __forceinline__ float e4m3_value(uint32_t c) {
   uint32_t e = (c >> 3) & 15, m = c & 7;
   float v = (e == 0) ? (float)m * 0.001953125f : __uint_as_float(((e + 120) << 23) | (m << 20));
@@ -165,16 +172,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* status, uint32_t code, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
-  long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
+  const long long t0 = clock64();
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0) {
-      if (*abort_flag) return false;
-      if (clock64() - t0 > limit) {
-        *abort_flag = 1;
-        atomicOr(status, code);
-        return false;
-      }
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(status, code);
+      return false;
     }
   }
 }

@@ -76,6 +76,7 @@ struct GemmArgs {
   float* y_out;
   uint32_t* status;
   long long limit;
+  int withhold_loads;
 };
 
 // Tile t -> (expert e, weight-row block mt, row tile index rt) in the order
@@ -187,6 +188,13 @@ __global__ void __launch_bounds__(256, 1)
           uint8_t* sbase = smem + stage * C::STAGE_BYTES;
           uint8_t* sB = sbase + C::NA * C::A_BYTES;
           uint8_t* sSF = sB + C::B_BYTES;
+          if (a.withhold_loads) {  // bounded-wait self-test: nothing arrives
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           mbar_expect_tx(&full[stage], bytes);
           armed |= 1u << stage;
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
@@ -382,7 +390,8 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   a.h_out = g.h_out;
   a.y_out = g.y_out;
   a.status = g.status;
-  a.limit = 4000000000LL;  // ~2 s of SM clock
+  a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock
+  a.withhold_loads = g.withhold_loads;
   return launch_k(k_moe_gemm<FMT, GATED>, dim3(g.num_sms), dim3(256), C::SMEM, st, pdl, *g.tmA0, *g.tmA1, *g.tmB, a);
 }
 

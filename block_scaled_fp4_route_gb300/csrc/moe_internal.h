@@ -84,6 +84,9 @@ cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const voi
 
 cudaError_t launch_pack_scales(const uint8_t* src, int64_t rows, int64_t cols, uint8_t* dst, cudaStream_t st);
 
+cudaError_t launch_fake_quant(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,
+                              int64_t group_rows, float* out, float* glob, cudaStream_t st);
+
 struct GemmLaunch {
   const moe_config* cfg;
   bool gated;          // GEMM1 (gate+up, SwiGLU epilogue) vs GEMM2 (down)
@@ -105,6 +108,8 @@ struct GemmLaunch {
   float* y_out;           // down:  [P, H]
   uint32_t* status;
   int num_sms;
+  long long wait_limit = 0;  // cycles per bounded wait; 0 = the default (~2 s)
+  int withhold_loads = 0;    // self-test only: the producer issues no loads, so every wait runs out
 };
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st, bool pdl);
 

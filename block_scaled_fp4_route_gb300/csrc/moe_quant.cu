@@ -383,6 +383,48 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_rows(const Src* __restri
                       cols / (FMT == MOE_FMT_NVFP4 ? 16 : 32));
 }
 
+// Fake quantisation: out = decode(encode(v)) in fp32, rounded once (the
+// products e2m1*scale and e4m3*2^k are exact; NVFP4 multiplies by g last).
+template <int FMT, typename Src>
+__global__ void __launch_bounds__(kQThreads) k_fake_quant_rows(const Src* __restrict__ src, int64_t cols,
+                                                               int64_t group_rows, int mx_mode,
+                                                               const float* group_amax, float* glob_rows,
+                                                               float* __restrict__ out) {
+  __shared__ float red[32];
+  constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  const int64_t r = blockIdx.x;
+  const Src* row = src + r * cols;
+  float G = 1.0f;
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (group_rows > 0) G = nvfp4_G(group_amax[r / group_rows]);
+    else G = nvfp4_G(row_absmax(row, (int)cols, red));
+  }
+  const float g = __fdiv_rn(1.0f, G);
+  if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (group_rows == 0 && threadIdx.x == 0 && glob_rows) glob_rows[r] = g;
+  }
+  for (int64_t b = threadIdx.x; b < cols / BS; b += blockDim.x) {
+    float v[BS];
+    load_block<Src>(row + b * BS, BS, v);
+    float* o = out + r * cols + b * BS;
+    if constexpr (FMT == MOE_FMT_NVFP4) {
+      uint2 c;
+      const uint32_t sb = nvfp4_block(v, G, &c);
+      const float sv = e4m3_value(sb);
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t q = ((i < 8 ? c.x : c.y) >> (4 * (i & 7))) & 15u;
+        o[i] = __fmul_rn(__fmul_rn(e2m1_value(q), sv), g);
+      }
+    } else {
+      uint4 c[2];
+      const uint32_t s = mxfp8_block(v, mx_mode, c);
+      const float X = exp2i((int)s - 127);
+      const uint32_t w[8] = {c[0].x, c[0].y, c[0].z, c[0].w, c[1].x, c[1].y, c[1].z, c[1].w};
+      for (int i = 0; i < 32; ++i) o[i] = __fmul_rn(e4m3_value((w[i / 4] >> (8 * (i % 4))) & 0xFFu), X);
+    }
+  }
+}
+
 __global__ void k_finalize_groups(float* glob, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     glob[i] = __fdiv_rn(1.0f, nvfp4_G(glob[i]));
@@ -462,6 +504,37 @@ cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const voi
     else
       k_quantize_rows<MOE_FMT_MXFP8, __nv_bfloat16><<<grid, kQThreads, 0, st>>>(
           (const __nv_bfloat16*)src, cols, 0, mx_mode, tiled, codes, scales, nullptr, nullptr);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fake_quant(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,
+                              int64_t group_rows, float* out, float* glob, cudaStream_t st) {
+  float* group_scratch = glob;
+  const bool nv = fmt == MOE_FMT_NVFP4;
+  if (nv && group_rows > 0) {
+    int64_t ng = rows / group_rows, n = group_rows * cols, chunk = 1 << 16;
+    k_zero_f32<<<grid_1d(ng, 256), 256, 0, st>>>(group_scratch, ng);
+    dim3 grid((unsigned)((n + chunk - 1) / chunk), (unsigned)ng);
+    if (src_fp32) k_group_amax<float><<<grid, 256, 0, st>>>((const float*)src, cols, group_rows, chunk, group_scratch);
+    else k_group_amax<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)src, cols, group_rows, chunk, group_scratch);
+  }
+  dim3 grid((unsigned)rows);
+  if (nv) {
+    if (src_fp32)
+      k_fake_quant_rows<MOE_FMT_NVFP4, float><<<grid, kQThreads, 0, st>>>((const float*)src, cols, group_rows, mx_mode,
+                                                                         group_scratch, glob, out);
+    else
+      k_fake_quant_rows<MOE_FMT_NVFP4, __nv_bfloat16><<<grid, kQThreads, 0, st>>>(
+          (const __nv_bfloat16*)src, cols, group_rows, mx_mode, group_scratch, glob, out);
+    if (group_rows > 0) k_finalize_groups<<<grid_1d(rows / group_rows, 256), 256, 0, st>>>(glob, rows / group_rows);
+  } else {
+    if (src_fp32)
+      k_fake_quant_rows<MOE_FMT_MXFP8, float><<<grid, kQThreads, 0, st>>>((const float*)src, cols, 0, mx_mode, nullptr,
+                                                                         nullptr, out);
+    else
+      k_fake_quant_rows<MOE_FMT_MXFP8, __nv_bfloat16><<<grid, kQThreads, 0, st>>>(
+          (const __nv_bfloat16*)src, cols, 0, mx_mode, nullptr, nullptr, out);
   }
   return cudaGetLastError();
 }

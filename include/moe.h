@@ -236,6 +236,18 @@ MOE_API moe_status moe_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp
                         int64_t rows, int64_t cols, int64_t group_rows, moe_scale_layout layout,
                         void* codes_dev, void* scales_dev, float* global_dev, void* stream);
 
+/* Fake quantisation [MI 5.3: full-parameter training fake-quantises the
+ * expert weights to their layer's format with a straight-through gradient]:
+ * out = decode(encode(src)) in fp32, bit for bit the value the layer's GEMMs
+ * see (encode as moe_quantize; decode e2m1*scale*g or e4m3*2^(s-127), one
+ * fp32 rounding).  Its gradient is the identity (straight-through), so a
+ * trainer applies it in the forward pass and passes gradients unchanged.
+ *   out_dev fp32 [rows, cols]; global_dev as in moe_quantize (NVFP4 only;
+ *   receives the decode factors). */
+MOE_API moe_status moe_fake_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32, const void* src_dev,
+                                     int64_t rows, int64_t cols, int64_t group_rows, float* out_dev,
+                                     float* global_dev, void* stream);
+
 /* ROWMAJOR -> TILED scale re-layout (rows % 128 == 0, scale columns % 4 == 0). */
 MOE_API moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64_t scale_cols, void* tiled_dev,
                            void* stream);
@@ -243,6 +255,16 @@ MOE_API moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns MOE_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out. */
 MOE_API moe_status moe_poll_device_status(void* ws_dev, void* stream);
+
+/* Test hook for the device-side failure detection: launches the gate/up GEMM
+ * over the tile plan already in the workspace (a moe_forward or
+ * moe_expert_ffn must have run on it) with its loads withheld and every
+ * bounded wait limited to limit_cycles (1000 .. 4e9) SM cycles, so that the
+ * waits run out and the kernel exits with a timeout bit in the workspace
+ * status word, which moe_poll_device_status then reports as
+ * MOE_ERR_DEVICE_TIMEOUT.  The device stays usable. */
+MOE_API moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qweight* gate, const moe_qweight* up,
+                                             void* ws_dev, size_t ws_bytes, int64_t limit_cycles, void* stream);
 
 /* Byte offsets of the layer's intermediates inside the workspace, for
  * inspection by tests (all buffers in padded expert-row order: each expert's

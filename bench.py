@@ -124,6 +124,25 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
+# replicas across ranks: no collective on the data path, only the timing
+# ----------------------------------------------------------------------------
+
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The slowest rank's time (every rank gets the same number)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank_step: int, steps: int, world: int, slowest_ms: float) -> float:
+    """Whole-job throughput: the tokens of every rank over the slowest rank's time."""
+    return world * tokens_per_rank_step * steps / (slowest_ms / 1e3)
+
+
+# ----------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
 # ----------------------------------------------------------------------------
 
@@ -265,13 +284,9 @@ def main():
     torch.cuda.synchronize()
     clocks.stop()
     barrier()
-    ms = start.elapsed_time(end)
-    if dist:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
     ms_per_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = job_tokens_per_s(T, args.steps, world, ms)
     launches_per_step = 10
 
     # ---- per-stage device times (events between the stages, same stream) ----
@@ -308,12 +323,8 @@ def main():
                             gw.out, gw.ws)
             out_host.copy_(gw.out, non_blocking=True)
             st.synchronize()
-        dt = time.perf_counter() - t0
-        if dist:
-            t = torch.tensor([dt], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * T * n_e2e / dt, "unit": UNIT, "h2d_bytes_per_step": int(gw.x.numel() * 2),
+        dt = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
+        e2e = {"value": job_tokens_per_s(T, n_e2e, world, dt * 1e3), "unit": UNIT, "h2d_bytes_per_step": int(gw.x.numel() * 2),
                "d2h_bytes_per_step": int(gw.out.numel() * 2), "steps": n_e2e}
 
     # ---- roofline of the dominant kernel (GEMM1: gate/up + SwiGLU) ----

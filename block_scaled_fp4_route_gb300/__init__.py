@@ -48,7 +48,7 @@ _LAYOUT_FIELDS = ["status", "logits", "topk_idx", "topk_w", "counts", "offsets",
 
 
 class moe_ws_layout(ctypes.Structure):
-    _fields_ = [("R", ctypes.c_int64)] + [(f, ctypes.c_size_t) for f in _LAYOUT_FIELDS]
+    _fields_ = [("R", ctypes.c_int64), ("tile_rows", ctypes.c_int64)] + [(f, ctypes.c_size_t) for f in _LAYOUT_FIELDS]
 
 
 _lib = None
@@ -136,7 +136,7 @@ def moe_workspace_size(cfg: moe_config) -> int:
 def moe_workspace_layout(cfg: moe_config) -> dict:
     L = moe_ws_layout()
     _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)))
-    return {f: getattr(L, f) for f in ["R"] + _LAYOUT_FIELDS}
+    return {f: getattr(L, f) for f in ["R", "tile_rows"] + _LAYOUT_FIELDS}
 
 
 def moe_route(cfg, x, w_router, bias, topk_idx, topk_w, ws, stream=None):

@@ -240,6 +240,7 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
     return o;
   };
   L->R = R;
+  L->tile_rows = tile_rows(c);
   L->status = take(256);
   L->logits = take((size_t)router_splits(c) * T * E * 4);
   L->topk_idx = take(P * 4);
@@ -253,11 +254,11 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
   L->tiles = take(max_row_tiles(c) * sizeof(RowTile));
   L->rt_base = take((E + 1) * 4);
   L->xq_codes = take(R * code_bytes(c.fmt, c.H));
-  L->xq_scales = take(act_scale_bytes(R, c.H / bs));
+  L->xq_scales = take(act_scale_bytes(R, c.H / bs, tile_rows(c)));
   L->xq_global = take(R * 4);
   L->h_bf16 = take(R * c.F * 2);
   L->hq_codes = take(R * code_bytes(c.fmt, c.F));
-  L->hq_scales = take(act_scale_bytes(R, c.F / bs));
+  L->hq_scales = take(act_scale_bytes(R, c.F / bs, tile_rows(c)));
   L->hq_global = take(R * 4);
   L->y_perm = take(P * c.H * 4);
   L->total = off;

@@ -29,11 +29,12 @@ enum : uint32_t {
 __host__ __device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t c, int64_t C) {
   return ((r >> 7) * (C >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (c & 3);
 }
-// Activation (MMA B operand) scales: one 512-byte atom per row tile of kNT
-// rows and 4 scale columns; row rr of the tile at lane rr%32, word rr/32.
-__host__ __device__ __forceinline__ int64_t act_scale_offset(int64_t r, int64_t c, int64_t C) {
-  const int64_t rr = r % kNT;
-  return ((r / kNT) * (C >> 2) + (c >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (c & 3);
+// Activation (MMA B operand) scales: one 512-byte atom per row tile of nt
+// (64 or 128) rows and 4 scale columns; row rr of the tile at lane rr%32,
+// word rr/32.
+__host__ __device__ __forceinline__ int64_t act_scale_offset(int64_t r, int64_t c, int64_t C, int nt) {
+  const int64_t rr = r % nt;
+  return ((r / nt) * (C >> 2) + (c >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (c & 3);
 }
 
 // ----------------------------------------------------------------------------

@@ -7,7 +7,7 @@
 //   1. one CTA per expert builds the expert's token bitmap in shared memory
 //      from topk_idx and counts its pairs;
 //   2. one CTA scans counts -> offsets, padded segment starts (each expert's
-//      rows begin at a multiple of kNT) and the list of kNT-row tiles;
+//      rows begin at a multiple of nt) and the list of nt-row tiles;
 //   3. one CTA per expert ranks its tokens from the bitmap (popcount prefix)
 //      and writes perm / pair_pos.
 #include "moe_common.cuh"
@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
                                                     const int32_t* __restrict__ offsets_in, int E,
                                                     int32_t* __restrict__ offsets_out, int32_t* __restrict__ seg_start,
                                                     RowTile* __restrict__ tiles, int32_t* __restrict__ rt_base,
-                                                    uint32_t* __restrict__ status) {
+                                                    uint32_t* __restrict__ status, int nt) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
   pdl_wait();
@@ -96,8 +96,8 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
     if (e < E) offsets_out[e] = off;
     if (e == 0) offsets_out[E] = tot;
   }
-  int nrt = (c + kNT - 1) / kNT;
-  int padded = nrt * kNT;
+  int nrt = (c + nt - 1) / nt;
+  int padded = nrt * nt;
   int ptot;
   int seg = block_exclusive_scan(padded, &ptot, sh);
   if (e < E) seg_start[e] = seg;
@@ -109,9 +109,9 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
     for (int i = 0; i < nrt; ++i) {
       RowTile t;
       t.e = e;
-      t.row = seg + kNT * i;
-      t.n_valid = min(kNT, c - kNT * i);
-      t.canon = off + kNT * i;
+      t.row = seg + nt * i;
+      t.n_valid = min(nt, c - nt * i);
+      t.canon = off + nt * i;
       tiles[rt0 + i] = t;
     }
   }
@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos,
                                                          int32_t* __restrict__ seg_start, RowTile* __restrict__ tiles,
-                                                         int32_t* __restrict__ rt_base, uint32_t* __restrict__ status) {
+                                                         int32_t* __restrict__ rt_base, uint32_t* __restrict__ status,
+                                                         int nt) {
   extern __shared__ uint32_t sbm[];  // [E][W]
   __shared__ int sh[32];
   const int W = (T + 31) / 32;
@@ -182,9 +183,9 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
     for (int i = 0; i < W; ++i) c += __popc(sbm[e * W + i]);
   int tot;
   const int off = block_exclusive_scan(c, &tot, sh);
-  const int nrt = (c + kNT - 1) / kNT;
+  const int nrt = (c + nt - 1) / nt;
   int ptot;
-  const int seg = block_exclusive_scan(nrt * kNT, &ptot, sh);
+  const int seg = block_exclusive_scan(nrt * nt, &ptot, sh);
   int rtot;
   const int rt0 = block_exclusive_scan(nrt, &rtot, sh);
   if (e < E) {
@@ -195,9 +196,9 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
     for (int i = 0; i < nrt; ++i) {
       RowTile tl;
       tl.e = e;
-      tl.row = seg + kNT * i;
-      tl.n_valid = min(kNT, c - kNT * i);
-      tl.canon = off + kNT * i;
+      tl.row = seg + nt * i;
+      tl.n_valid = min(nt, c - nt * i);
+      tl.canon = off + nt * i;
       tiles[rt0 + i] = tl;
     }
     int rank = 0;
@@ -240,7 +241,7 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
     attr = true;
   }
   return launch_k(k_dispatch_small, dim3(1), dim3(1024), smem, st, pdl, idx, c.T, c.k, c.E, counts, offsets, perm,
-                  pair_pos, seg_start, tiles, rt_base, status);
+                  pair_pos, seg_start, tiles, rt_base, status, tile_rows(c));
 }
 
 cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
@@ -259,7 +260,7 @@ cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const i
                              int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
                              uint32_t* status, cudaStream_t st, bool pdl) {
   return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, counts, offsets_in, c.E, offsets_out, seg_start, tiles,
-                  rt_base, status);
+                  rt_base, status, tile_rows(c));
 }
 
 }  // namespace moe

@@ -8,8 +8,8 @@
 // (kind::mxf8f6f4, E4M3 x E4M3 with UE8M0 scales per 32).
 //
 // A tile holds two 128-row weight blocks (two MMAs with M = 128 sharing the
-// token operand) x up to kNT = 64 token rows of one expert (MMA N, rounded up
-// to 16) x the full K, "swap-AB": the weights fill M so a decode batch with
+// token operand) x up to NT = 64 (decode) or 128 (prefill) token rows of one
+// expert (MMA N, rounded up to 16) x the full K, "swap-AB": the weights fill M so a decode batch with
 // one or two tokens per expert wastes no weight bytes, and each pipeline
 // stage carries 32 KB of weights.
 //   GEMM1 (gated):  A0 = 128 W_gate rows, A1 = the same 128 W_up rows,
@@ -18,10 +18,13 @@
 //                   epilogue y = acc * g_w * g_h (fp32)
 // Tiles are walked expert by expert, then weight-row block, then token block,
 // so CTAs running side by side share an expert's weights and activations in
-// L2.  The TMEM accumulator is double-buffered: the epilogue of one tile runs
-// while the MMAs of the next one accumulate into the other buffer.
-// Warp roles (256 threads): warp 0 = TMA producer, warp 1 = MMA issuer,
-// warp 2 = TMEM allocator, warps 4..7 = epilogue (TMEM lane quadrants 0..3).
+// L2.  With NT = 64 the TMEM accumulator is double-buffered (the epilogue of
+// one tile runs while the next accumulates); with NT = 128 there is room for
+// one buffer only, so the epilogue copies its share to registers and frees
+// TMEM before the arithmetic.
+// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
+// allocator, warps 4..7 (and 8..11 when NT = 128) = epilogue; warp w reads
+// TMEM lane quadrant w % 4.
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit in
 // global memory, every role leaves its loop, the producer waits for its own
 // copies in flight, the MMA thread for its tcgen05 operations, and the CTA
@@ -32,13 +35,17 @@ namespace moe {
 
 namespace {
 
-template <int FMT, bool GATED>
+template <int FMT, bool GATED, bool WIDE>
 struct Cfg {
   static constexpr int NA = 2;                              // weight blocks per tile
   static constexpr int ROWS = GATED ? 128 : 256;            // output features per tile
-  static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 4 : 5;
+  static constexpr int NT = WIDE ? kNTWide : kNTDecode;     // token rows per tile
+  static constexpr int ACC_BUFS = WIDE ? 1 : 2;             // TMEM accumulator buffers
+  static constexpr int EPI_WARPS = WIDE ? 8 : 4;            // two warps per TMEM lane quadrant when wide
+  static constexpr int THREADS = (4 + EPI_WARPS) * 32;
+  static constexpr int STAGES = WIDE ? 4 : (FMT == MOE_FMT_NVFP4 ? 4 : 5);
   static constexpr int A_BYTES = 128 * 128;
-  static constexpr int B_BYTES = kNT * 128;
+  static constexpr int B_BYTES = NT * 128;
   static constexpr int SF_ATOMS = FMT == MOE_FMT_NVFP4 ? 4 : 1;  // 512-byte atoms per operand per stage
   static constexpr int SF_BYTES = SF_ATOMS * 512;
   static constexpr int RAW_STAGE = NA * A_BYTES + B_BYTES + (NA + 1) * SF_BYTES;
@@ -48,11 +55,11 @@ struct Cfg {
   static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + RTB_BYTES + 1024;
   static constexpr int ELEMS_PER_STAGE = FMT == MOE_FMT_NVFP4 ? 256 : 128;  // 128 bytes of codes
   static constexpr int BLOCK = FMT == MOE_FMT_NVFP4 ? 16 : 32;
-  static constexpr int ACC_COLS = kNT;          // one accumulator: 128 lanes x N columns
-  static constexpr int ACC_BUF = NA * ACC_COLS;  // gate (+ up) of one tile
+  static constexpr int ACC_COLS = NT;            // one accumulator: 128 lanes x N columns
+  static constexpr int ACC_BUF = NA * ACC_COLS;  // both weight blocks of one tile
   static constexpr int SF_COLS_OP = SF_ATOMS * 4;
   static constexpr int SF_COLS_STAGE = (NA + 1) * SF_COLS_OP;
-  static constexpr int TMEM_SF = 2 * ACC_BUF;
+  static constexpr int TMEM_SF = ACC_BUFS * ACC_BUF;
   static constexpr int TMEM_COLS = 512;
   static_assert(TMEM_SF + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
   static_assert(SMEM <= 232448, "shared memory budget");
@@ -94,11 +101,11 @@ __device__ __forceinline__ void map_tile(int t, int MT, const int32_t* rtb, int 
   rt = rtb[lo] + l % nrt;
 }
 
-template <int FMT, bool GATED>
-__global__ void __launch_bounds__(256, 1)
+template <int FMT, bool GATED, bool WIDE>
+__global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-  using C = Cfg<FMT, GATED>;
+  using C = Cfg<FMT, GATED, WIDE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -118,7 +125,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tmem_full[b], 1);
-      mbar_init(&tmem_empty[b], 4);
+      mbar_init(&tmem_empty[b], C::EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -178,7 +185,7 @@ __global__ void __launch_bounds__(256, 1)
         const int arow1 = (GATED || !second) ? arow : arow + 128;
         const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
         const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
-        const uint8_t* sfb = a.sfB + (int64_t)(rt.row / kNT) * atoms_per_row * 512;
+        const uint8_t* sfb = a.sfB + (int64_t)(rt.row / C::NT) * atoms_per_row * 512;
         const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
@@ -243,8 +250,8 @@ __global__ void __launch_bounds__(256, 1)
           map_tile(t + gridDim.x, MT, s_rtb, a.E, mt_n, rti_n);
           nv_next = a.tiles[rti_n].n_valid;
         }
-        const int buf = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1) & 1u;
+        const int buf = it % C::ACC_BUFS;
+        const uint32_t use = (uint32_t)(it / C::ACC_BUFS) & 1u;
         if (!mbar_wait(&tmem_empty[buf], use ^ 1, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
           ok = false;
           break;
@@ -303,7 +310,11 @@ __global__ void __launch_bounds__(256, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
+    // Warp (4 + i) reads TMEM lane quadrant i % 4 (its 32 output features)
+    // for token columns [64 * (i / 4), +64): the whole share goes to
+    // registers first, TMEM is released, then the arithmetic and stores run.
     const int q = warp & 3;
+    const int col_lo = ((warp - 4) >> 2) * 64;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -312,32 +323,43 @@ __global__ void __launch_bounds__(256, 1)
       const RowTile rt = a.tiles[rti];
       const int f = mt * C::ROWS + q * 32 + lane;       // feature of accumulator 0 (down: +128 for 1)
       const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+      const int col_hi = min(rt.n_valid, col_lo + 64);
       float sA0 = 1.0f, sA1 = 1.0f, gb_lo = 1.0f, gb_hi = 1.0f;
       if constexpr (FMT == MOE_FMT_NVFP4) {
         sA0 = a.gA0[rt.e];
         sA1 = a.gA1[rt.e];
-        if (lane < rt.n_valid) gb_lo = a.gB[rt.row + lane];
-        if (32 + lane < rt.n_valid) gb_hi = a.gB[rt.row + 32 + lane];
+        if (col_lo + lane < col_hi) gb_lo = a.gB[rt.row + col_lo + lane];
+        if (col_lo + 32 + lane < col_hi) gb_hi = a.gB[rt.row + col_lo + 32 + lane];
       }
-      const int buf = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1) & 1u;
+      const int buf = it % C::ACC_BUFS;
+      const uint32_t use = (uint32_t)(it / C::ACC_BUFS) & 1u;
       if (!mbar_wait(&tmem_full[buf], use, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
       tc_fence_after();
       const uint32_t tacc = tq + buf * C::ACC_BUF;
-      for (int c0 = 0; c0 < rt.n_valid; c0 += 16) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(tacc + c0, r0);
-        tmem_ld16(tacc + C::ACC_COLS + c0, r1);
-        tmem_wait_ld();
+      uint32_t r0[4][16], r1[4][16];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        if (col_lo + ch * 16 < col_hi) {
+          tmem_ld16(tacc + col_lo + ch * 16, r0[ch]);
+          tmem_ld16(tacc + C::ACC_COLS + col_lo + ch * 16, r1[ch]);
+        }
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        if (col_lo + ch * 16 >= col_hi) continue;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const int n = c0 + j;
-          const float gb = __shfl_sync(0xffffffffu, n < 32 ? gb_lo : gb_hi, n & 31);
-          if (n < rt.n_valid) {
+          const int n = col_lo + ch * 16 + j;
+          const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
+          if (n < col_hi) {
             const int64_t row = (int64_t)rt.row + n;
             if constexpr (GATED) {
-              float g = __uint_as_float(r0[j]) * (sA0 * gb);
-              float u = __uint_as_float(r1[j]) * (sA1 * gb);
+              float g = __uint_as_float(r0[ch][j]) * (sA0 * gb);
+              float u = __uint_as_float(r1[ch][j]) * (sA1 * gb);
               if (a.cap > 0.0f) {
                 g = a.cap * tanhf(g / a.cap);
                 u = a.cap * tanhf(u / a.cap);
@@ -346,15 +368,12 @@ __global__ void __launch_bounds__(256, 1)
               a.h_out[row * a.NA + f] = __float2bfloat16_rn(h);
             } else {
               float* yrow = a.y_out + (int64_t)(rt.canon + n) * a.NA;
-              yrow[f] = __uint_as_float(r0[j]) * (sA0 * gb);
-              if (second) yrow[f + 128] = __uint_as_float(r1[j]) * (sA1 * gb);
+              yrow[f] = __uint_as_float(r0[ch][j]) * (sA0 * gb);
+              if (second) yrow[f + 128] = __uint_as_float(r1[ch][j]) * (sA1 * gb);
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tmem_empty[buf]);
     }
   }
   __syncthreads();
@@ -365,12 +384,12 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int FMT, bool GATED>
+template <int FMT, bool GATED, bool WIDE>
 cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  using C = Cfg<FMT, GATED>;
+  using C = Cfg<FMT, GATED, WIDE>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -392,15 +411,20 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   a.status = g.status;
   a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock
   a.withhold_loads = g.withhold_loads;
-  return launch_k(k_moe_gemm<FMT, GATED>, dim3(g.num_sms), dim3(256), C::SMEM, st, pdl, *g.tmA0, *g.tmA1, *g.tmB, a);
+  return launch_k(k_moe_gemm<FMT, GATED, WIDE>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
+                  *g.tmB, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  if (g.cfg->fmt == MOE_FMT_NVFP4)
-    return g.gated ? launch_t<MOE_FMT_NVFP4, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false>(g, st, pdl);
-  return g.gated ? launch_t<MOE_FMT_MXFP8, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false>(g, st, pdl);
+  const bool wide = tile_rows(*g.cfg) == kNTWide;
+  if (g.cfg->fmt == MOE_FMT_NVFP4) {
+    if (wide) return g.gated ? launch_t<MOE_FMT_NVFP4, true, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, true>(g, st, pdl);
+    return g.gated ? launch_t<MOE_FMT_NVFP4, true, false>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, false>(g, st, pdl);
+  }
+  if (wide) return g.gated ? launch_t<MOE_FMT_MXFP8, true, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, true>(g, st, pdl);
+  return g.gated ? launch_t<MOE_FMT_MXFP8, true, false>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, false>(g, st, pdl);
 }
 
 }  // namespace moe

@@ -11,16 +11,19 @@
 
 namespace moe {
 
-// Token rows per expert tile (MMA N <= kNT).  Each expert's rows start at a
-// multiple of kNT in the expert-grouped activation buffers.
-constexpr int kNT = 64;
+// Token rows per expert tile (MMA N <= NT): 64 for decode batches (two TMEM
+// accumulator buffers), 128 when the experts see 64 tokens or more on average
+// (one buffer, twice the work per weight byte).  Each expert's rows start at a
+// multiple of NT in the expert-grouped activation buffers.
+constexpr int kNTDecode = 64;
+constexpr int kNTWide = 128;
 
-// One block of up to kNT consecutive rows of one expert in padded row order.
+// One block of up to NT consecutive rows of one expert in padded row order.
 struct RowTile {
   int e;        // expert
-  int row;      // first padded row (multiple of kNT)
-  int n_valid;  // valid rows in the tile (1..kNT)
-  int canon;    // first canonical pair position (offsets[e] + kNT*i)
+  int row;      // first padded row (multiple of NT)
+  int n_valid;  // valid rows in the tile (1..NT)
+  int canon;    // first canonical pair position (offsets[e] + NT*i)
 };
 
 constexpr int kTileRows = 128;     // weight rows (MMA M) per tile
@@ -31,14 +34,17 @@ constexpr int kMaxK = 32;
 inline int block_elems(moe_format f) { return f == MOE_FMT_NVFP4 ? 16 : 32; }
 inline int64_t code_bytes(moe_format f, int64_t K) { return f == MOE_FMT_NVFP4 ? K / 2 : K; }
 
+inline int tile_rows(const moe_config& c) {
+  return (int64_t)c.T * c.k >= (int64_t)64 * c.E ? kNTWide : kNTDecode;
+}
 // Padded row capacity of the expert-grouped activation buffers.
 inline int64_t padded_rows(const moe_config& c) {
-  int64_t P = (int64_t)c.T * c.k;
-  return ((P + kNT - 1) / kNT + c.E) * kNT;
+  const int64_t P = (int64_t)c.T * c.k, nt = tile_rows(c);
+  return ((P + nt - 1) / nt + c.E) * nt;
 }
-inline int64_t max_row_tiles(const moe_config& c) { return padded_rows(c) / kNT; }
+inline int64_t max_row_tiles(const moe_config& c) { return padded_rows(c) / tile_rows(c); }
 // Bytes of activation block scales in the per-row-tile atom layout.
-inline int64_t act_scale_bytes(int64_t R, int64_t scale_cols) { return (R / kNT) * (scale_cols / 4) * 512; }
+inline int64_t act_scale_bytes(int64_t R, int64_t scale_cols, int nt) { return (R / nt) * (scale_cols / 4) * 512; }
 
 void ws_layout(const moe_config& c, moe_ws_layout* L);
 

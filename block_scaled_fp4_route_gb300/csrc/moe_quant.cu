@@ -115,7 +115,7 @@ __device__ __forceinline__ float nvfp4_G(float amax) { return amax == 0.0f ? 1.0
 enum ScaleLayout { SL_ROWMAJOR = 0, SL_TILED = 1, SL_ACT = 2 };
 
 __device__ __forceinline__ int64_t scale_index(int layout, int64_t r, int64_t c, int64_t C) {
-  return layout == SL_TILED ? tiled_scale_offset(r, c, C) : (layout == SL_ACT ? act_scale_offset(r, c, C) : r * C + c);
+  return layout == SL_TILED ? tiled_scale_offset(r, c, C) : r * C + c;
 }
 
 template <int FMT, typename Src>
@@ -157,7 +157,7 @@ constexpr int kRowRounds = 2;
 template <int FMT>
 __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
                                                const int64_t* dst, uint8_t* codes, uint8_t* scales, float* glob,
-                                               float* red) {
+                                               float* red, int nt) {
   constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   const int nb = K / BS;
   const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
@@ -188,7 +188,7 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
       for (int d = 0; d < ndst; ++d) {
         const int64_t rr = dst[d];
         *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
-        scales[act_scale_offset(rr, b, C)] = (uint8_t)sc;
+        scales[act_scale_offset(rr, b, C, nt)] = (uint8_t)sc;
       }
     } else {
       uint4 c[2];
@@ -198,7 +198,7 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
         uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
         o[0] = c[0];
         o[1] = c[1];
-        scales[act_scale_offset(rr, b, C)] = (uint8_t)sc;
+        scales[act_scale_offset(rr, b, C, nt)] = (uint8_t)sc;
       }
     }
   }
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ pair_pos,
                                                        const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                       uint8_t* scales, float* glob) {
+                                                       uint8_t* scales, float* glob, int nt) {
   __shared__ float red[32];
   __shared__ int64_t dst[kMaxK];
   const int t = blockIdx.x;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
     dst[threadIdx.x] = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
   }
   __syncthreads();
-  quant_row_regs<FMT>(x + (int64_t)t * H, H, mx_mode, k, dst, codes, scales, glob, red);
+  quant_row_regs<FMT>(x + (int64_t)t * H, H, mx_mode, k, dst, codes, scales, glob, red, nt);
 }
 
 // h: one CTA per canonical pair position p; row = its padded row.
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ perm,
                                                        const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                       uint8_t* scales, float* glob) {
+                                                       uint8_t* scales, float* glob, int nt) {
   __shared__ float red[32];
   __shared__ int64_t dst[1];
   const int p = blockIdx.x;
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
     dst[0] = (int64_t)seg_start[e] + (p - offsets[e]);
   }
   __syncthreads();
-  quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, codes, scales, glob, red);
+  quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, codes, scales, glob, red, nt);
 }
 
 // Many short rows (prefill): one warp per row, eight rows per CTA.  Pass 1
@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
 // block by block.  dst_lane: lane d < ndst holds destination row d.
 template <int FMT>
 __device__ __forceinline__ void quant_row_warp(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
-                                               int64_t dst_lane, uint8_t* codes, uint8_t* scales, float* glob) {
+                                               int64_t dst_lane, uint8_t* codes, uint8_t* scales, float* glob, int nt) {
   constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   const int lane = threadIdx.x & 31;
   const int nb = K / BS;
@@ -281,7 +281,7 @@ __device__ __forceinline__ void quant_row_warp(const __nv_bfloat16* __restrict__
       for (int d = 0; d < ndst; ++d) {
         const int64_t rr = __shfl_sync(0xffffffffu, dst_lane, d);
         *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
-        scales[act_scale_offset(rr, b, nb)] = (uint8_t)sc;
+        scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
       }
     } else {
       uint4 c[2];
@@ -291,7 +291,7 @@ __device__ __forceinline__ void quant_row_warp(const __nv_bfloat16* __restrict__
         uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
         o[0] = c[0];
         o[1] = c[1];
-        scales[act_scale_offset(rr, b, nb)] = (uint8_t)sc;
+        scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
       }
     }
   }
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __
                                                          const int32_t* __restrict__ pair_pos,
                                                          const int32_t* __restrict__ perm,
                                                          const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                         uint8_t* scales, float* glob) {
+                                                         uint8_t* scales, float* glob, int nt) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_wait();
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __
     row = src + (int64_t)r * K;
     ndst = k;
   }
-  quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, codes, scales, glob);
+  quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, codes, scales, glob, nt);
 }
 
 constexpr int kWarpRowsFrom = 2048;  // rows from which one warp per row is used
@@ -452,11 +452,11 @@ cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const in
   if (c.T >= kWarpRowsFrom) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((c.T + 7) / 8), dim3(256), 0, st, pdl, x, c.T, c.H, c.k, 0, c.mx_scale_mode, idx, offsets,
-                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob);
+                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob, tile_rows(c));
   }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_x<MOE_FMT_NVFP4> : k_quant_x<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(c.T), dim3(kQThreads), 0, st, pdl, x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
-                  seg_start, codes, scales, glob);
+                  seg_start, codes, scales, glob, tile_rows(c));
 }
 
 cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx, const int32_t* offsets,
@@ -466,11 +466,11 @@ cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const in
   if (P >= kWarpRowsFrom) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((P + 7) / 8), dim3(256), 0, st, pdl, h, P, c.F, c.k, 1, c.mx_scale_mode, idx, offsets,
-                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob);
+                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob, tile_rows(c));
   }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_h<MOE_FMT_NVFP4> : k_quant_h<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(P), dim3(kQThreads), 0, st, pdl, h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
-                  codes, scales, glob);
+                  codes, scales, glob, tile_rows(c));
 }
 
 cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,

@@ -268,12 +268,13 @@ MOE_API moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qw
 
 /* Byte offsets of the layer's intermediates inside the workspace, for
  * inspection by tests (all buffers in padded expert-row order: each expert's
- * rows start at a multiple of 64).  R = padded row capacity.  The activation
- * block scales (xq_scales, hq_scales) use one 512-byte atom per 64-row tile
- * and 4 scale columns: row r, column c at
- *   ((r/64)*(C/4) + c/4)*512 + (r%64%32)*16 + (r%64/32)*4 + c%4. */
+ * rows start at a multiple of tile_rows = NT).  R = padded row capacity.  The
+ * activation block scales (xq_scales, hq_scales) use one 512-byte atom per
+ * NT-row tile and 4 scale columns: row r, column c at
+ *   ((r/NT)*(C/4) + c/4)*512 + (r%NT%32)*16 + (r%NT/32)*4 + c%4. */
 typedef struct {
   int64_t R;
+  int64_t tile_rows; /* token rows per expert tile: 64 (decode) or 128 */
   size_t status, logits, topk_idx, topk_w, counts, offsets, perm, pair_pos, bitmap, seg_start,
       tiles, rt_base, xq_codes, xq_scales, xq_global, h_bf16, hq_codes, hq_scales, hq_global,
       y_perm, total;

@@ -53,8 +53,10 @@ def test_workspace_size_and_layout():
                            "bitmap", "seg_start", "tiles", "rt_base", "xq_codes", "xq_scales", "xq_global",
                            "h_bf16", "hq_codes", "hq_scales", "hq_global", "y_perm", "total"]]
     assert offs == sorted(offs) and all(o % 1024 == 0 for o in offs)
-    # padded rows: one 64-row tile per expert on top of the pairs
-    assert L["R"] == ((64 * 8 + 63) // 64 + 384) * 64
+    # padded rows: one token tile per expert on top of the pairs
+    assert L["tile_rows"] == 64 and L["R"] == ((64 * 8 + 63) // 64 + 384) * 64
+    Lp = moe.moe_workspace_layout(cfg(T=4096))      # >= 64 tokens per expert: 128-row tiles
+    assert Lp["tile_rows"] == 128 and Lp["R"] == ((4096 * 8 + 127) // 128 + 384) * 128
     assert L["hq_codes"] - L["h_bf16"] >= L["R"] * 2304 * 2
     # larger T needs no less workspace
     assert moe.moe_workspace_size(cfg(T=4096)) > n

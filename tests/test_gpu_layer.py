@@ -71,9 +71,10 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
     nv = w["fmt"] == "nvfp4"
     cb, bs = (H // 2, 16) if nv else (H, 32)
     codes = gw.ws_view("xq_codes", torch.uint8, R * cb).view(R, cb)
-    scales = gw.ws_view("xq_scales", torch.uint8, R * (H // bs) * 2).cpu().numpy()
+    nt = gw.layout["tile_rows"]
+    scales = gw.ws_view("xq_scales", torch.uint8, (R // nt) * (H // bs // 4) * 512).cpu().numpy()
     gcodes = codes[torch.from_numpy(prow.ravel()).cuda()].cpu().numpy().reshape(len(tokens), k, cb)
-    gsc = untile_scales(scales, R, H // bs, tile_rows=64)[prow.ravel()].reshape(len(tokens), k, H // bs)
+    gsc = untile_scales(scales, R, H // bs, tile_rows=nt)[prow.ravel()].reshape(len(tokens), k, H // bs)
     for j in range(k):
         assert np.array_equal(gcodes[:, j], xq[0])
         assert np.array_equal(gsc[:, j], xq[1])

@@ -287,7 +287,7 @@ def main():
     ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
     ms_per_step = ms / args.steps
     value = job_tokens_per_s(T, args.steps, world, ms)
-    launches_per_step = 10
+    launches_per_step = moe.moe_forward_kernel_count(gw.cfg)
 
     # ---- per-stage device times (events between the stages, same stream) ----
     n_prof = min(args.steps, 200)

@@ -22,7 +22,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
-            "moe_route_noalloc", "moe_fake_quantize", "moe_selftest_bounded_wait", "moe_status_string"]
+            "moe_route_noalloc", "moe_fake_quantize", "moe_selftest_bounded_wait", "moe_forward_kernel_count",
+            "moe_status_string"]
 
 
 class MoeError(RuntimeError):
@@ -130,6 +131,12 @@ def qweight(codes, scales, global_scale=None) -> moe_qweight:
 def moe_workspace_size(cfg: moe_config) -> int:
     n = ctypes.c_size_t(0)
     _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def moe_forward_kernel_count(cfg: moe_config) -> int:
+    n = ctypes.c_int(0)
+    _check("moe_forward_kernel_count", lib().moe_forward_kernel_count(ctypes.byref(cfg), ctypes.byref(n)))
     return n.value
 
 

@@ -176,13 +176,17 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g1.NA = c.F;
   g1.K = c.H;
   g1.h_out = h;
+  g1.hq_codes = hq;
+  g1.hq_scales = hs;
   g1.status = status;
   g1.num_sms = sms;
   mark(ev, 3, st);
   if (launch_gemm(g1, st, true) != cudaSuccess) return MOE_ERR_CUDA;
 
   mark(ev, 4, st);
-  if (launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h_row_pass(c) &&
+      launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st, true) != cudaSuccess)
+    return MOE_ERR_CUDA;
 
   GemmLaunch g2{};
   g2.cfg = &c;
@@ -256,7 +260,7 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
   L->xq_codes = take(R * code_bytes(c.fmt, c.H));
   L->xq_scales = take(act_scale_bytes(R, c.H / bs, tile_rows(c)));
   L->xq_global = take(R * 4);
-  L->h_bf16 = take(R * c.F * 2);
+  L->h_bf16 = take(h_row_pass(c) ? R * c.F * 2 : 0);
   L->hq_codes = take(R * code_bytes(c.fmt, c.F));
   L->hq_scales = take(act_scale_bytes(R, c.F / bs, tile_rows(c)));
   L->hq_global = take(R * 4);
@@ -388,6 +392,21 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   s = cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st, true));
   mark(ev, 7, st);
   return s;
+}
+
+moe_status moe_forward_kernel_count(const moe_config* cfg, int* count) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!count) return MOE_ERR_INVALID_ARG;
+  const moe_config& c = *cfg;
+  int n = 2;                                  // router: logits, top-k
+  n += dispatch_fits_one_cta(c) ? 1 : 3;      // dispatch: one CTA, or bitmap + scan + scatter
+  n += 1;                                     // x quantisation
+  n += 1;                                     // GEMM1
+  n += h_row_pass(c) ? 1 : 0;                 // h quantisation (else inside GEMM1)
+  n += 2;                                     // GEMM2, combine
+  *count = n;
+  return MOE_OK;
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev, const float* bias_dev,

@@ -60,18 +60,18 @@ __device__ __forceinline__ uint32_t e2m1_encode(float v) {
   return sign | q;
 }
 
+// Written with selects only (no branches), so that unrolled callers can
+// interleave independent elements.
 __device__ __forceinline__ uint32_t e4m3_encode(float v) {
-  uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
-  float a = fabsf(v);
-  if (!(a < 448.0f)) return sign | 0x7Eu;
-  int e = (int)(__float_as_uint(a) >> 23) - 127;
-  if (e < -6) {  // E4M3 subnormal range: quantum 2^-9
-    uint32_t q = __float2uint_rn(__fmul_rn(a, 512.0f));
-    return sign | q;  // q == 8 encodes the smallest normal 0x08
-  }
-  uint32_t m = __float2uint_rn(__fmul_rn(a, exp2i(3 - e)));  // in [8, 16]
-  if (m == 16) { m = 8; e += 1; }
-  return sign | ((uint32_t)(e + 7) << 3) | (m - 8);
+  const uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
+  const float a = fabsf(v);
+  // exponent of a, clamped below at -6: the subnormal range has the quantum
+  // 2^-9 of the smallest normal binade
+  const int e = max((int)(__float_as_uint(a) >> 23) - 127, -6);
+  const uint32_t m = __float2uint_rn(__fmul_rn(a, exp2i(3 - e)));  // normal: [8, 16]; subnormal: [0, 8]
+  const uint32_t up = m == 16u;                                     // rounded into the next binade
+  const uint32_t mag = m < 8u ? m : (((uint32_t)(e + 7) + up) << 3) | (up ? 0u : m - 8u);
+  return sign | (a < 448.0f ? mag : 0x7Eu);  // saturate (also NaN)
 }
 
 // E2M1 code -> value {0, .5, 1, 1.5, 2, 3, 4, 6} with sign (exact).
@@ -89,20 +89,19 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 
 // floor(log2 a) for a finite a > 0, exact from the bits.
 __device__ __forceinline__ int ilog2_floor(float a) {
-  uint32_t b = __float_as_uint(a);
-  int ef = (int)(b >> 23);
-  if (ef > 0) return ef - 127;
-  uint32_t m = b & 0x7FFFFFu;
-  return (31 - __clz(m)) - 149;
+  const uint32_t b = __float_as_uint(a);
+  const int ef = (int)(b >> 23);
+  const int sub = (31 - __clz(b & 0x7FFFFFu)) - 149;  // subnormal: position of the leading bit
+  return ef > 0 ? ef - 127 : sub;
 }
 
 __device__ __forceinline__ int ilog2_ceil(float a) {
-  uint32_t b = __float_as_uint(a);
-  int ef = (int)(b >> 23);
-  uint32_t m = b & 0x7FFFFFu;
-  if (ef > 0) return ef - 127 + (m != 0);
-  int p = 31 - __clz(m);
-  return p - 149 + (m != (1u << p));
+  const uint32_t b = __float_as_uint(a);
+  const int ef = (int)(b >> 23);
+  const uint32_t m = b & 0x7FFFFFu;
+  const int p = 31 - __clz(m);
+  const int sub = p - 149 + (m != (1u << (p & 31)));
+  return ef > 0 ? ef - 127 + (m != 0u) : sub;
 }
 
 // E8M0 scale byte of one MXFP8 block with absolute maximum amax_b > 0.
@@ -265,6 +264,19 @@ __device__ __forceinline__ void mma_mxfp8(uint32_t d, uint64_t adesc, uint64_t b
           d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
       : "memory");
+}
+
+// Hardware approximations (PTX ex2.approx / rcp.approx, relative error of a
+// few 2^-23).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // 32 lanes x 16 consecutive 32-bit columns of TMEM into registers.

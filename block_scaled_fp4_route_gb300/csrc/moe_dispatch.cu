@@ -225,8 +225,10 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
 
 }  // namespace
 
+// The one-CTA path ranks each expert's tokens serially, so it is kept for
+// decode batches (up to 256 tokens).
 bool dispatch_fits_one_cta(const moe_config& c) {
-  return c.E <= 1024 && (int64_t)c.E * ((c.T + 31) / 32) <= kSmallWords;
+  return c.T <= 256 && c.E <= 1024 && (int64_t)c.E * ((c.T + 31) / 32) <= kSmallWords;
 }
 
 cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,

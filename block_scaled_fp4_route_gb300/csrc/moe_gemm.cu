@@ -13,7 +13,11 @@
 // one or two tokens per expert wastes no weight bytes, and each pipeline
 // stage carries 32 KB of weights.
 //   GEMM1 (gated):  A0 = 128 W_gate rows, A1 = the same 128 W_up rows,
-//                   epilogue h = bf16(silu(cap g) * cap u)
+//                   epilogue h = bf16(silu(cap g) * cap u); with 64-row
+//                   token tiles and MXFP8 the epilogue also quantises h (a
+//                   warp holds one 32-feature block of a token row); else
+//                   h goes to a row pass (NVFP4: its global spans the row;
+//                   128-row tiles: measured faster than the longer epilogue)
 //   GEMM2:          A0, A1 = 256 consecutive W_down rows,
 //                   epilogue y = acc * g_w * g_h (fp32)
 // Tiles are walked expert by expert, then weight-row block, then token block,
@@ -79,12 +83,44 @@ struct GemmArgs {
   int NA;  // weight rows per expert (= output features; also the output row stride)
   int K;   // reduction length in elements
   float cap;
-  __nv_bfloat16* h_out;
+  float inv_cap;  // fp32(1 / cap), 0 when cap == 0
+  __nv_bfloat16* h_out;  // NVFP4: bf16 h (quantised by a row pass: its global spans the row)
+  uint8_t* hq_codes;     // MXFP8: h codes and scales written by the epilogue
+  uint8_t* hq_scales;
+  int mx_mode;
   float* y_out;
   uint32_t* status;
   long long limit;
   int withhold_loads;
 };
+
+// tanh for the soft cap c * tanh(v / c), in fp32 to a few ulp: below 0.5 the
+// odd Taylor series of tanh through the x^15 term (alternating, so the
+// truncation error is under the first dropped term, 9e-9 relative at 0.5);
+// above, 1 - 2 / (e^{2|x|} + 1), which has no cancellation there, with the
+// hardware base-2 exponential and reciprocal.
+__device__ __forceinline__ float tanh_soft(float x) {
+  const float ax = fabsf(x);
+  if (ax < 0.5f) {
+    const float x2 = x * x;
+    float p = -929569.0f / 638512875.0f;
+    p = fmaf(p, x2, 21844.0f / 6081075.0f);
+    p = fmaf(p, x2, -1382.0f / 155925.0f);
+    p = fmaf(p, x2, 62.0f / 2835.0f);
+    p = fmaf(p, x2, -17.0f / 315.0f);
+    p = fmaf(p, x2, 2.0f / 15.0f);
+    p = fmaf(p, x2, -1.0f / 3.0f);
+    return fmaf(x * x2, p, x);
+  }
+  const float e = ex2_approx(2.8853900817779268f * ax);  // e^{2|x|}; +inf for large |x|
+  return copysignf(1.0f - 2.0f * rcp_approx(e + 1.0f), x);
+}
+
+// silu(g) = g / (1 + e^{-g}), with the hardware base-2 exponential and
+// reciprocal (a few ulp; -0 for large negative g, g for large positive g).
+__device__ __forceinline__ float silu(float g) {
+  return g * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * g));
+}
 
 // Tile t -> (expert e, weight-row block mt, row tile index rt) in the order
 // expert, mt, token block.  rtb[e] is the first row tile of expert e.
@@ -336,6 +372,40 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
       if (!mbar_wait(&tmem_full[buf], use, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
       tc_fence_after();
       const uint32_t tacc = tq + buf * C::ACC_BUF;
+      // one 16-column chunk of the gated epilogue: h = bf16(silu(cap g) cap u),
+      // then (MXFP8, 64-row tiles) its codes and block scale, else the bf16 h.  Every element
+      // of the chunk is computed (columns past n_valid hold stale accumulators
+      // and are only discarded), so the 16 elements are straight-line code;
+      // only the stores are predicated.
+      auto gated_chunk = [&](const uint32_t (&c0)[16], const uint32_t (&c1)[16], int ch) {
+        const float gbv = ch < 2 ? gb_lo : gb_hi;
+        const bool capped = a.cap > 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int n = col_lo + ch * 16 + j;
+          const bool valid = n < col_hi;  // warp-uniform
+          float gb = 1.0f;
+          if constexpr (FMT == MOE_FMT_NVFP4) gb = __shfl_sync(0xffffffffu, gbv, (ch * 16 + j) & 31);
+          const int64_t row = (int64_t)rt.row + n;
+          float g = __uint_as_float(c0[j]) * (sA0 * gb);
+          float u = __uint_as_float(c1[j]) * (sA1 * gb);
+          g = capped ? a.cap * tanh_soft(g * a.inv_cap) : g;
+          u = capped ? a.cap * tanh_soft(u * a.inv_cap) : u;
+          const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * u);
+          if constexpr (FMT == MOE_FMT_MXFP8 && !WIDE) {
+            // the warp's 32 lanes are one 32-feature block of this token
+            // row; |v| orders like its bit pattern
+            const float v = __bfloat162float(hb);
+            const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
+            const uint32_t sc = m != 0.0f ? mx_scale_code(m, a.mx_mode) : 0u;
+            const uint32_t code = m != 0.0f ? e4m3_encode(__fmul_rn(v, exp2i(127 - (int)sc))) : 0u;
+            if (valid) a.hq_codes[row * a.NA + f] = (uint8_t)code;
+            if (valid && lane == 0) a.hq_scales[act_scale_offset(row, f >> 5, a.NA >> 5, C::NT)] = (uint8_t)sc;
+          } else {
+            if (valid) a.h_out[row * a.NA + f] = hb;
+          }
+        }
+      };
       uint32_t r0[4][16], r1[4][16];
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
@@ -348,25 +418,33 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tmem_empty[buf]);
+      if constexpr (GATED) {
+        // The gated element is long (soft cap, SwiGLU, MXFP8 quantisation), so
+        // only one 16-column chunk is unrolled (the chunks rotate through
+        // r0[0] / r1[0]): a fully unrolled epilogue no longer fits the
+        // instruction cache beside the producer and MMA loops.
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          if (col_lo + ch * 16 >= col_hi) break;
+          gated_chunk(r0[0], r1[0], ch);
+          // the next chunk moves to the front (register moves, no indexing)
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        if (col_lo + ch * 16 >= col_hi) continue;
+          for (int i = 0; i < 3; ++i)
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int n = col_lo + ch * 16 + j;
-          const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
-          if (n < col_hi) {
-            const int64_t row = (int64_t)rt.row + n;
-            if constexpr (GATED) {
-              float g = __uint_as_float(r0[ch][j]) * (sA0 * gb);
-              float u = __uint_as_float(r1[ch][j]) * (sA1 * gb);
-              if (a.cap > 0.0f) {
-                g = a.cap * tanhf(g / a.cap);
-                u = a.cap * tanhf(u / a.cap);
-              }
-              const float h = g / (1.0f + expf(-g)) * u;
-              a.h_out[row * a.NA + f] = __float2bfloat16_rn(h);
-            } else {
+            for (int j = 0; j < 16; ++j) {
+              r0[i][j] = r0[i + 1][j];
+              r1[i][j] = r1[i + 1][j];
+            }
+        }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          if (col_lo + ch * 16 >= col_hi) continue;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int n = col_lo + ch * 16 + j;
+            const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
+            if (n < col_hi) {
               float* yrow = a.y_out + (int64_t)(rt.canon + n) * a.NA;
               yrow[f] = __uint_as_float(r0[ch][j]) * (sA0 * gb);
               if (second) yrow[f + 128] = __uint_as_float(r1[ch][j]) * (sA1 * gb);
@@ -406,7 +484,11 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   a.NA = g.NA;
   a.K = g.K;
   a.cap = g.cfg->swiglu_cap;
+  a.inv_cap = a.cap > 0.0f ? 1.0f / a.cap : 0.0f;
   a.h_out = g.h_out;
+  a.hq_codes = g.hq_codes;
+  a.hq_scales = g.hq_scales;
+  a.mx_mode = g.cfg->mx_scale_mode;
   a.y_out = g.y_out;
   a.status = g.status;
   a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock

@@ -37,6 +37,10 @@ inline int64_t code_bytes(moe_format f, int64_t K) { return f == MOE_FMT_NVFP4 ?
 inline int tile_rows(const moe_config& c) {
   return (int64_t)c.T * c.k >= (int64_t)64 * c.E ? kNTWide : kNTDecode;
 }
+// h goes through the bf16 buffer and a row-quantisation pass for NVFP4 (its
+// global scale spans the whole row) and for 128-row tiles; MXFP8 with 64-row
+// tiles quantises h in GEMM1's epilogue.
+inline bool h_row_pass(const moe_config& c) { return c.fmt == MOE_FMT_NVFP4 || tile_rows(c) == kNTWide; }
 // Padded row capacity of the expert-grouped activation buffers.
 inline int64_t padded_rows(const moe_config& c) {
   const int64_t P = (int64_t)c.T * c.k, nt = tile_rows(c);
@@ -110,7 +114,9 @@ struct GemmLaunch {
   int E;
   int NA;              // rows of A per expert
   int K;               // reduction length (elements)
-  __nv_bfloat16* h_out;   // gated: [R, F]
+  __nv_bfloat16* h_out;   // gated, NVFP4: bf16 h [R, F]
+  uint8_t* hq_codes = nullptr;   // gated, MXFP8: h codes [R, F] and scales, written by the epilogue
+  uint8_t* hq_scales = nullptr;
   float* y_out;           // down:  [P, H]
   uint32_t* status;
   int num_sms;

@@ -174,7 +174,9 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_d
  *   a   = quantise(x_t) per token over the full H (NVFP4: per-row global)
  *   g,u = W_gate,e a , W_up,e a          (tcgen05 block-scaled MMA, fp32)
  *   h   = bf16( silu(cap g) * cap u )
- *   y_p = W_down,e quantise(h)           (NVFP4: per-row global over F)
+ *   y_p = W_down,e quantise(h)           (NVFP4: per-row global over F;
+ *                                         MXFP8, decode tiles: quantised in
+ *                                         GEMM1's epilogue)
  *   x_dev        bf16 [T, H]
  *   topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev: from moe_route /
  *                moe_dispatch (the tile plan is rebuilt from offsets_dev)
@@ -203,12 +205,18 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x_dev, const v
                        const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes,
                        void* stream);
 
+/* Number of kernels one moe_forward call launches for this configuration
+ * (2 router + 1 or 3 dispatch + x quantisation + GEMM1 + h quantisation
+ * unless GEMM1 did it + GEMM2 + combine).  Host-only; no device is touched.
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE as moe_forward's checks. */
+MOE_API moe_status moe_forward_kernel_count(const moe_config* cfg, int* count);
+
 /* moe_forward, also recording events[i] (cudaEvent_t handles, created by the
  * caller) on `stream` at the start of stage i and events[MOE_NUM_STAGES] after
  * the last, so that the caller can time each stage:
  *   0 router (logits, top-k)      1 dispatch (bitmap, scan, scatter)
  *   2 x quantisation              3 GEMM1 gate/up + capped SwiGLU
- *   4 h quantisation              5 GEMM2 down
+ *   4 h quantisation (empty when GEMM1 did it)  5 GEMM2 down
  *   6 combine
  * Same results as moe_forward. */
 #define MOE_NUM_STAGES 7
@@ -271,7 +279,9 @@ MOE_API moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qw
  * rows start at a multiple of tile_rows = NT).  R = padded row capacity.  The
  * activation block scales (xq_scales, hq_scales) use one 512-byte atom per
  * NT-row tile and 4 scale columns: row r, column c at
- *   ((r/NT)*(C/4) + c/4)*512 + (r%NT%32)*16 + (r%NT/32)*4 + c%4. */
+ *   ((r/NT)*(C/4) + c/4)*512 + (r%NT%32)*16 + (r%NT/32)*4 + c%4.
+ * h_bf16 is empty (sharing its offset with hq_codes) when GEMM1's epilogue
+ * quantises h itself: MXFP8 with tile_rows 64. */
 typedef struct {
   int64_t R;
   int64_t tile_rows; /* token rows per expert tile: 64 (decode) or 128 */

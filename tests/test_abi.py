@@ -58,6 +58,10 @@ def test_workspace_size_and_layout():
     Lp = moe.moe_workspace_layout(cfg(T=4096))      # >= 64 tokens per expert: 128-row tiles
     assert Lp["tile_rows"] == 128 and Lp["R"] == ((4096 * 8 + 127) // 128 + 384) * 128
     assert L["hq_codes"] - L["h_bf16"] >= L["R"] * 2304 * 2
+    Lm = moe.moe_workspace_layout(cfg(fmt="mxfp8"))  # MXFP8 decode: h quantised inside GEMM1, no bf16 h
+    assert Lm["hq_codes"] == Lm["h_bf16"]
+    Lw = moe.moe_workspace_layout(cfg(fmt="mxfp8", T=4096))  # 128-row tiles: bf16 h and a row pass
+    assert Lw["hq_codes"] - Lw["h_bf16"] >= Lw["R"] * 2304 * 2
     # larger T needs no less workspace
     assert moe.moe_workspace_size(cfg(T=4096)) > n
 
@@ -118,3 +122,13 @@ def test_argument_validation_without_a_device():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_pack_scales(ok, 100, 16, ok, stream=0)
     assert ei.value.status == 2
+
+
+def test_forward_kernel_count():
+    # router 2 + dispatch (1 for decode batches, else 3) + x quant + GEMM1 + (NVFP4: h quant) + GEMM2 + combine
+    assert moe.moe_forward_kernel_count(cfg()) == 8
+    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=192)) == 7
+    assert moe.moe_forward_kernel_count(cfg(T=4096)) == 10
+    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=16384)) == 10
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward_kernel_count(cfg(T=0))

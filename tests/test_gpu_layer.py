@@ -95,19 +95,36 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
         stats["err_over_rms"] = parity.check_output(gpu_out[tokens], res["out"])
 
     if check_h:
-        # h = bf16(silu(cap g) cap u): near-exact (GEMM accumulation order differs)
-        hbuf = gw.ws_view("h_bf16", torch.int16, R * F).view(R, F)
-        flips, total = 0, 0
+        # h = bf16(silu(cap g) cap u) as GEMM1 writes it, or, where GEMM1's
+        # epilogue quantises h itself (MXFP8, 64-row tiles), the h codes and
+        # block scales.  Near-exact: the GEMM accumulation order differs from
+        # the oracle's.
+        h_in_ws = gw.layout["hq_codes"] > gw.layout["h_bf16"]
+        if h_in_ws:
+            hbuf = gw.ws_view("h_bf16", torch.int16, R * F).view(R, F)
+        else:
+            hbuf = gw.ws_view("hq_codes", torch.uint8, R * F).view(R, F)
+            hs = untile_scales(gw.ws_view("hq_scales", torch.uint8, (R // nt) * (F // 32 // 4) * 512).cpu().numpy(),
+                               R, F // 32, tile_rows=nt)
+        flips, total, sflips, stotal = 0, 0, 0, 0
         od = res["dispatch"]
         for e, pr in res["pairs"].items():
             lo, hi = od["offsets"][e], od["offsets"][e + 1]
             pids = od["perm"][lo:hi]
             grow = prow[pids // k, pids % k]
-            gh = hbuf[torch.from_numpy(grow).cuda()].cpu().numpy().view(np.uint16)
-            flips += int((gh != pr["h_bf16"]).sum())
+            gh = hbuf[torch.from_numpy(grow).cuda()].cpu().numpy()
+            if h_in_ws:
+                flips += int((gh.view(np.uint16) != pr["h_bf16"]).sum())
+            else:
+                flips += int((gh != pr["hq_codes"]).sum())
+                sflips += int((hs[grow] != pr["hq_sf"]).sum())
+                stotal += pr["hq_sf"].size
             total += gh.size
         stats["h_flip_rate"] = flips / max(total, 1)
         assert stats["h_flip_rate"] < 0.01
+        if not h_in_ws:
+            stats["h_scale_flip_rate"] = sflips / max(stotal, 1)
+            assert stats["h_scale_flip_rate"] < 0.01
     return stats
 
 

@@ -100,20 +100,6 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2D u8 tensor [rows, row_bytes] with 128-byte swizzle, box 128 bytes x box_rows.
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 template <typename T>
@@ -225,14 +211,28 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, int32_t* count
   if (dispatch_fits_one_cta(c))
     return cuda_status(launch_dispatch_small(c, idx, counts, offsets, perm, pair_pos, seg, tiles, rtb, status, st, pdl));
   uint32_t* bm = at<uint32_t>(ws, L.bitmap);
-  if (launch_dispatch(c, idx, counts, offsets, perm, pair_pos, bm, st, pdl) != cudaSuccess ||
-      launch_scan_plan(c, counts, nullptr, offsets, seg, tiles, rtb, status, st, true) != cudaSuccess ||
+  int32_t* chunk_counts = reinterpret_cast<int32_t*>(bm + (size_t)c.E * ((c.T + 31) / 32));
+  if (launch_dispatch(c, idx, bm, chunk_counts, st, pdl) != cudaSuccess ||
+      launch_scan_plan(c, chunk_counts, counts, nullptr, offsets, seg, tiles, rtb, status, st, true) != cudaSuccess ||
       launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st, true) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
 }  // namespace
+
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 void ws_layout(const moe_config& c, moe_ws_layout* L) {
   const int64_t T = c.T, E = c.E, P = T * c.k, R = padded_rows(c), W = (T + 31) / 32;
@@ -246,14 +246,14 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
   L->R = R;
   L->tile_rows = tile_rows(c);
   L->status = take(256);
-  L->logits = take((size_t)router_splits(c) * T * E * 4);
+  L->logits = take(router_scratch_floats(c) * 4);
   L->topk_idx = take(P * 4);
   L->topk_w = take(P * 4);
   L->counts = take(E * 4);
   L->offsets = take((E + 1) * 4);
   L->perm = take(P * 4);
   L->pair_pos = take(P * 4);
-  L->bitmap = take(E * W * 4);
+  L->bitmap = take((E * W + (int64_t)dispatch_chunks(c) * E) * 4);  // bitmap [E, W], then chunk counts
   L->seg_start = take((E + 1) * 4);
   L->tiles = take(max_row_tiles(c) * sizeof(RowTile));
   L->rt_base = take((E + 1) * 4);
@@ -302,7 +302,8 @@ moe_status moe_route(const moe_config* cfg, const void* x_dev, const void* w_rou
   moe_ws_layout L;
   ws_layout(*cfg, &L);
   return cuda_status(launch_router(*cfg, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                                   at<float>(ws_dev, L.logits), topk_idx_dev, topk_w_dev, (cudaStream_t)stream, false));
+                                   at<float>(ws_dev, L.logits), topk_idx_dev, topk_w_dev,
+                                   at<uint32_t>(ws_dev, L.status), (cudaStream_t)stream, false));
 }
 
 moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int32_t* counts_dev, int32_t* offsets_dev,
@@ -335,7 +336,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_
   moe_ws_layout L;
   ws_layout(*cfg, &L);
   cudaStream_t st = (cudaStream_t)stream;
-  if (launch_scan_plan(*cfg, nullptr, offsets_dev, nullptr, at<int32_t>(ws_dev, L.seg_start),
+  if (launch_scan_plan(*cfg, nullptr, nullptr, offsets_dev, nullptr, at<int32_t>(ws_dev, L.seg_start),
                        at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.rt_base),
                        at<uint32_t>(ws_dev, L.status), st, false) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -379,11 +380,12 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
   float* y = at<float>(ws_dev, L.y_perm);
   mark(ev, 0, st);
+  // the router's first kernel clears the status word of the call
   if (launch_router(c, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                    at<float>(ws_dev, L.logits), idx, w, st, false) != cudaSuccess)
+                    at<float>(ws_dev, L.logits), idx, w, at<uint32_t>(ws_dev, L.status), st, false) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(ev, 1, st);
-  s = dispatch_impl(c, idx, counts, offsets, perm, pair_pos, ws_dev, at<uint32_t>(ws_dev, L.status), st, true);
+  s = dispatch_impl(c, idx, counts, offsets, perm, pair_pos, ws_dev, nullptr, st, true);
   if (s != MOE_OK) return s;
   (void)bm;
   s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st, ev);
@@ -399,7 +401,7 @@ moe_status moe_forward_kernel_count(const moe_config* cfg, int* count) {
   if (s != MOE_OK) return s;
   if (!count) return MOE_ERR_INVALID_ARG;
   const moe_config& c = *cfg;
-  int n = 2;                                  // router: logits, top-k
+  int n = router_uses_tc(c) ? 3 : 2;         // router: (norms,) logits, top-k
   n += dispatch_fits_one_cta(c) ? 1 : 3;      // dispatch: one CTA, or bitmap + scan + scatter
   n += 1;                                     // x quantisation
   n += 1;                                     // GEMM1

@@ -4,10 +4,11 @@
 // plan the grouped GEMMs walk.
 //
 // Three small kernels, all deterministic:
-//   1. one CTA per expert builds the expert's token bitmap in shared memory
-//      from topk_idx and counts its pairs;
-//   2. one CTA scans counts -> offsets, padded segment starts (each expert's
-//      rows begin at a multiple of nt) and the list of nt-row tiles;
+//   1. one CTA per 256-token chunk sets the chunk's bits of every expert's
+//      token bitmap (shared memory, then global) and counts them;
+//   2. one CTA sums the chunk counts and scans counts -> offsets, padded
+//      segment starts (each expert's rows begin at a multiple of nt) and the
+//      list of nt-row tiles;
 //   3. one CTA per expert ranks its tokens from the bitmap (popcount prefix)
 //      and writes perm / pair_pos.
 #include "moe_common.cuh"
@@ -17,38 +18,37 @@ namespace moe {
 namespace {
 
 constexpr int kDThreads = 256;
-constexpr int kMaxWords = kMaxT / 32;
 
-__global__ void __launch_bounds__(kDThreads) k_disp_bitmap(const int32_t* __restrict__ idx, int T, int k,
-                                                           uint32_t* __restrict__ bitmap, int32_t* __restrict__ counts) {
-  __shared__ uint32_t bm[kMaxWords];
-  __shared__ int red[kDThreads / 32];
-  const int e = blockIdx.x;
-  const int W = (T + 31) / 32;
+constexpr int kChunkTokens = 256;  // tokens per bitmap CTA: 8 bitmap words per expert
+
+// One CTA per 256-token chunk: the chunk's token bits of every expert are
+// set in shared memory, copied to the global bitmap [E, W], and counted per
+// expert into chunk_counts [chunk, E].  idx is read once in total.
+__global__ void __launch_bounds__(kDThreads) k_disp_bitmap(const int32_t* __restrict__ idx, int T, int k, int E,
+                                                           uint32_t* __restrict__ bitmap,
+                                                           int32_t* __restrict__ chunk_counts) {
+  extern __shared__ uint32_t cbm[];  // [E][8]
+  const int ch = blockIdx.x;
+  const int t0 = ch * kChunkTokens, t1 = min(T, t0 + kChunkTokens);
+  const int W = (T + 31) / 32, w0 = t0 / 32, nw = min(8, W - w0);
   pdl_wait();
   pdl_trigger();
-  for (int i = threadIdx.x; i < W; i += blockDim.x) bm[i] = 0u;
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) cbm[i] = 0u;
   __syncthreads();
-  const int P = T * k;
-  for (int p = threadIdx.x; p < P; p += blockDim.x)
-    if (idx[p] == e) {
-      int t = p / k;
-      atomicOr(&bm[t >> 5], 1u << (t & 31));
-    }
-  __syncthreads();
-  int c = 0;
-  for (int i = threadIdx.x; i < W; i += blockDim.x) {
-    uint32_t v = bm[i];
-    bitmap[(int64_t)e * W + i] = v;
-    c += __popc(v);
+  for (int p = t0 * k + threadIdx.x; p < t1 * k; p += blockDim.x) {
+    const int t = p / k, e = idx[p];
+    if ((unsigned)e < (unsigned)E) atomicOr(&cbm[e * 8 + ((t - t0) >> 5)], 1u << (t & 31));
   }
-  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int s = 0;
-    for (int i = 0; i < kDThreads / 32; ++i) s += red[i];
-    counts[e] = s;
+  for (int i = threadIdx.x; i < E * 8; i += blockDim.x) {
+    const int e = i >> 3, j = i & 7;
+    if (j < nw) bitmap[(int64_t)e * W + w0 + j] = cbm[i];
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c += __popc(cbm[e * 8 + j]);
+    chunk_counts[(int64_t)ch * E + e] = c;
   }
 }
 
@@ -78,7 +78,10 @@ __device__ int block_exclusive_scan(int v, int* total, int* sh) {
 }
 
 // counts (if non-null) or offsets_in -> offsets_out, seg_start, tile list.
-__global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ counts,
+// The pair counts come from per-chunk counts (summed here and written to
+// counts_out), or from offsets_in.
+__global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ chunk_counts, int nch,
+                                                    int32_t* __restrict__ counts_out,
                                                     const int32_t* __restrict__ offsets_in, int E,
                                                     int32_t* __restrict__ offsets_out, int32_t* __restrict__ seg_start,
                                                     RowTile* __restrict__ tiles, int32_t* __restrict__ rt_base,
@@ -89,7 +92,14 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
   pdl_trigger();
   if (status && e == 0) *status = 0u;
   int c = 0;
-  if (e < E) c = counts ? counts[e] : (offsets_in[e + 1] - offsets_in[e]);
+  if (e < E) {
+    if (chunk_counts) {
+      for (int ch = 0; ch < nch; ++ch) c += chunk_counts[(int64_t)ch * E + e];
+      if (counts_out) counts_out[e] = c;
+    } else {
+      c = offsets_in[e + 1] - offsets_in[e];
+    }
+  }
   int tot;
   int off = block_exclusive_scan(c, &tot, sh);
   if (offsets_out) {
@@ -173,8 +183,8 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
   __syncthreads();
   const int P = T * k;
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    int t = p / k;
-    atomicOr(&sbm[idx[p] * W + (t >> 5)], 1u << (t & 31));
+    const int t = p / k, e = idx[p];
+    if ((unsigned)e < (unsigned)E) atomicOr(&sbm[e * W + (t >> 5)], 1u << (t & 31));
   }
   __syncthreads();
   const int e = threadIdx.x;
@@ -246,9 +256,12 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
                   pair_pos, seg_start, tiles, rt_base, status, tile_rows(c));
 }
 
-cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
-                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st, bool pdl) {
-  return launch_k(k_disp_bitmap, dim3(c.E), dim3(kDThreads), 0, st, pdl, idx, c.T, c.k, bitmap, counts);
+int dispatch_chunks(const moe_config& c) { return (c.T + kChunkTokens - 1) / kChunkTokens; }
+
+cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, uint32_t* bitmap, int32_t* chunk_counts,
+                            cudaStream_t st, bool pdl) {
+  return launch_k(k_disp_bitmap, dim3(dispatch_chunks(c)), dim3(kDThreads), (size_t)c.E * 8 * 4, st, pdl, idx, c.T,
+                  c.k, c.E, bitmap, chunk_counts);
 }
 
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
@@ -258,11 +271,11 @@ cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, con
                   pair_pos);
 }
 
-cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
-                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
-                             uint32_t* status, cudaStream_t st, bool pdl) {
-  return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, counts, offsets_in, c.E, offsets_out, seg_start, tiles,
-                  rt_base, status, tile_rows(c));
+cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, int32_t* counts_out,
+                             const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
+                             int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
+  return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, chunk_counts, dispatch_chunks(c), counts_out,
+                  offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status, tile_rows(c));
 }
 
 }  // namespace moe

@@ -56,14 +56,26 @@ void ws_layout(const moe_config& c, moe_ws_layout* L);
 // Launches after the first of an API call use programmatic dependent launch
 // (`pdl` = true): the kernel may start while its predecessor drains and waits
 // for it on the device.
+// Router: logits + top-k + weights.  `scratch` holds router_scratch_floats(c)
+// floats; `status` (nullable) is cleared by the router's first kernel.
 cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr,
-                          const float* bias, float* logits, int32_t* idx, float* w, cudaStream_t st, bool pdl);
-
+                          const float* bias, float* scratch, int32_t* idx, float* w, uint32_t* status,
+                          cudaStream_t st, bool pdl);
+size_t router_scratch_floats(const moe_config& c);
 int router_splits(const moe_config& c);
+// Prefill router (tensor-core logits, exact re-check of the candidates).
+bool router_uses_tc(const moe_config& c);
+size_t router_tc_scratch_floats(const moe_config& c);
+cudaError_t launch_router_tc(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr,
+                             const float* bias, float* scratch, int32_t* idx, float* w, uint32_t* status,
+                             cudaStream_t st, bool pdl);
+// 2D u8 tensor map [rows, row_bytes] with 128-byte swizzle, box 128 bytes x box_rows.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes, int box_rows);
 
-// bitmap [E, ceil(T/32)] and counts [E]
-cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
-                            int32_t* perm, int32_t* pair_pos, uint32_t* bitmap, cudaStream_t st, bool pdl);
+// bitmap [E, ceil(T/32)] and chunk_counts [dispatch_chunks(c), E]
+int dispatch_chunks(const moe_config& c);
+cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, uint32_t* bitmap, int32_t* chunk_counts,
+                            cudaStream_t st, bool pdl);
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
                                     const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st,
                                     bool pdl);
@@ -73,12 +85,13 @@ bool dispatch_fits_one_cta(const moe_config& c);
 cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
                                   int32_t* perm, int32_t* pair_pos, int32_t* seg_start, RowTile* tiles,
                                   int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl);
-// counts (or offsets_in when counts == nullptr) -> offsets_out (optional),
+// pair counts (the sum of chunk_counts, also written to counts_out; or from
+// offsets_in when chunk_counts == nullptr) -> offsets_out (optional),
 // seg_start [E+1], tiles, rt_base [E+1] (first row tile of each expert; the
 // total at E); zeroes *status when given
-cudaError_t launch_scan_plan(const moe_config& c, const int32_t* counts, const int32_t* offsets_in,
-                             int32_t* offsets_out, int32_t* seg_start, RowTile* tiles, int32_t* rt_base,
-                             uint32_t* status, cudaStream_t st, bool pdl);
+cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, int32_t* counts_out,
+                             const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
+                             int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl);
 
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx,
                            const int32_t* offsets, const int32_t* pair_pos, const int32_t* seg_start,

@@ -7,7 +7,9 @@
 // (exact in fp32) in chunks of 32 with plain fp32 adds, and the chunk sums are
 // added with Kahan compensation (within a K split and again across splits).
 // Hence |l_gpu - l| <= (gamma_31 + 3u) * sum_h |x_h w_eh| <= 40u * sum|x w|,
-// u = 2^-24, which the top-k parity check uses to certify near-ties.
+// u = 2^-24, which the top-k parity check uses to certify near-ties.  Decode
+// batches (T <= 256) use these kernels; larger batches the tensor-core router
+// with an exact re-check (moe_route_tc.cu).
 #include <mutex>
 
 #include "moe_common.cuh"
@@ -34,7 +36,7 @@ struct Kahan {
 template <int RM, int RN>
 __global__ void __launch_bounds__(256) k_router_logits(const __nv_bfloat16* __restrict__ x,
                                                        const __nv_bfloat16* __restrict__ wr, float* __restrict__ part,
-                                                       int T, int H, int E, int k_len) {
+                                                       int T, int H, int E, int k_len, uint32_t* status) {
   constexpr int TM = 16 * RM, TE = 16 * RN;
   extern __shared__ __align__(16) float router_smem[];
   float(*As)[TM][kKC + kPad] = reinterpret_cast<float(*)[TM][kKC + kPad]>(router_smem);
@@ -45,6 +47,7 @@ __global__ void __launch_bounds__(256) k_router_logits(const __nv_bfloat16* __re
   const int kbeg = split * k_len;
   const int nst = k_len / kKC;
   pdl_wait();
+  if (status && (blockIdx.x | blockIdx.y | blockIdx.z | threadIdx.x) == 0) *status = 0u;
 
   // register staging of one stage: rows x 8 uint4 (8 bf16 each)
   constexpr int A_VEC = TM * (kKC / 8), B_VEC = TE * (kKC / 8);
@@ -231,8 +234,13 @@ int router_splits(const moe_config& c) {
   return 1;
 }
 
+size_t router_scratch_floats(const moe_config& c) {
+  return router_uses_tc(c) ? router_tc_scratch_floats(c) : (size_t)router_splits(c) * c.T * c.E;
+}
+
 cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr, const float* bias,
-                          float* logits, int32_t* idx, float* w, cudaStream_t st, bool pdl) {
+                          float* logits, int32_t* idx, float* w, uint32_t* status, cudaStream_t st, bool pdl) {
+  if (router_uses_tc(c)) return launch_router_tc(c, x, wr, bias, logits, idx, w, status, st, pdl);
   const int ns = router_splits(c);
   const int k_len = c.H / ns;
   constexpr int smem = router_smem_bytes(4, 4);
@@ -243,7 +251,8 @@ cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __n
     attr = true;
   }
   dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, ns);
-  cudaError_t e = launch_k(k_router_logits<4, 4>, grid, dim3(256), smem, st, pdl, x, wr, logits, c.T, c.H, c.E, k_len);
+  cudaError_t e =
+      launch_k(k_router_logits<4, 4>, grid, dim3(256), smem, st, pdl, x, wr, logits, c.T, c.H, c.E, k_len, status);
   if (e != cudaSuccess) return e;
   return launch_k(k_router_topk, dim3(c.T), dim3((c.E + 31) / 32 * 32), 0, st, true, (const float*)logits, ns, bias,
                   c.T, c.E, c.k, c.bias_in_weights, c.routed_scale, idx, w);
@@ -255,13 +264,14 @@ cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __n
 // Some callers cannot allocate device memory at the point where they route
 // tokens: for example code running inside a captured CUDA graph region, a
 // plugin that has no access to its host framework's allocator, or a runtime
-// that forbids allocation after start-up.  For them the router's only scratch
-// (the fp32 logits partials) lives in a fixed array that the CUDA module
+// that forbids allocation after start-up.  For them the router's scratch (a
+// status word and the fp32 logits) lives in a fixed array that the CUDA module
 // reserves when the library is loaded, so the call itself allocates nothing.
 // ----------------------------------------------------------------------------
 namespace {
 
-constexpr size_t kNoAllocScratchFloats = (size_t)1 << 20;  // 4 MiB of logits partials
+constexpr size_t kNoAllocScratchFloats = (size_t)1 << 20;  // 4 MiB: status word area + router scratch
+constexpr size_t kNoAllocHeaderFloats = 64;
 static __device__ __align__(256) float g_route_scratch[kNoAllocScratchFloats];
 
 struct NoAllocDevice {
@@ -318,7 +328,8 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev
     if (!p) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MOE_ERR_MISALIGNED;
   }
-  const size_t need = (size_t)router_splits(*cfg) * (size_t)cfg->T * (size_t)cfg->E;
+  // the array holds a 256-byte status word area, then the router's scratch
+  const size_t need = kNoAllocHeaderFloats + router_scratch_floats(*cfg);
   if (need > kNoAllocScratchFloats) return MOE_ERR_WORKSPACE_TOO_SMALL;
   float* scratch = nullptr;
   s = noalloc_setup(&scratch);
@@ -326,6 +337,7 @@ extern "C" moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev
   // every logits partial the top-k kernel reads is written first by the
   // logits kernel of the same call, so nothing needs clearing
   cudaError_t e = launch_router(*cfg, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                                scratch, topk_idx_dev, topk_w_dev, (cudaStream_t)stream, false);
+                                scratch + kNoAllocHeaderFloats, topk_idx_dev, topk_w_dev,
+                                reinterpret_cast<uint32_t*>(scratch), (cudaStream_t)stream, false);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -128,7 +128,12 @@ MOE_API moe_status moe_workspace_size(const moe_config* cfg, size_t* bytes);
  *                s = sigmoid(x . w_e); ties go to the lower expert index.
  *   topk_w_dev   fp32 [T, k] (out): routed_scale * s_j / sum_i s_i.
  * Logits accumulate in fp32 in chunks of 32 products, the chunk sums
- * compensated (Kahan): |error| <= 40 * 2^-24 * sum_h |x_h w_eh|. */
+ * compensated (Kahan): |error| <= 40 * 2^-24 * sum_h |x_h w_eh|.  For T > 256
+ * (and E % 16 == 0) the logits are first computed on the tensor cores, and
+ * only the experts that can reach the top-k within 2^-11 ||x|| ||w_e|| of
+ * tensor-core rounding are recomputed with that bound; the selection and the
+ * weights use the recomputed logits.  The status word of the workspace is
+ * cleared, and set on a bounded-wait timeout (moe_poll_device_status). */
 MOE_API moe_status moe_route(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                      const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,
                      void* ws_dev, size_t ws_bytes, void* stream);
@@ -139,12 +144,14 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x_dev, const voi
  * allocation after start-up).  The pages have no counterpart: it is an
  * interface convenience, with the same arguments and results as moe_route
  * but no workspace.
- *   Its scratch (the fp32 logits partials) is a fixed 4 MiB array inside the
- *   library, reserved on every device that loads the library until the
- *   process exits.  Configurations whose partials do not fit return
- *   MOE_ERR_WORKSPACE_TOO_SMALL: splits * T * E <= 2^20 floats, where splits
- *   is the largest s <= 24 (T <= 64), <= 8 (T <= 256) or 1 (T > 256) with
- *   H % (64*s) == 0; e.g. every T <= 256 at E = 384, H = 4608.
+ *   Its scratch (a status word area and the fp32 logits) is a fixed 4 MiB
+ *   array inside the library, reserved on every device that loads the
+ *   library until the process exits.  Configurations whose scratch does not
+ *   fit return MOE_ERR_WORKSPACE_TOO_SMALL: 64 + splits * T * E <= 2^20
+ *   floats, where splits is the largest s <= 24 (T <= 64) or <= 8 (T <= 256)
+ *   with H % (64*s) == 0; for T > 256 with E % 16 == 0, 64 + T * E +
+ *   ceil(E/64)*64 <= 2^20 (e.g. T <= 2560 at E = 384); e.g. every T <= 256 at
+ *   E = 384, H = 4608.
  *   The first call on a device looks up the array's device address; make that
  *   first call before any stream capture.
  *   Every call uses the same array: calls that may overlap on the GPU (other
@@ -157,7 +164,9 @@ MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev, c
 /* Token dispatch [CB MegaMoE: dispatch is a step of the fused unit]: groups
  * the P = T*k pairs (t, j)
  * by expert, and within an expert by token.
- *   topk_idx_dev int32 [T, k]
+ *   topk_idx_dev int32 [T, k]: each row k distinct experts in [0, E), as
+ *                moe_route writes them (entries outside [0, E) are ignored,
+ *                and leave perm / pair_pos entries unwritten)
  *   counts_dev   int32 [E] (out)     pairs per expert
  *   offsets_dev  int32 [E+1] (out)   exclusive scan of counts
  *   perm_dev     int32 [P] (out)     perm[p] = t*k + j, sorted by (e, t)

@@ -125,10 +125,12 @@ def test_argument_validation_without_a_device():
 
 
 def test_forward_kernel_count():
-    # router 2 + dispatch (1 for decode batches, else 3) + x quant + GEMM1 + (NVFP4: h quant) + GEMM2 + combine
+    # router (2 for decode batches, 3 with tensor-core logits) + dispatch (1 for decode batches, else 3)
+    # + x quant + GEMM1 + h quant (unless GEMM1 quantises h) + GEMM2 + combine
     assert moe.moe_forward_kernel_count(cfg()) == 8
     assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=192)) == 7
-    assert moe.moe_forward_kernel_count(cfg(T=4096)) == 10
-    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=16384)) == 10
+    assert moe.moe_forward_kernel_count(cfg(T=4096)) == 11
+    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=16384)) == 11
+    assert moe.moe_forward_kernel_count(cfg(T=4096, E=376)) == 10  # E % 16 != 0: CUDA-core router
     with pytest.raises(moe.MoeError):
         moe.moe_forward_kernel_count(cfg(T=0))

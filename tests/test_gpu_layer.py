@@ -25,6 +25,10 @@ SMALL = {
     "multitile_mxfp8": dict(T=290, H=384, E=3, k=2, F=256, fmt="mxfp8", seed=15, **U),
     "k_eq_E_mxfp8": dict(T=5, H=256, E=4, k=4, F=128, fmt="mxfp8", seed=13, **U),
     "one_token_nvfp4": dict(T=1, H=512, E=16, k=4, F=256, fmt="nvfp4", seed=14, **U),
+    # T > 256: the tensor-core router; ragged token and expert tiles
+    "tc_router_nvfp4": dict(T=600, H=512, E=48, k=4, F=256, fmt="nvfp4", seed=16, **U),
+    "tc_router_mxfp8_outliers": dict(T=520, H=384, E=160, k=6, F=128, fmt="mxfp8", seed=17, outlier_frac=0.02,
+                                     bias="uniform"),
 }
 
 
@@ -131,7 +135,7 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
 @pytest.mark.parametrize("name", list(SMALL))
 def test_small_layer_all_tokens(name):
     gw = GpuWorkload(SMALL[name], torch)
-    st = check_layer(gw)
+    st = check_layer(gw, out_rowwise=gw.w["outlier_frac"] > 0)
     print(name, st)
 
 
@@ -142,8 +146,9 @@ def test_small_layer_uncapped_and_mx_round_up():
     print(check_layer(gw, cap=0.0))
 
 
-def test_staged_calls_equal_forward():
-    gw = GpuWorkload(SMALL["ragged_mxfp8"], torch)
+@pytest.mark.parametrize("name", ["ragged_mxfp8", "tc_router_nvfp4"])
+def test_staged_calls_equal_forward(name):
+    gw = GpuWorkload(SMALL[name], torch)
     ref = gw.forward().clone()
     c, T, k, E, H = gw.cfg, gw.w["T"], gw.w["k"], gw.w["E"], gw.w["H"]
     dev = "cuda"

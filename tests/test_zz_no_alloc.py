@@ -19,9 +19,12 @@ import block_scaled_fp4_route_gb300 as moe  # noqa: E402
 from synth.gpu_workload import GpuWorkload  # noqa: E402
 
 
-@pytest.mark.parametrize("name", ["decode64_nvfp4", "decode192_mxfp8_outliers", "tiny_mxfp8"])
+PREFILL2048 = dict(T=2048, H=4608, E=384, k=8, F=2304, fmt="nvfp4", seed=5, outlier_frac=0.0, bias="uniform")
+
+
+@pytest.mark.parametrize("name", ["decode64_nvfp4", "decode192_mxfp8_outliers", "tiny_mxfp8", "prefill2048"])
 def test_noalloc_router_matches_moe_route_twice(name):
-    gw = GpuWorkload(name, torch, with_weights=False)
+    gw = GpuWorkload(PREFILL2048 if name == "prefill2048" else name, torch, with_weights=False)
     T, k = gw.w["T"], gw.w["k"]
     ref_idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
     ref_w = torch.empty((T, k), dtype=torch.float32, device="cuda")

@@ -45,34 +45,23 @@ __device__ __forceinline__ float exp2i(int n) {  // 2^n, n in [-127, 127], exact
   return n >= -126 ? __uint_as_float((uint32_t)(n + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
-__device__ __forceinline__ uint32_t e2m1_encode(float v) {
-  uint32_t sign = (__float_as_uint(v) >> 31) << 3;
-  float a = fabsf(v);
-  uint32_t q;
-  if (a <= 0.25f) q = 0;        // midpoint 0.25 goes to code 0 (even)
-  else if (a < 0.75f) q = 1;    // 0.5
-  else if (a <= 1.25f) q = 2;   // 1.0 (0.75 and 1.25 are ties to code 2)
-  else if (a < 1.75f) q = 3;    // 1.5
-  else if (a <= 2.5f) q = 4;    // 2.0 (1.75, 2.5 ties to code 4)
-  else if (a < 3.5f) q = 5;     // 3.0
-  else if (a <= 5.0f) q = 6;    // 4.0 (3.5, 5 ties to code 6)
-  else q = 7;                   // 6.0, saturating (also NaN)
-  return sign | q;
+// E2M1 and E4M3 encoders: the hardware conversions (cvt.rn.satfinite):
+// round to nearest even, saturation to the largest finite (6 / 448), the sign
+// bit kept also for zero.  The pair forms put the first value in the low
+// nibble / byte.
+__device__ __forceinline__ uint32_t e2m1x2_encode(float lo, float hi) {
+  uint32_t r;
+  asm("{\n.reg .b8 t;\ncvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\ncvt.u32.u8 %0, t;\n}" : "=r"(r) : "f"(hi), "f"(lo));
+  return r & 0xFFu;
 }
+__device__ __forceinline__ uint32_t e2m1_encode(float v) { return e2m1x2_encode(v, 0.0f) & 0xFu; }
 
-// Written with selects only (no branches), so that unrolled callers can
-// interleave independent elements.
-__device__ __forceinline__ uint32_t e4m3_encode(float v) {
-  const uint32_t sign = (__float_as_uint(v) >> 24) & 0x80u;
-  const float a = fabsf(v);
-  // exponent of a, clamped below at -6: the subnormal range has the quantum
-  // 2^-9 of the smallest normal binade
-  const int e = max((int)(__float_as_uint(a) >> 23) - 127, -6);
-  const uint32_t m = __float2uint_rn(__fmul_rn(a, exp2i(3 - e)));  // normal: [8, 16]; subnormal: [0, 8]
-  const uint32_t up = m == 16u;                                     // rounded into the next binade
-  const uint32_t mag = m < 8u ? m : (((uint32_t)(e + 7) + up) << 3) | (up ? 0u : m - 8u);
-  return sign | (a < 448.0f ? mag : 0x7Eu);  // saturate (also NaN)
+__device__ __forceinline__ uint32_t e4m3x2_encode(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return (uint32_t)r;
 }
+__device__ __forceinline__ uint32_t e4m3_encode(float v) { return e4m3x2_encode(v, 0.0f) & 0xFFu; }
 
 // E2M1 code -> value {0, .5, 1, 1.5, 2, 3, 4, 6} with sign (exact).
 __device__ __forceinline__ float e2m1_value(uint32_t q) {

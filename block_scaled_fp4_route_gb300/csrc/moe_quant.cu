@@ -60,9 +60,10 @@ __device__ __forceinline__ uint32_t nvfp4_block(const float* v, float G, uint2* 
   if (sb != 0) {
     float inv = __fdiv_rn(G, e4m3_value(sb));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) lo |= e2m1_encode(__fmul_rn(v[i], inv)) << (4 * i);
+    for (int i = 0; i < 4; ++i) lo |= e2m1x2_encode(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv)) << (8 * i);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) hi |= e2m1_encode(__fmul_rn(v[8 + i], inv)) << (4 * i);
+    for (int i = 0; i < 4; ++i)
+      hi |= e2m1x2_encode(__fmul_rn(v[8 + 2 * i], inv), __fmul_rn(v[8 + 2 * i + 1], inv)) << (8 * i);
   }
   *codes_out = make_uint2(lo, hi);
   return sb;
@@ -79,7 +80,7 @@ __device__ __forceinline__ uint32_t mxfp8_block(const float* v, int mode, uint4*
     s = mx_scale_code(amax, mode);
     float mul = exp2i(127 - (int)s);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) w[i / 4] |= e4m3_encode(__fmul_rn(v[i], mul)) << (8 * (i % 4));
+    for (int i = 0; i < 16; ++i) w[i / 2] |= e4m3x2_encode(__fmul_rn(v[2 * i], mul), __fmul_rn(v[2 * i + 1], mul)) << (16 * (i % 2));
   }
   codes_out[0] = make_uint4(w[0], w[1], w[2], w[3]);
   codes_out[1] = make_uint4(w[4], w[5], w[6], w[7]);

@@ -140,8 +140,8 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   CUtensorMap mg, mu, md, mx, mh;
   if (!make_map(&mg, gate->codes, (int64_t)c.E * c.F, hb, 128) ||
       !make_map(&mu, up->codes, (int64_t)c.E * c.F, hb, 128) ||
-      !make_map(&md, down->codes, (int64_t)c.E * c.H, fb, 128) || !make_map(&mx, xq, R, hb, 16) ||
-      !make_map(&mh, hq, R, fb, 16))
+      !make_map(&md, down->codes, (int64_t)c.E * c.H, fb, 128) || !make_map(&mx, xq, R, hb, b_box_rows(c)) ||
+      !make_map(&mh, hq, R, fb, b_box_rows(c)))
     return MOE_ERR_CUDA;
 
   GemmLaunch g1{};
@@ -501,7 +501,7 @@ moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qweight* g
   const int64_t hb = code_bytes(c.fmt, c.H);
   CUtensorMap mg, mu, mx;
   if (!make_map(&mg, gate->codes, (int64_t)c.E * c.F, hb, 128) || !make_map(&mu, up->codes, (int64_t)c.E * c.F, hb, 128) ||
-      !make_map(&mx, at<uint8_t>(ws_dev, L.xq_codes), L.R, hb, 16))
+      !make_map(&mx, at<uint8_t>(ws_dev, L.xq_codes), L.R, hb, b_box_rows(*cfg)))
     return MOE_ERR_CUDA;
   GemmLaunch g1{};
   g1.cfg = &c;

@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
         const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
         const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
         const uint8_t* sfb = a.sfB + (int64_t)(rt.row / C::NT) * atoms_per_row * 512;
-        const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
+        const uint32_t bytes = C::NA * C::A_BYTES + (WIDE ? C::B_BYTES : N * 128) + (C::NA + 1) * C::SF_BYTES;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
             ok = false;
@@ -243,7 +243,11 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           tma_load_2d(sbase, &tmA0, &full[stage], kb * 128, arow);
           tma_load_2d(sbase + C::A_BYTES, &tmA1, &full[stage], kb * 128, arow1);
-          for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
+          if constexpr (WIDE) {  // the whole 128-row tile in one copy (box of 128 rows)
+            tma_load_2d(sB, &tmB, &full[stage], kb * 128, rt.row);
+          } else {  // 16-row boxes, only the rows the tile holds
+            for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
+          }
           bulk_load(sSF, sfa0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
           bulk_load(sSF + C::SF_BYTES, sfa1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
           bulk_load(sSF + C::NA * C::SF_BYTES, sfb + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);

@@ -37,6 +37,10 @@ inline int64_t code_bytes(moe_format f, int64_t K) { return f == MOE_FMT_NVFP4 ?
 inline int tile_rows(const moe_config& c) {
   return (int64_t)c.T * c.k >= (int64_t)64 * c.E ? kNTWide : kNTDecode;
 }
+// Rows of the token-operand TMA box: 16 for decode tiles (only the rows a
+// tile holds are loaded), the whole tile for 128-row tiles (one copy per
+// stage; a ragged tile reads rows of the next segment, which stay unused).
+inline int b_box_rows(const moe_config& c) { return tile_rows(c) == kNTWide ? kNTWide : 16; }
 // h goes through the bf16 buffer and a row-quantisation pass for NVFP4 (its
 // global scale spans the whole row) and for 128-row tiles; MXFP8 with 64-row
 // tiles quantises h in GEMM1's epilogue.

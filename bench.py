@@ -33,12 +33,20 @@ UNIT = "tokens/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
 
 
+# dense tensor-core peak per dtype relative to bf16 (nominal GB300 figures:
+# 2.25 PFLOP/s bf16, 4.5 fp8, 13.5 fp4)
+TENSOR_RATIO = {"nvfp4": 13.5 / 2.25, "mxfp8": 4.5 / 2.25}
+
+
 def peaks():
+    """HBM copy bandwidth and the sustained bf16 GEMM rate (the GEMMs are timed
+    inside a long step): measured on this GPU type, else the fallback."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return dict(hbm_gbs=d["hbm_gbs"], source="measured")
-    return dict(hbm_gbs=6800.0, source="fallback")
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1700.0, source="fallback")
 
 
 def kernel_source_sha() -> str:
@@ -52,17 +60,25 @@ def kernel_source_sha() -> str:
 # algorithmic bytes of one launch of each expert GEMM
 # ----------------------------------------------------------------------------
 
-def gemm_bytes(w: dict, n_touched: int):
+def gemm_bytes(w: dict, n_touched: int, h_quantised_in_gemm1: bool = False):
     """Algorithmic HBM bytes of GEMM1 (gate+up) and GEMM2 (down) per launch:
     the encoded weights of the touched experts (each read once), the encoded
-    activations read and the output written."""
+    activations read and the output written (GEMM1: bf16 h, or its MXFP8
+    codes and scales when the epilogue quantises h; GEMM2: fp32 y)."""
     H, F, P = w["H"], w["F"], w["T"] * w["k"]
     nv = w["fmt"] == "nvfp4"
     bpe = 0.5 + 1 / 16 if nv else 1 + 1 / 32          # bytes per element incl. block scales
     glob = 4 if nv else 0
-    g1 = n_touched * (2 * (F * H * bpe + glob)) + P * (H * bpe + glob) + P * F * 2
+    h_out = P * F * (bpe if h_quantised_in_gemm1 else 2)
+    g1 = n_touched * (2 * (F * H * bpe + glob)) + P * (H * bpe + glob) + h_out
     g2 = n_touched * (H * F * bpe + glob) + P * (F * bpe + glob) + P * H * 4
     return g1, g2
+
+
+def gemm_flops(w: dict):
+    """Useful flops of GEMM1 (gate and up: 2 x 2 H F per pair) and GEMM2 (2 H F per pair)."""
+    P = w["T"] * w["k"]
+    return 4.0 * P * w["H"] * w["F"], 2.0 * P * w["H"] * w["F"]
 
 
 # ----------------------------------------------------------------------------
@@ -329,24 +345,35 @@ def main():
 
     # ---- roofline of the dominant kernel (GEMM1: gate/up + SwiGLU) ----
     pk = peaks()
-    g1_bytes, g2_bytes = gemm_bytes(w, n_touched)
-    g1_ms = stage_ms["gemm1_gate_up_swiglu"]
+    g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"])
+    g1_flops, g2_flops = gemm_flops(w)
+    g1_ms, g2_ms = stage_ms["gemm1_gate_up_swiglu"], stage_ms["gemm2_down"]
     achieved = g1_bytes / (g1_ms / 1e3) / 1e9
+    tpeak = pk["bf16_tflops"] * TENSOR_RATIO[w["fmt"]]   # TFLOP/s, the dtype's dense peak
+    t1 = g1_flops / (g1_ms / 1e3) / 1e12
+    # the binding roof of GEMM1: tensor when its flops per byte exceed the machine balance
+    tensor_bound = g1_flops / g1_bytes > tpeak * 1e12 / (pk["hbm_gbs"] * 1e9)
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         tr = json.load(open(TRAFFIC_FILE))
         ent = tr.get(args.workload, {}).get("gemm1")
         if ent and tr.get("source_sha") == kernel_source_sha():
             traffic = ent
-    roofline = {"bound": "hbm", "kernel": "gemm1_gate_up_swiglu", "achieved": achieved, "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                "peak_source": pk["source"], "algorithmic_bytes": g1_bytes,
-                "gemm2": {"achieved": g2_bytes / (stage_ms["gemm2_down"] / 1e3) / 1e9,
-                          "frac": g2_bytes / (stage_ms["gemm2_down"] / 1e3) / 1e9 / pk["hbm_gbs"],
-                          "algorithmic_bytes": g2_bytes}}
+    hbm = {"achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+           "algorithmic_bytes": g1_bytes}
+    tensor = {"achieved": t1, "peak": tpeak, "unit": "TFLOP/s", "frac": t1 / tpeak, "flops": g1_flops,
+              "peak_note": f"sustained bf16 x {TENSOR_RATIO[w['fmt']]:g} ({w['fmt']} / bf16 nominal dense ratio)"}
+    main = tensor if tensor_bound else hbm
+    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": "gemm1_gate_up_swiglu",
+                "achieved": main["achieved"], "peak": main["peak"], "unit": main["unit"], "frac": main["frac"],
+                "traffic": traffic, "peak_source": pk["source"], "hbm": hbm, "tensor": tensor,
+                "gemm2": {"hbm_frac": g2_bytes / (g2_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                          "tensor_frac": g2_flops / (g2_ms / 1e3) / 1e12 / tpeak,
+                          "algorithmic_bytes": g2_bytes, "flops": g2_flops}}
     layer_bytes = g1_bytes + g2_bytes + w["E"] * w["H"] * 2 + T * w["H"] * 4
     layer = {"us_per_layer": ms_per_step * 1e3, "alg_bytes": layer_bytes,
              "hbm_frac_whole_layer": layer_bytes / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"],
+             "tensor_frac_whole_layer": (g1_flops + g2_flops) / (ms_per_step / 1e3) / 1e12 / tpeak,
              "stage_ms": stage_ms}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----

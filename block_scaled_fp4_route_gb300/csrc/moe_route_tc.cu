@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
 
   // ||x|| (upper bound)
   float ss = 0.0f;
+#pragma unroll 6
   for (int i = lane * 8; i < H; i += 256) {
     const uint4 u = *reinterpret_cast<const uint4*>(xr + i);
     const uint32_t v[4] = {u.x, u.y, u.z, u.w};
@@ -332,6 +333,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
   const float xn = sqrtf(ss) * kNormInflate;
 
   // approximate keys and their margins
+#pragma unroll 4
   for (int e = lane; e < E; e += 32) {
     const float a = __fadd_rn(router_sigmoid(lt[(int64_t)t * E + e]), bias[e]);
     const float m = 0.25f * kTcGamma * xn * wnorm[e] + kKeySlack;

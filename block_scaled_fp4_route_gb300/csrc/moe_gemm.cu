@@ -13,11 +13,10 @@
 // one or two tokens per expert wastes no weight bytes, and each pipeline
 // stage carries 32 KB of weights.
 //   GEMM1 (gated):  A0 = 128 W_gate rows, A1 = the same 128 W_up rows,
-//                   epilogue h = bf16(silu(cap g) * cap u); with 64-row
-//                   token tiles and MXFP8 the epilogue also quantises h (a
-//                   warp holds one 32-feature block of a token row); else
-//                   h goes to a row pass (NVFP4: its global spans the row;
-//                   128-row tiles: measured faster than the longer epilogue)
+//                   epilogue h = bf16(silu(cap g) * cap u); for MXFP8 the
+//                   epilogue also quantises h (a warp holds one 32-feature
+//                   block of a token row); NVFP4 h goes to a row pass (its
+//                   global spans the row)
 //   GEMM2:          A0, A1 = 256 consecutive W_down rows,
 //                   epilogue y = acc * g_w * g_h (fp32)
 // Tiles are walked expert by expert, then weight-row block, then token block,
@@ -466,15 +465,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
   }
 }
 
-template <int FMT, bool GATED, bool WIDE>
-cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  using C = Cfg<FMT, GATED, WIDE>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+GemmArgs gemm_args(const GemmLaunch& g) {
   GemmArgs a;
   a.sfA0 = g.sfA0;
   a.sfA1 = g.sfA1;
@@ -497,7 +488,372 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   a.status = g.status;
   a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock
   a.withhold_loads = g.withhold_loads;
+  return a;
+}
+
+template <int FMT, bool GATED, bool WIDE>
+cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  using C = Cfg<FMT, GATED, WIDE>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const GemmArgs a = gemm_args(g);
   return launch_k(k_moe_gemm<FMT, GATED, WIDE>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
+                  *g.tmB, a);
+}
+
+// ---------------------------------------------------------------------------
+// Wide tiles, token-major.  For prefill batches the token rows of an expert
+// fill the MMA's M = 128 and the tile's two 128-row weight blocks (gate and up
+// rows of the same 128 features, or 256 consecutive W_down rows) form one
+// N = 256 operand, so each k-step is one 128 x 256 MMA: the token operand is
+// read from shared memory once instead of once per weight block, half as many
+// MMAs are issued, and a thread of the epilogue (TMEM lane = token) holds the
+// gate and up values of the same features side by side.
+// ---------------------------------------------------------------------------
+template <int FMT, bool GATED>
+struct CfgTM {
+  static constexpr int NT = kNTWide;               // token rows per tile (MMA M)
+  static constexpr int ROWS = GATED ? 128 : 256;   // output features per tile
+  static constexpr int NB = 256;                   // weight rows per tile (MMA N)
+  static constexpr int EPI_WARPS = 8;              // two warps per TMEM lane quadrant
+  static constexpr int THREADS = (4 + EPI_WARPS) * 32;
+  static constexpr int STAGES = 4;
+  static constexpr int A_BYTES = NT * 128;         // tokens, 128 bytes of codes per row per stage
+  static constexpr int B_BYTES = NB * 128;         // weights
+  static constexpr int SF_ATOMS = FMT == MOE_FMT_NVFP4 ? 4 : 1;  // 512-byte atoms per 128 rows per stage
+  static constexpr int SF_BYTES = SF_ATOMS * 512;
+  static constexpr int RAW_STAGE = A_BYTES + B_BYTES + 3 * SF_BYTES;
+  static constexpr int STAGE_BYTES = (RAW_STAGE + 1023) / 1024 * 1024;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int RTB_BYTES = (kMaxE + 1) * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + RTB_BYTES + 1024;
+  static constexpr int ELEMS_PER_STAGE = FMT == MOE_FMT_NVFP4 ? 256 : 128;
+  static constexpr int BLOCK = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  static constexpr int ACC_COLS = NB;              // 128 lanes (tokens) x 256 columns (weight rows)
+  static constexpr int SFA_COLS = SF_ATOMS * 4;    // token scales
+  static constexpr int SFB_COLS = 2 * SF_ATOMS * 4;  // weight scales: per MMA, rows 128..255 four columns on
+  static constexpr int SF_COLS_STAGE = SFA_COLS + SFB_COLS;
+  static constexpr int TMEM_SF = ACC_COLS;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(TMEM_SF + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(16 * STAGES + 64 <= BAR_BYTES, "barrier area");
+};
+
+template <int FMT, bool GATED>
+__global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
+    k_moe_gemm_tm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                  const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+  using C = CfgTM<FMT, GATED>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tmem_full = empty + C::STAGES;
+  uint64_t* tmem_empty = tmem_full + 1;
+  uint64_t* drain = tmem_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_rtb = reinterpret_cast<int32_t*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tmem_full, 1);
+    mbar_init(tmem_empty, C::EPI_WARPS);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tmap(&tmA0);
+    prefetch_tmap(&tmA1);
+    prefetch_tmap(&tmB);
+  }
+  pdl_wait();
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = a.rt_base[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int MT = (a.NA + C::ROWS - 1) / C::ROWS;
+  const int total = s_rtb[a.E] * MT;
+  const int KB = a.K / C::ELEMS_PER_STAGE;
+  const int64_t atoms_per_row = (a.K / C::BLOCK) / 4;  // scale atoms per 128 rows over K
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      int mt = 0, rti = 0;
+      RowTile rt{};
+      if (blockIdx.x < total) {
+        map_tile(blockIdx.x, MT, s_rtb, a.E, mt, rti);
+        rt = a.tiles[rti];
+      }
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+        int mt_n = 0, rti_n = 0;
+        RowTile rt_n{};
+        if (t + (int)gridDim.x < total) {
+          map_tile(t + gridDim.x, MT, s_rtb, a.E, mt_n, rti_n);
+          rt_n = a.tiles[rti_n];
+        }
+        const int arow = rt.e * a.NA + mt * C::ROWS;
+        // down: the second block of the last tile lies past the expert when
+        // NA % 256 == 128; it then re-reads the first block and the epilogue
+        // drops its results
+        const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+        const int arow1 = (GATED || !second) ? arow : arow + 128;
+        const uint8_t* sfw0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
+        const uint8_t* sfw1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
+        const uint8_t* sft = a.sfB + (int64_t)(rt.row / C::NT) * atoms_per_row * 512;
+        constexpr uint32_t bytes = C::A_BYTES + C::B_BYTES + 3 * C::SF_BYTES;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sTok = smem + stage * C::STAGE_BYTES;
+          uint8_t* sW = sTok + C::A_BYTES;
+          uint8_t* sSF = sW + C::B_BYTES;  // token scales, weight block 0, weight block 1
+          if (a.withhold_loads) {  // bounded-wait self-test: nothing arrives
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
+          mbar_expect_tx(&full[stage], bytes);
+          armed |= 1u << stage;
+          armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+          tma_load_2d(sTok, &tmB, &full[stage], kb * 128, rt.row);
+          tma_load_2d(sW, &tmA0, &full[stage], kb * 128, arow);
+          tma_load_2d(sW + C::B_BYTES / 2, &tmA1, &full[stage], kb * 128, arow1);
+          bulk_load(sSF, sft + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          bulk_load(sSF + C::SF_BYTES, sfw0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          bulk_load(sSF + 2 * C::SF_BYTES, sfw1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        mt = mt_n;
+        rt = rt_n;
+      }
+      if (!ok) {
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (!((armed >> s) & 1u)) continue;
+          const uint32_t par = (armed_par >> s) & 1u;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&full[s], par) && clock64() - t0 < a.limit) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total; t += gridDim.x, ++it) {
+        if (!mbar_wait(tmem_empty, (it & 1) ^ 1, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, a.status, ST_TIMEOUT_MMA, a.limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint8_t* sTok = smem + stage * C::STAGE_BYTES;
+          uint8_t* sW = sTok + C::A_BYTES;
+          uint8_t* sSF = sW + C::B_BYTES;
+          const uint32_t sfa_t = tmem + C::TMEM_SF + stage * C::SF_COLS_STAGE;
+          const uint32_t sfb_t = sfa_t + C::SFA_COLS;
+#pragma unroll
+          for (int at = 0; at < C::SF_ATOMS; ++at) {
+            tc_cp_32x128b_x4(sfa_t + 4 * at, sdesc_atom(smem_u32(sSF + at * 512)));
+            tc_cp_32x128b_x4(sfb_t + 8 * at, sdesc_atom(smem_u32(sSF + C::SF_BYTES + at * 512)));
+            tc_cp_32x128b_x4(sfb_t + 8 * at + 4, sdesc_atom(smem_u32(sSF + 2 * C::SF_BYTES + at * 512)));
+          }
+          const uint64_t dA = sdesc_sw128(smem_u32(sTok));
+          const uint64_t dB = sdesc_sw128(smem_u32(sW));
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint32_t accum = (kb | s) != 0;
+            const uint64_t koff = (uint64_t)((s * 32) >> 4);
+            if constexpr (FMT == MOE_FMT_NVFP4) {
+              mma_nvfp4(tmem, dA + koff, dB + koff, idesc_nvfp4(C::NB), sfa_t + 4 * s, sfb_t + 8 * s, accum);
+            } else {
+              mma_mxfp8(tmem, dA + koff, dB + koff, idesc_mxfp8(C::NB, (uint32_t)s), sfa_t, sfb_t, accum);
+            }
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tmem_full);
+      }
+      tc_commit(drain);
+      const long long t0 = clock64();
+      while (!mbar_try_wait(drain, 0) && clock64() - t0 < a.limit) {
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue ----------------
+    // Warp (4 + i): TMEM lane quadrant i % 4 (tokens 32 (i % 4) + lane), and
+    // columns [64 (i / 4), +64) of each weight block: the share is copied to
+    // registers, TMEM is released, then the arithmetic and stores run.
+    const int q = warp & 3;
+    const int hc = (warp - 4) >> 2;
+    const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+    const int n = q * 32 + lane;  // token row within the tile
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      int mt, rti;
+      map_tile(t, MT, s_rtb, a.E, mt, rti);
+      const RowTile rt = a.tiles[rti];
+      const bool valid = n < rt.n_valid;
+      const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+      float sA0 = 1.0f, sA1 = 1.0f, gb = 1.0f;
+      if constexpr (FMT == MOE_FMT_NVFP4) {
+        sA0 = a.gA0[rt.e];
+        sA1 = a.gA1[rt.e];
+        if (valid) gb = a.gB[rt.row + n];
+      }
+      if (!mbar_wait(tmem_full, it & 1, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
+      tc_fence_after();
+      uint32_t r0[4][16], r1[4][16];
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        tmem_ld16(tq + 64 * hc + 16 * ch, r0[ch]);
+        tmem_ld16(tq + 128 + 64 * hc + 16 * ch, r1[ch]);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty);
+      if (!valid) continue;
+      const float s0 = sA0 * gb, s1 = sA1 * gb;
+      if constexpr (GATED) {
+        const bool capped = a.cap > 0.0f;
+        const int64_t row = (int64_t)rt.row + n;
+        const int f0 = mt * C::ROWS + 64 * hc;  // first feature of this thread's share
+        // two 32-feature blocks (one MXFP8 scale block each), one unrolled
+#pragma unroll 1
+        for (int b = 0; b < 2; ++b) {
+          uint32_t pk[16];  // 32 bf16 h values
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const int c = j >> 4, jj = j & 15;
+            float g0 = __uint_as_float(r0[c][jj]) * s0, g1 = __uint_as_float(r0[c][jj + 1]) * s0;
+            float u0 = __uint_as_float(r1[c][jj]) * s1, u1 = __uint_as_float(r1[c][jj + 1]) * s1;
+            if (capped) {
+              g0 = a.cap * tanh_soft(g0 * a.inv_cap);
+              g1 = a.cap * tanh_soft(g1 * a.inv_cap);
+              u0 = a.cap * tanh_soft(u0 * a.inv_cap);
+              u1 = a.cap * tanh_soft(u1 * a.inv_cap);
+            }
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(silu(g0) * u0, silu(g1) * u1);
+            pk[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+          }
+          const int f = f0 + 32 * b;
+          if constexpr (FMT == MOE_FMT_MXFP8) {
+            // the block's 32 features are this thread's: amax, E8M0 scale and
+            // E4M3 codes in registers
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              m = fmaxf(m, fmaxf(fabsf(__uint_as_float(pk[i] << 16)), fabsf(__uint_as_float(pk[i] & 0xFFFF0000u))));
+            uint32_t sc = 0, q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            if (m != 0.0f) {
+              sc = mx_scale_code(m, a.mx_mode);
+              const float mul = exp2i(127 - (int)sc);
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                q[i / 2] |= e4m3x2_encode(__fmul_rn(__uint_as_float(pk[i] << 16), mul),
+                                          __fmul_rn(__uint_as_float(pk[i] & 0xFFFF0000u), mul))
+                            << (16 * (i & 1));
+            }
+            uint4* dst = reinterpret_cast<uint4*>(a.hq_codes + row * a.NA + f);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            a.hq_scales[act_scale_offset(row, f >> 5, a.NA >> 5, C::NT)] = (uint8_t)sc;
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(a.h_out + row * a.NA + f);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          }
+          // the next block moves to the front (register moves, no indexing)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            r0[0][j] = r0[2][j];
+            r0[1][j] = r0[3][j];
+            r1[0][j] = r1[2][j];
+            r1[1][j] = r1[3][j];
+          }
+        }
+      } else {
+        float* yrow = a.y_out + ((int64_t)rt.canon + n) * a.NA + mt * C::ROWS + 64 * hc;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          float4* d0 = reinterpret_cast<float4*>(yrow + 16 * ch);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d0[i] = make_float4(__uint_as_float(r0[ch][4 * i]) * s0, __uint_as_float(r0[ch][4 * i + 1]) * s0,
+                                __uint_as_float(r0[ch][4 * i + 2]) * s0, __uint_as_float(r0[ch][4 * i + 3]) * s0);
+          if (second) {
+            float4* d1 = reinterpret_cast<float4*>(yrow + 128 + 16 * ch);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d1[i] = make_float4(__uint_as_float(r1[ch][4 * i]) * s1, __uint_as_float(r1[ch][4 * i + 1]) * s1,
+                                  __uint_as_float(r1[ch][4 * i + 2]) * s1, __uint_as_float(r1[ch][4 * i + 3]) * s1);
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  pdl_trigger();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int FMT, bool GATED>
+cudaError_t launch_tm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
+  using C = CfgTM<FMT, GATED>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm_tm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const GemmArgs a = gemm_args(g);
+  return launch_k(k_moe_gemm_tm<FMT, GATED>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
                   *g.tmB, a);
 }
 
@@ -505,11 +861,13 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   const bool wide = tile_rows(*g.cfg) == kNTWide;
+  // wide tiles: token-major for GEMM1; GEMM2 keeps the weight-major tile,
+  // whose epilogue writes each fp32 y row feature-contiguously across a warp
   if (g.cfg->fmt == MOE_FMT_NVFP4) {
-    if (wide) return g.gated ? launch_t<MOE_FMT_NVFP4, true, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, true>(g, st, pdl);
+    if (wide) return g.gated ? launch_tm<MOE_FMT_NVFP4, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, true>(g, st, pdl);
     return g.gated ? launch_t<MOE_FMT_NVFP4, true, false>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, false>(g, st, pdl);
   }
-  if (wide) return g.gated ? launch_t<MOE_FMT_MXFP8, true, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, true>(g, st, pdl);
+  if (wide) return g.gated ? launch_tm<MOE_FMT_MXFP8, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, true>(g, st, pdl);
   return g.gated ? launch_t<MOE_FMT_MXFP8, true, false>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, false>(g, st, pdl);
 }
 

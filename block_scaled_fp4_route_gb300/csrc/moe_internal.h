@@ -42,9 +42,8 @@ inline int tile_rows(const moe_config& c) {
 // stage; a ragged tile reads rows of the next segment, which stay unused).
 inline int b_box_rows(const moe_config& c) { return tile_rows(c) == kNTWide ? kNTWide : 16; }
 // h goes through the bf16 buffer and a row-quantisation pass for NVFP4 (its
-// global scale spans the whole row) and for 128-row tiles; MXFP8 with 64-row
-// tiles quantises h in GEMM1's epilogue.
-inline bool h_row_pass(const moe_config& c) { return c.fmt == MOE_FMT_NVFP4 || tile_rows(c) == kNTWide; }
+// global scale spans the whole row); MXFP8 h is quantised in GEMM1's epilogue.
+inline bool h_row_pass(const moe_config& c) { return c.fmt == MOE_FMT_NVFP4; }
 // Padded row capacity of the expert-grouped activation buffers.
 inline int64_t padded_rows(const moe_config& c) {
   const int64_t P = (int64_t)c.T * c.k, nt = tile_rows(c);

@@ -184,8 +184,7 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_d
  *   g,u = W_gate,e a , W_up,e a          (tcgen05 block-scaled MMA, fp32)
  *   h   = bf16( silu(cap g) * cap u )
  *   y_p = W_down,e quantise(h)           (NVFP4: per-row global over F;
- *                                         MXFP8, decode tiles: quantised in
- *                                         GEMM1's epilogue)
+ *                                         MXFP8: quantised in GEMM1's epilogue)
  *   x_dev        bf16 [T, H]
  *   topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev: from moe_route /
  *                moe_dispatch (the tile plan is rebuilt from offsets_dev)
@@ -290,7 +289,7 @@ MOE_API moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qw
  * NT-row tile and 4 scale columns: row r, column c at
  *   ((r/NT)*(C/4) + c/4)*512 + (r%NT%32)*16 + (r%NT/32)*4 + c%4.
  * h_bf16 is empty (sharing its offset with hq_codes) when GEMM1's epilogue
- * quantises h itself: MXFP8 with tile_rows 64. */
+ * quantises h itself: MXFP8. */
 typedef struct {
   int64_t R;
   int64_t tile_rows; /* token rows per expert tile: 64 (decode) or 128 */

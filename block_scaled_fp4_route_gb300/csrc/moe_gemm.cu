@@ -7,11 +7,16 @@
 // (kind::mxf4nvf4, E2M1 x E2M1 with UE4M3 scales per 16) and MXFP8
 // (kind::mxf8f6f4, E4M3 x E4M3 with UE8M0 scales per 32).
 //
-// A tile holds two 128-row weight blocks (two MMAs with M = 128 sharing the
-// token operand) x up to NT = 64 (decode) or 128 (prefill) token rows of one
-// expert (MMA N, rounded up to 16) x the full K, "swap-AB": the weights fill M so a decode batch with
-// one or two tokens per expert wastes no weight bytes, and each pipeline
-// stage carries 32 KB of weights.
+// Two tile shapes, both persistent and warp-specialised (warp 0 = TMA
+// producer, warp 1 = MMA issuer, warp 2 = TMEM allocator, the rest epilogue;
+// an epilogue warp w reads TMEM lane quadrant w % 4):
+//
+// Decode batches (64-row token tiles, k_moe_gemm), "swap-AB": two 128-row
+// weight blocks fill M (two MMAs sharing the token operand) and up to 64
+// token rows of one expert fill N (rounded up to 16), so a batch with one or
+// two tokens per expert wastes no weight bytes; each stage carries 32 KB of
+// weights; the TMEM accumulators are double-buffered (the epilogue of one
+// tile runs while the next accumulates).
 //   GEMM1 (gated):  A0 = 128 W_gate rows, A1 = the same 128 W_up rows,
 //                   epilogue h = bf16(silu(cap g) * cap u); for MXFP8 the
 //                   epilogue also quantises h (a warp holds one 32-feature
@@ -19,15 +24,13 @@
 //                   global spans the row)
 //   GEMM2:          A0, A1 = 256 consecutive W_down rows,
 //                   epilogue y = acc * g_w * g_h (fp32)
+//
+// Prefill batches (128-row token tiles, k_moe_gemm_tm), token-major: the 128
+// token rows fill M and the two weight blocks one N = 256 operand (see there).
+//
 // Tiles are walked expert by expert, then weight-row block, then token block,
 // so CTAs running side by side share an expert's weights and activations in
-// L2.  With NT = 64 the TMEM accumulator is double-buffered (the epilogue of
-// one tile runs while the next accumulates); with NT = 128 there is room for
-// one buffer only, so the epilogue copies its share to registers and frees
-// TMEM before the arithmetic.
-// Warp roles: warp 0 = TMA producer, warp 1 = MMA issuer, warp 2 = TMEM
-// allocator, warps 4..7 (and 8..11 when NT = 128) = epilogue; warp w reads
-// TMEM lane quadrant w % 4.
+// L2.
 // Every mbarrier wait is bounded; a wait that runs out sets a status bit in
 // global memory, every role leaves its loop, the producer waits for its own
 // copies in flight, the MMA thread for its tcgen05 operations, and the CTA
@@ -38,15 +41,15 @@ namespace moe {
 
 namespace {
 
-template <int FMT, bool GATED, bool WIDE>
+template <int FMT, bool GATED>
 struct Cfg {
   static constexpr int NA = 2;                              // weight blocks per tile
   static constexpr int ROWS = GATED ? 128 : 256;            // output features per tile
-  static constexpr int NT = WIDE ? kNTWide : kNTDecode;     // token rows per tile
-  static constexpr int ACC_BUFS = WIDE ? 1 : 2;             // TMEM accumulator buffers
-  static constexpr int EPI_WARPS = WIDE ? 8 : 4;            // two warps per TMEM lane quadrant when wide
+  static constexpr int NT = kNTDecode;                      // token rows per tile
+  static constexpr int ACC_BUFS = 2;                        // TMEM accumulator buffers
+  static constexpr int EPI_WARPS = 4;                       // one warp per TMEM lane quadrant
   static constexpr int THREADS = (4 + EPI_WARPS) * 32;
-  static constexpr int STAGES = WIDE ? 4 : (FMT == MOE_FMT_NVFP4 ? 4 : 5);
+  static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 4 : 5;
   static constexpr int A_BYTES = 128 * 128;
   static constexpr int B_BYTES = NT * 128;
   static constexpr int SF_ATOMS = FMT == MOE_FMT_NVFP4 ? 4 : 1;  // 512-byte atoms per operand per stage
@@ -136,11 +139,11 @@ __device__ __forceinline__ void map_tile(int t, int MT, const int32_t* rtb, int 
   rt = rtb[lo] + l % nrt;
 }
 
-template <int FMT, bool GATED, bool WIDE>
-__global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
+template <int FMT, bool GATED>
+__global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
-  using C = Cfg<FMT, GATED, WIDE>;
+  using C = Cfg<FMT, GATED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
         const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
         const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
         const uint8_t* sfb = a.sfB + (int64_t)(rt.row / C::NT) * atoms_per_row * 512;
-        const uint32_t bytes = C::NA * C::A_BYTES + (WIDE ? C::B_BYTES : N * 128) + (C::NA + 1) * C::SF_BYTES;
+        const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
             ok = false;
@@ -242,11 +245,8 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
           armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
           tma_load_2d(sbase, &tmA0, &full[stage], kb * 128, arow);
           tma_load_2d(sbase + C::A_BYTES, &tmA1, &full[stage], kb * 128, arow1);
-          if constexpr (WIDE) {  // the whole 128-row tile in one copy (box of 128 rows)
-            tma_load_2d(sB, &tmB, &full[stage], kb * 128, rt.row);
-          } else {  // 16-row boxes, only the rows the tile holds
-            for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
-          }
+          // 16-row boxes, only the rows the tile holds
+          for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
           bulk_load(sSF, sfa0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
           bulk_load(sSF + C::SF_BYTES, sfa1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
           bulk_load(sSF + C::NA * C::SF_BYTES, sfb + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
@@ -349,11 +349,12 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
     }
   } else if (warp >= 4) {
     // ---------------- epilogue ----------------
-    // Warp (4 + i) reads TMEM lane quadrant i % 4 (its 32 output features)
-    // for token columns [64 * (i / 4), +64): the whole share goes to
-    // registers first, TMEM is released, then the arithmetic and stores run.
+    // Warp (4 + i) reads TMEM lane quadrant i (its 32 output features) for
+    // the tile's up to 64 token columns: the whole share goes to registers
+    // first, the accumulator buffer is released, then the arithmetic and
+    // stores run.
     const int q = warp & 3;
-    const int col_lo = ((warp - 4) >> 2) * 64;
+    constexpr int col_lo = 0;
     const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -372,7 +373,10 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
       }
       const int buf = it % C::ACC_BUFS;
       const uint32_t use = (uint32_t)(it / C::ACC_BUFS) & 1u;
-      if (!mbar_wait(&tmem_full[buf], use, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
+      // the warp leaves together: tcgen05.ld and the shuffles below need all lanes
+      if (!__all_sync(0xffffffffu, mbar_wait(&tmem_full[buf], use, abort_flag, a.status, ST_TIMEOUT_EPILOGUE,
+                                             a.limit)))
+        break;
       tc_fence_after();
       const uint32_t tacc = tq + buf * C::ACC_BUF;
       // one 16-column chunk of the gated epilogue: h = bf16(silu(cap g) cap u),
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED, WIDE>::THREADS, 1)
           g = capped ? a.cap * tanh_soft(g * a.inv_cap) : g;
           u = capped ? a.cap * tanh_soft(u * a.inv_cap) : u;
           const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * u);
-          if constexpr (FMT == MOE_FMT_MXFP8 && !WIDE) {
+          if constexpr (FMT == MOE_FMT_MXFP8) {
             // the warp's 32 lanes are one 32-feature block of this token
             // row; |v| orders like its bit pattern
             const float v = __bfloat162float(hb);
@@ -491,17 +495,17 @@ GemmArgs gemm_args(const GemmLaunch& g) {
   return a;
 }
 
-template <int FMT, bool GATED, bool WIDE>
+template <int FMT, bool GATED>
 cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
-  using C = Cfg<FMT, GATED, WIDE>;
+  using C = Cfg<FMT, GATED>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const GemmArgs a = gemm_args(g);
-  return launch_k(k_moe_gemm<FMT, GATED, WIDE>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
+  return launch_k(k_moe_gemm<FMT, GATED>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
                   *g.tmB, a);
 }
 
@@ -514,6 +518,37 @@ cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
 // MMAs are issued, and a thread of the epilogue (TMEM lane = token) holds the
 // gate and up values of the same features side by side.
 // ---------------------------------------------------------------------------
+// 32 x 32 transpose across a warp, values v[0..15] = lo, v[16..31] = hi: on
+// entry lane L holds row L (v[j] = M[L][j]), on exit column L (v[i] = M[i][L]).
+// Five rounds; in the round of bit m, lanes L and L ^ m swap the elements
+// whose index bit m differs from their lane bit m.
+__device__ __forceinline__ void warp_transpose32(uint32_t (&lo)[16], uint32_t (&hi)[16], int lane) {
+#pragma unroll
+  for (int k = 4; k >= 0; --k) {
+    const int m = 1 << k;
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i & m) continue;
+      uint32_t& a = i < 16 ? lo[i & 15] : hi[i & 15];
+      uint32_t& b = (i | m) < 16 ? lo[(i | m) & 15] : hi[(i | m) & 15];
+      const uint32_t recv = __shfl_xor_sync(0xffffffffu, up ? a : b, m);
+      if (up) a = recv;
+      else b = recv;
+    }
+  }
+}
+
+// After warp_transpose32: row i of the 32-row group at base + i * stride,
+// lane L writing element L (128 contiguous bytes per instruction); rows at or
+// past nv are skipped (warp-uniform).
+__device__ __forceinline__ void store_rows32(float* base, int stride, int nv, const uint32_t (&lo)[16],
+                                             const uint32_t (&hi)[16]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < nv) base[(int64_t)i * stride] = __uint_as_float(i < 16 ? lo[i] : hi[i - 16]);
+}
+
 template <int FMT, bool GATED>
 struct CfgTM {
   static constexpr int NT = kNTWide;               // token rows per tile (MMA M)
@@ -743,7 +778,9 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
         sA1 = a.gA1[rt.e];
         if (valid) gb = a.gB[rt.row + n];
       }
-      if (!mbar_wait(tmem_full, it & 1, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)) break;
+      // the warp leaves together: tcgen05.ld and the shuffles below need all lanes
+      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full, it & 1, abort_flag, a.status, ST_TIMEOUT_EPILOGUE, a.limit)))
+        break;
       tc_fence_after();
       uint32_t r0[4][16], r1[4][16];
 #pragma unroll
@@ -755,9 +792,11 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
-      if (!valid) continue;
       const float s0 = sA0 * gb, s1 = sA1 * gb;
+      // every lane stays on the same path below (the down epilogue shuffles
+      // across the warp); lanes past n_valid only skip their stores
       if constexpr (GATED) {
+        if (!valid) continue;  // no warp-collective operation in the gated epilogue
         const bool capped = a.cap > 0.0f;
         const int64_t row = (int64_t)rt.row + n;
         const int f0 = mt * C::ROWS + 64 * hc;  // first feature of this thread's share
@@ -816,21 +855,27 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
           }
         }
       } else {
-        float* yrow = a.y_out + ((int64_t)rt.canon + n) * a.NA + mt * C::ROWS + 64 * hc;
+        // y rows are written feature-contiguously: each 32 x 32 (token x
+        // feature) group of the warp is transposed with xor shuffles, then
+        // lane L stores feature L of one token row per instruction
+        const int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile
+        float* ybase = a.y_out + ((int64_t)rt.canon + q * 32) * a.NA + mt * C::ROWS + 64 * hc + lane;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float4* d0 = reinterpret_cast<float4*>(yrow + 16 * ch);
+        for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d0[i] = make_float4(__uint_as_float(r0[ch][4 * i]) * s0, __uint_as_float(r0[ch][4 * i + 1]) * s0,
-                                __uint_as_float(r0[ch][4 * i + 2]) * s0, __uint_as_float(r0[ch][4 * i + 3]) * s0);
-          if (second) {
-            float4* d1 = reinterpret_cast<float4*>(yrow + 128 + 16 * ch);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d1[i] = make_float4(__uint_as_float(r1[ch][4 * i]) * s1, __uint_as_float(r1[ch][4 * i + 1]) * s1,
-                                  __uint_as_float(r1[ch][4 * i + 2]) * s1, __uint_as_float(r1[ch][4 * i + 3]) * s1);
+          for (int j = 0; j < 16; ++j) {
+            r0[ch][j] = __float_as_uint(__uint_as_float(r0[ch][j]) * s0);
+            r1[ch][j] = __float_as_uint(__uint_as_float(r1[ch][j]) * s1);
           }
+        warp_transpose32(r0[0], r0[1], lane);
+        warp_transpose32(r0[2], r0[3], lane);
+        store_rows32(ybase, a.NA, nv, r0[0], r0[1]);
+        store_rows32(ybase + 32, a.NA, nv, r0[2], r0[3]);
+        if (second) {
+          warp_transpose32(r1[0], r1[1], lane);
+          warp_transpose32(r1[2], r1[3], lane);
+          store_rows32(ybase + 128, a.NA, nv, r1[0], r1[1]);
+          store_rows32(ybase + 160, a.NA, nv, r1[2], r1[3]);
         }
       }
     }
@@ -861,14 +906,12 @@ cudaError_t launch_tm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
 
 cudaError_t launch_gemm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   const bool wide = tile_rows(*g.cfg) == kNTWide;
-  // wide tiles: token-major for GEMM1; GEMM2 keeps the weight-major tile,
-  // whose epilogue writes each fp32 y row feature-contiguously across a warp
   if (g.cfg->fmt == MOE_FMT_NVFP4) {
-    if (wide) return g.gated ? launch_tm<MOE_FMT_NVFP4, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, true>(g, st, pdl);
-    return g.gated ? launch_t<MOE_FMT_NVFP4, true, false>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false, false>(g, st, pdl);
+    if (wide) return g.gated ? launch_tm<MOE_FMT_NVFP4, true>(g, st, pdl) : launch_tm<MOE_FMT_NVFP4, false>(g, st, pdl);
+    return g.gated ? launch_t<MOE_FMT_NVFP4, true>(g, st, pdl) : launch_t<MOE_FMT_NVFP4, false>(g, st, pdl);
   }
-  if (wide) return g.gated ? launch_tm<MOE_FMT_MXFP8, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, true>(g, st, pdl);
-  return g.gated ? launch_t<MOE_FMT_MXFP8, true, false>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false, false>(g, st, pdl);
+  if (wide) return g.gated ? launch_tm<MOE_FMT_MXFP8, true>(g, st, pdl) : launch_tm<MOE_FMT_MXFP8, false>(g, st, pdl);
+  return g.gated ? launch_t<MOE_FMT_MXFP8, true>(g, st, pdl) : launch_t<MOE_FMT_MXFP8, false>(g, st, pdl);
 }
 
 }  // namespace moe

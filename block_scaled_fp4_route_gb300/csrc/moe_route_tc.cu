@@ -184,7 +184,8 @@ __global__ void __launch_bounds__(256, 1) k_router_tc(const __grid_constant__ CU
   } else if (warp >= 4) {
     const int q = warp & 3;
     const int t = t0 + q * 32 + lane;
-    if (mbar_wait(done, 0, abort_flag, status, ST_TIMEOUT_EPILOGUE, limit)) {
+    // the warp decides together: tcgen05.ld needs all lanes
+    if (__all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, status, ST_TIMEOUT_EPILOGUE, limit))) {
       tc_fence_after();
       for (int c = 0; c < N; c += 16) {
         uint32_t r[16];

@@ -152,22 +152,22 @@ __global__ void __launch_bounds__(256) k_router_logits(const __nv_bfloat16* __re
 constexpr int kMaxSplits = 24;
 
 // One CTA per token, one thread per expert: sum the K-split partials (Kahan,
-// fixed order), sigmoid, bias, then k rounds of a block-wide arg-max; ties in
-// the key go to the lower expert index.
+// fixed order; all loads of the token in flight at once), sigmoid, bias, into
+// shared memory; then warp 0 runs k rounds of a warp arg-max over them (ties
+// in the key go to the lower expert index) and normalises the weights over
+// the winners in selection order.
 __global__ void __launch_bounds__(1024) k_router_topk(const float* __restrict__ part, int nsplit,
                                                       const float* __restrict__ bias, int T, int E, int k,
                                                       int bias_in_weights, float routed_scale,
                                                       int32_t* __restrict__ idx, float* __restrict__ w) {
-  __shared__ float s_key[32];
-  __shared__ int s_e[32];
-  __shared__ int s_win[kMaxK];
-  __shared__ float s_num[kMaxK];
+  extern __shared__ float topk_smem[];  // key[E], sg[E]
+  float* key = topk_smem;
+  float* sgm = key + E;
   const int t = blockIdx.x;
   const int e = threadIdx.x;
-  const int lane = e & 31, warp = e >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31;
   pdl_wait();
   pdl_trigger();
-  float key = -INFINITY, sg = 0.0f;
   if (e < E) {
     float v[kMaxSplits];
 #pragma unroll
@@ -176,47 +176,45 @@ __global__ void __launch_bounds__(1024) k_router_topk(const float* __restrict__ 
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s)
       if (s < nsplit) l.add(v[s]);
-    sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l.s)));
-    key = __fadd_rn(sg, bias[e]);
-  }
-  bool taken = e >= E;
-  for (int j = 0; j < k; ++j) {
-    float bk = taken ? -INFINITY : key;
-    int be = taken ? 0x7fffffff : e;
-    for (int o = 16; o > 0; o >>= 1) {
-      float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-      int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ok > bk || (ok == bk && oe < be)) { bk = ok; be = oe; }
-    }
-    if (lane == 0) {
-      s_key[warp] = bk;
-      s_e[warp] = be;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      bk = lane < nw ? s_key[lane] : -INFINITY;
-      be = lane < nw ? s_e[lane] : 0x7fffffff;
-      for (int o = 16; o > 0; o >>= 1) {
-        float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-        int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ok > bk || (ok == bk && oe < be)) { bk = ok; be = oe; }
-      }
-      if (lane == 0) s_win[j] = be;
-    }
-    __syncthreads();
-    if (e == s_win[j]) {
-      taken = true;
-      s_num[j] = bias_in_weights ? key : sg;
-    }
+    const float sg = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-l.s)));
+    sgm[e] = sg;
+    key[e] = __fadd_rn(sg, bias[e]);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float den = 0.0f;
-    for (int j = 0; j < k; ++j) den = __fadd_rn(den, s_num[j]);
-    for (int j = 0; j < k; ++j) {
-      idx[(int64_t)t * k + j] = s_win[j];
-      w[(int64_t)t * k + j] = __fmul_rn(routed_scale, __fdiv_rn(s_num[j], den));
+  if (threadIdx.x >= 32) return;
+  float num = 0.0f;  // lane j keeps winner j's numerator
+  int win = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int i = lane; i < E; i += 32)
+      if (key[i] > bv) {  // ascending index: the first of equal keys stays
+        bv = key[i];
+        be = i;
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) {
+        bv = ov;
+        be = oe;
+      }
     }
+    if (be >= E) be = 0;  // only if every remaining key is NaN; stays in bounds
+    if (lane == j) {
+      win = be;
+      num = bias_in_weights ? key[be] : sgm[be];
+    }
+    __syncwarp();
+    if (lane == (be & 31)) key[be] = -INFINITY;
+    __syncwarp();
+  }
+  float den = 0.0f;
+  for (int j = 0; j < k; ++j) den = __fadd_rn(den, __shfl_sync(0xffffffffu, num, j));
+  if (lane < k) {
+    idx[(int64_t)t * k + lane] = win;
+    w[(int64_t)t * k + lane] = __fmul_rn(routed_scale, __fdiv_rn(num, den));
   }
 }
 
@@ -243,19 +241,29 @@ cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __n
   if (router_uses_tc(c)) return launch_router_tc(c, x, wr, bias, logits, idx, w, status, st, pdl);
   const int ns = router_splits(c);
   const int k_len = c.H / ns;
-  constexpr int smem = router_smem_bytes(4, 4);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         router_smem_bytes(4, 4));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_router_logits<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               router_smem_bytes(1, 4));
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  dim3 grid((c.E + 63) / 64, (c.T + 63) / 64, ns);
-  cudaError_t e =
-      launch_k(k_router_logits<4, 4>, grid, dim3(256), smem, st, pdl, x, wr, logits, c.T, c.H, c.E, k_len, status);
+  // token tiles of 16 rows for the smallest batches (a quarter of the FMAs
+  // of the 64-row tile; every logit's arithmetic is the same)
+  cudaError_t e;
+  if (c.T <= 16) {
+    e = launch_k(k_router_logits<1, 4>, dim3((c.E + 63) / 64, 1, ns), dim3(256), router_smem_bytes(1, 4), st, pdl, x,
+                 wr, logits, c.T, c.H, c.E, k_len, status);
+  } else {
+    e = launch_k(k_router_logits<4, 4>, dim3((c.E + 63) / 64, (c.T + 63) / 64, ns), dim3(256),
+                 router_smem_bytes(4, 4), st, pdl, x, wr, logits, c.T, c.H, c.E, k_len, status);
+  }
   if (e != cudaSuccess) return e;
-  return launch_k(k_router_topk, dim3(c.T), dim3((c.E + 31) / 32 * 32), 0, st, true, (const float*)logits, ns, bias,
-                  c.T, c.E, c.k, c.bias_in_weights, c.routed_scale, idx, w);
+  return launch_k(k_router_topk, dim3(c.T), dim3((c.E + 31) / 32 * 32), (size_t)2 * c.E * 4, st, true,
+                  (const float*)logits, ns, bias, c.T, c.E, c.k, c.bias_in_weights, c.routed_scale, idx, w);
 }
 
 // ----------------------------------------------------------------------------

@@ -57,6 +57,13 @@ WORKLOADS = {
                               outlier_frac=0.0, bias="uniform"),
     "prefill16384_mxfp8_zipf": dict(T=16384, H=4608, E=384, k=8, F=2304, fmt="mxfp8", seed=4,
                                     outlier_frac=0.0, bias="zipf"),
+    # single-user and small-batch decode (latency-bound: few experts, few tiles)
+    "decode1_nvfp4": dict(T=1, H=4608, E=384, k=8, F=2304, fmt="nvfp4", seed=31,
+                          outlier_frac=0.0, bias="uniform"),
+    "decode8_nvfp4": dict(T=8, H=4608, E=384, k=8, F=2304, fmt="nvfp4", seed=32,
+                          outlier_frac=0.0, bias="uniform"),
+    "decode32_mxfp8": dict(T=32, H=4608, E=384, k=8, F=2304, fmt="mxfp8", seed=33,
+                           outlier_frac=0.0, bias="uniform"),
     # smaller cases of the same kernels for detailed profiler captures (a few
     # GB resident, touched weights still far above the L2 size)
     "profile_decode16_nvfp4_e96": dict(T=16, H=4608, E=96, k=8, F=2304, fmt="nvfp4", seed=21,

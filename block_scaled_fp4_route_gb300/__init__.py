@@ -35,7 +35,7 @@ class MoeError(RuntimeError):
 class moe_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
                 ("F", ctypes.c_int), ("fmt", ctypes.c_int), ("swiglu_cap", ctypes.c_float),
-                ("mx_scale_mode", ctypes.c_int), ("bias_in_weights", ctypes.c_int),
+                ("act_global_mode", ctypes.c_int), ("mx_scale_mode", ctypes.c_int), ("bias_in_weights", ctypes.c_int),
                 ("routed_scale", ctypes.c_float)]
 
 
@@ -70,10 +70,10 @@ def lib():
             L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
             L.moe_route_noalloc.argtypes = [cfgp, P, P, P, P, P, P]
             L.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
-            L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, sz, P]
+            L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, P, sz, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
-            L.moe_forward.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, sz, P]
-            L.moe_forward_profiled.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, sz, P,
+            L.moe_forward.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, P, sz, P]
+            L.moe_forward_profiled.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, P, sz, P,
                                                ctypes.POINTER(ctypes.c_void_p)]
             L.moe_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64, i64, i64, ctypes.c_int,
                                        P, P, P, P]
@@ -114,10 +114,11 @@ def _stream(stream):
     return torch.cuda.current_stream().cuda_stream
 
 
-def make_config(T, H, E, k, F, fmt, swiglu_cap=10.0, mx_scale_mode=0, bias_in_weights=0, routed_scale=1.0):
+def make_config(T, H, E, k, F, fmt, swiglu_cap=10.0, mx_scale_mode=0, bias_in_weights=0, routed_scale=1.0,
+                act_global_mode=0):
     if isinstance(fmt, str):
         fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
-    return moe_config(T, H, E, k, F, fmt, swiglu_cap, mx_scale_mode, bias_in_weights, routed_scale)
+    return moe_config(T, H, E, k, F, fmt, swiglu_cap, act_global_mode, mx_scale_mode, bias_in_weights, routed_scale)
 
 
 def qweight(codes, scales, global_scale=None) -> moe_qweight:
@@ -165,11 +166,12 @@ def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None
                                               _stream(stream)))
 
 
-def moe_expert_ffn(cfg, x, topk_idx, offsets, perm, pair_pos, gate, up, down, y_perm, ws, stream=None):
+def moe_expert_ffn(cfg, x, topk_idx, offsets, perm, pair_pos, gate, up, down, y_perm, ws, stream=None,
+                   act_static_scales=None):
     _check("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(offsets),
                                                   _ptr(perm), _ptr(pair_pos), ctypes.byref(gate), ctypes.byref(up),
-                                                  ctypes.byref(down), _ptr(y_perm), _ptr(ws),
-                                                  ws.numel() * ws.element_size(), _stream(stream)))
+                                                  ctypes.byref(down), _ptr(act_static_scales), _ptr(y_perm),
+                                                  _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def moe_combine(cfg, y_perm, topk_w, pair_pos, out, stream=None):
@@ -177,22 +179,26 @@ def moe_combine(cfg, y_perm, topk_w, pair_pos, out, stream=None):
                                             _ptr(out), _stream(stream)))
 
 
-def moe_forward(cfg, x, w_router, bias, gate, up, down, out, ws, stream=None):
+def moe_forward(cfg, x, w_router, bias, gate, up, down, out, ws, stream=None, act_static_scales=None):
+    """act_static_scales: fp32 [E, 2] (g_x, g_h) on the device when cfg.act_global_mode == 1."""
     _check("moe_forward", lib().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias),
-                                            ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), _ptr(out),
-                                            _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+                                            ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down),
+                                            _ptr(act_static_scales), _ptr(out), _ptr(ws),
+                                            ws.numel() * ws.element_size(), _stream(stream)))
 
 
 NUM_STAGES = 7
 STAGE_NAMES = ["router", "dispatch", "quant_x", "gemm1_gate_up_swiglu", "quant_h", "gemm2_down", "combine"]
 
 
-def moe_forward_profiled(cfg, x, w_router, bias, gate, up, down, out, ws, events, stream=None):
+def moe_forward_profiled(cfg, x, w_router, bias, gate, up, down, out, ws, events, stream=None,
+                         act_static_scales=None):
     """events: NUM_STAGES + 1 torch.cuda.Event objects (created with timing)."""
     arr = (ctypes.c_void_p * (NUM_STAGES + 1))(*[e.cuda_event for e in events])
     _check("moe_forward_profiled", lib().moe_forward_profiled(
         ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), ctypes.byref(gate), ctypes.byref(up),
-        ctypes.byref(down), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream), arr))
+        ctypes.byref(down), _ptr(act_static_scales), _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+        _stream(stream), arr))
 
 
 def moe_quantize(fmt, src, codes, scales, global_scale=None, group_rows=0, layout=SCALES_TILED, mx_scale_mode=0,

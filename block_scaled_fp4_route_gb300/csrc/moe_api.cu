@@ -51,6 +51,16 @@ moe_status check_cfg(const moe_config* c) {
   if ((int64_t)c->T * c->k > (1 << 30)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!(c->swiglu_cap >= 0.0f)) return MOE_ERR_INVALID_ARG;
   if (c->mx_scale_mode != 0 && c->mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;
+  if (c->act_global_mode != 0 && c->act_global_mode != 1) return MOE_ERR_INVALID_ARG;
+  if (c->act_global_mode == 1 && c->fmt != MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;  // MXFP8 has no global
+  return MOE_OK;
+}
+
+// act_static_scales: required (4-byte aligned) in act_global_mode 1, else ignored.
+moe_status check_static(const moe_config* c, const float* act_static) {
+  if (c->act_global_mode != 1) return MOE_OK;
+  if (!act_static) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(act_static) & 3u) != 0) return MOE_ERR_MISALIGNED;
   return MOE_OK;
 }
 
@@ -116,7 +126,9 @@ void mark(cudaEvent_t* ev, int i, cudaStream_t st) {
 // GEMM2).
 moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
                     const int32_t* perm, const int32_t* pair_pos, const moe_qweight* gate, const moe_qweight* up,
-                    const moe_qweight* down, float* y, void* ws, cudaStream_t st, cudaEvent_t* ev = nullptr) {
+                    const moe_qweight* down, const float* act_static, float* y, void* ws, cudaStream_t st,
+                    cudaEvent_t* ev = nullptr) {
+  if (c.act_global_mode != 1) act_static = nullptr;
   moe_ws_layout L;
   ws_layout(c, &L);
   const int64_t R = L.R;
@@ -133,7 +145,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   uint32_t* status = at<uint32_t>(ws, L.status);
 
   mark(ev, 2, st);
-  cudaError_t e = launch_quant_x(c, x, idx, offsets, pair_pos, seg, xq, xs, xg, st, true);
+  cudaError_t e = launch_quant_x(c, x, idx, offsets, pair_pos, seg, xq, xs, xg, act_static, st, true);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   const int64_t hb = code_bytes(c.fmt, c.H), fb = code_bytes(c.fmt, c.F);
@@ -171,7 +183,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
 
   mark(ev, 4, st);
   if (h_row_pass(c) &&
-      launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, st, true) != cudaSuccess)
+      launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, act_static, st, true) != cudaSuccess)
     return MOE_ERR_CUDA;
 
   GemmLaunch g2{};
@@ -322,10 +334,12 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int3
 
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
                           const int32_t* offsets_dev, const int32_t* perm_dev, const int32_t* pair_pos_dev,
-                          const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down, float* y_perm_dev,
-                          void* ws_dev, size_t ws_bytes, void* stream) {
+                          const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down,
+                          const float* act_static_scales, float* y_perm_dev, void* ws_dev, size_t ws_bytes,
+                          void* stream) {
   moe_status s = check_cfg(cfg);
   if (s == MOE_OK) s = check_ptrs({x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, y_perm_dev});
+  if (s == MOE_OK) s = check_static(cfg, act_static_scales);
   if (s == MOE_OK) s = check_qw(cfg, gate);
   if (s == MOE_OK) s = check_qw(cfg, up);
   if (s == MOE_OK) s = check_qw(cfg, down);
@@ -341,7 +355,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_
                        at<uint32_t>(ws_dev, L.status), st, false) != cudaSuccess)
     return MOE_ERR_CUDA;
   return ffn_core(*cfg, sms, (const __nv_bfloat16*)x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, gate, up,
-                  down, y_perm_dev, ws_dev, st);
+                  down, act_static_scales, y_perm_dev, ws_dev, st);
 }
 
 moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const float* topk_w_dev,
@@ -356,10 +370,11 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const flo
 
 static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                                const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
-                               const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes, void* stream,
-                               cudaEvent_t* ev) {
+                               const moe_qweight* down, const float* act_static, void* out_dev, void* ws_dev,
+                               size_t ws_bytes, void* stream, cudaEvent_t* ev) {
   moe_status s = check_cfg(cfg);
   if (s == MOE_OK) s = check_ptrs({x_dev, w_router_dev, bias_dev, out_dev});
+  if (s == MOE_OK) s = check_static(cfg, act_static);
   if (s == MOE_OK) s = check_qw(cfg, gate);
   if (s == MOE_OK) s = check_qw(cfg, up);
   if (s == MOE_OK) s = check_qw(cfg, down);
@@ -388,7 +403,8 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   s = dispatch_impl(c, idx, counts, offsets, perm, pair_pos, ws_dev, nullptr, st, true);
   if (s != MOE_OK) return s;
   (void)bm;
-  s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, y, ws_dev, st, ev);
+  s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, act_static, y, ws_dev,
+               st, ev);
   if (s != MOE_OK) return s;
   mark(ev, 6, st);
   s = cuda_status(launch_combine(c, y, w, pair_pos, (__nv_bfloat16*)out_dev, st, true));
@@ -412,21 +428,23 @@ moe_status moe_forward_kernel_count(const moe_config* cfg, int* count) {
 }
 
 moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev, const float* bias_dev,
-                       const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down, void* out_dev,
-                       void* ws_dev, size_t ws_bytes, void* stream) {
-  return forward_impl(cfg, x_dev, w_router_dev, bias_dev, gate, up, down, out_dev, ws_dev, ws_bytes, stream, nullptr);
+                       const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down,
+                       const float* act_static_scales, void* out_dev, void* ws_dev, size_t ws_bytes, void* stream) {
+  return forward_impl(cfg, x_dev, w_router_dev, bias_dev, gate, up, down, act_static_scales, out_dev, ws_dev, ws_bytes,
+                      stream, nullptr);
 }
 
 moe_status moe_forward_profiled(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                                 const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
-                                const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes, void* stream,
-                                void* const* events) {
+                                const moe_qweight* down, const float* act_static_scales, void* out_dev,
+                                void* ws_dev, size_t ws_bytes, void* stream, void* const* events) {
   if (!events) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < MOE_NUM_STAGES + 1; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   cudaEvent_t ev[MOE_NUM_STAGES + 1];
   for (int i = 0; i < MOE_NUM_STAGES + 1; ++i) ev[i] = (cudaEvent_t)events[i];
-  return forward_impl(cfg, x_dev, w_router_dev, bias_dev, gate, up, down, out_dev, ws_dev, ws_bytes, stream, ev);
+  return forward_impl(cfg, x_dev, w_router_dev, bias_dev, gate, up, down, act_static_scales, out_dev, ws_dev, ws_bytes,
+                      stream, ev);
 }
 
 moe_status moe_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32, const void* src_dev, int64_t rows,

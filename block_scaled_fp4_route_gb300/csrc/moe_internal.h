@@ -96,13 +96,17 @@ cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, i
                              const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
                              int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl);
 
+// act_static: NVFP4 static activation globals fp32 [E, 2] (x, h) or nullptr
+// (dynamic per-row globals).
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx,
                            const int32_t* offsets, const int32_t* pair_pos, const int32_t* seg_start,
-                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st, bool pdl);
+                           uint8_t* codes, uint8_t* scales, float* glob, const float* act_static, cudaStream_t st,
+                           bool pdl);
 
 cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx,
                            const int32_t* offsets, const int32_t* perm, const int32_t* seg_start,
-                           uint8_t* codes, uint8_t* scales, float* glob, cudaStream_t st, bool pdl);
+                           uint8_t* codes, uint8_t* scales, float* glob, const float* act_static, cudaStream_t st,
+                           bool pdl);
 
 cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows,
                             int64_t cols, int64_t group_rows, moe_scale_layout layout, uint8_t* codes,

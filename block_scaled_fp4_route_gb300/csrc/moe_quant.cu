@@ -155,10 +155,12 @@ __device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst,
 // the codes.  Rows of up to kRowRounds * kQThreads blocks (16384 elements).
 constexpr int kRowRounds = 2;
 
+// sg (NVFP4, static activation globals): the decode factor of each
+// destination (its expert's); nullptr = dynamic, from the row maximum.
 template <int FMT>
 __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
-                                               const int64_t* dst, uint8_t* codes, uint8_t* scales, float* glob,
-                                               float* red, int nt) {
+                                               const int64_t* dst, const float* sg, uint8_t* codes, uint8_t* scales,
+                                               float* glob, float* red, int nt) {
   constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   const int nb = K / BS;
   const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
@@ -176,6 +178,23 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
   }
   float G = 1.0f;
   if constexpr (FMT == MOE_FMT_NVFP4) {
+    if (sg) {  // static: each destination encodes with its own expert's global
+      if (threadIdx.x < ndst) glob[dst[threadIdx.x]] = sg[threadIdx.x];
+      for (int d = 0; d < ndst; ++d) {
+        const float Gd = __fdiv_rn(1.0f, sg[d]);
+        const int64_t rr = dst[d];
+#pragma unroll
+        for (int r = 0; r < kRowRounds; ++r) {
+          const int b = threadIdx.x + r * blockDim.x;
+          if (b >= nb) continue;
+          uint2 c;
+          const uint32_t sc = nvfp4_block(v[r], Gd, &c);
+          *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
+          scales[act_scale_offset(rr, b, C, nt)] = (uint8_t)sc;
+        }
+      }
+      return;
+    }
     G = nvfp4_G(block_max(m, red));
     if (threadIdx.x < ndst) glob[dst[threadIdx.x]] = __fdiv_rn(1.0f, G);
   }
@@ -212,9 +231,10 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ pair_pos,
                                                        const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                       uint8_t* scales, float* glob, int nt) {
+                                                       uint8_t* scales, float* glob, const float* act_static, int nt) {
   __shared__ float red[32];
   __shared__ int64_t dst[kMaxK];
+  __shared__ float sg[kMaxK];
   const int t = blockIdx.x;
   pdl_wait();
   pdl_trigger();
@@ -222,9 +242,10 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
     const int pid = t * k + threadIdx.x;
     const int e = idx[pid];
     dst[threadIdx.x] = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
+    if (act_static) sg[threadIdx.x] = act_static[2 * e];
   }
   __syncthreads();
-  quant_row_regs<FMT>(x + (int64_t)t * H, H, mx_mode, k, dst, codes, scales, glob, red, nt);
+  quant_row_regs<FMT>(x + (int64_t)t * H, H, mx_mode, k, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
 }
 
 // h: one CTA per canonical pair position p; row = its padded row.
@@ -234,65 +255,85 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ perm,
                                                        const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                       uint8_t* scales, float* glob, int nt) {
+                                                       uint8_t* scales, float* glob, const float* act_static, int nt) {
   __shared__ float red[32];
   __shared__ int64_t dst[1];
+  __shared__ float sg[1];
   const int p = blockIdx.x;
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x == 0) {
     const int e = idx[perm[p]];
     dst[0] = (int64_t)seg_start[e] + (p - offsets[e]);
+    if (act_static) sg[0] = act_static[2 * e + 1];
   }
   __syncthreads();
-  quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, codes, scales, glob, red, nt);
+  quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
 }
 
 // Many short rows (prefill): one warp per row, eight rows per CTA.  Pass 1
-// finds the row maximum (NVFP4 only), pass 2 re-reads the row (now in L1)
-// block by block.  dst_lane: lane d < ndst holds destination row d.
+// finds the row maximum (NVFP4, dynamic globals only), pass 2 re-reads the row
+// (now in L1) block by block.  Every lane runs every iteration (lanes past the
+// last block only skip their loads and stores), so the shuffles see the whole
+// warp.  dst_lane: lane d < ndst holds destination row d; sg_lane (NVFP4,
+// static globals) its decode factor, else 0.
 template <int FMT>
 __device__ __forceinline__ void quant_row_warp(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
-                                               int64_t dst_lane, uint8_t* codes, uint8_t* scales, float* glob, int nt) {
+                                               int64_t dst_lane, float sg_lane, bool is_static, uint8_t* codes,
+                                               uint8_t* scales, float* glob, int nt) {
   constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
   const int lane = threadIdx.x & 31;
   const int nb = K / BS;
   const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
   float G = 1.0f;
   if constexpr (FMT == MOE_FMT_NVFP4) {
-    float m = 0.0f;
-    const uint4* q = reinterpret_cast<const uint4*>(row);
-    for (int i = lane; i < K / 8; i += 32) {
-      uint4 u = q[i];
-      uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    if (is_static) {
+      if (lane < ndst) glob[dst_lane] = sg_lane;
+    } else {
+      float m = 0.0f;
+      const uint4* q = reinterpret_cast<const uint4*>(row);
+      for (int i = lane; i < K / 8; i += 32) {
+        uint4 u = q[i];
+        uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+        for (int j = 0; j < 4; ++j)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+      }
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      G = nvfp4_G(m);
+      if (lane < ndst) glob[dst_lane] = __fdiv_rn(1.0f, G);
     }
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    G = nvfp4_G(m);
-    if (lane < ndst) glob[dst_lane] = __fdiv_rn(1.0f, G);
   }
-  for (int b = lane; b < nb; b += 32) {
+  for (int b0 = 0; b0 < nb; b0 += 32) {
+    const int b = b0 + lane;
+    const bool in = b < nb;
     float v[BS];
-    load_block_bf16(row + (int64_t)b * BS, BS, v);
+    if (in) load_block_bf16(row + (int64_t)b * BS, BS, v);
+    else
+#pragma unroll
+      for (int i = 0; i < BS; ++i) v[i] = 0.0f;
     if constexpr (FMT == MOE_FMT_NVFP4) {
       uint2 c;
-      const uint32_t sc = nvfp4_block(v, G, &c);
+      uint32_t sc = is_static ? 0u : nvfp4_block(v, G, &c);
       for (int d = 0; d < ndst; ++d) {
         const int64_t rr = __shfl_sync(0xffffffffu, dst_lane, d);
-        *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
-        scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
+        if (is_static) sc = nvfp4_block(v, __fdiv_rn(1.0f, __shfl_sync(0xffffffffu, sg_lane, d)), &c);
+        if (in) {
+          *reinterpret_cast<uint2*>(codes + rr * cbytes + (int64_t)b * 8) = c;
+          scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
+        }
       }
     } else {
       uint4 c[2];
       const uint32_t sc = mxfp8_block(v, mx_mode, c);
       for (int d = 0; d < ndst; ++d) {
         const int64_t rr = __shfl_sync(0xffffffffu, dst_lane, d);
-        uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
-        o[0] = c[0];
-        o[1] = c[1];
-        scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
+        if (in) {
+          uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
+          o[0] = c[0];
+          o[1] = c[1];
+          scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
+        }
       }
     }
   }
@@ -306,18 +347,21 @@ __global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __
                                                          const int32_t* __restrict__ pair_pos,
                                                          const int32_t* __restrict__ perm,
                                                          const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                         uint8_t* scales, float* glob, int nt) {
+                                                         uint8_t* scales, float* glob, const float* act_static,
+                                                         int nt) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_wait();
   pdl_trigger();
-  if (r >= rows) return;
+  if (r >= rows) return;  // whole warp
   int64_t dst = 0;
+  float sg = 0.0f;
   const __nv_bfloat16* row;
   int ndst;
   if (is_h) {
     const int e = idx[perm[r]];
     dst = (int64_t)seg_start[e] + (r - offsets[e]);
+    if (act_static) sg = act_static[2 * e + 1];
     row = src + dst * K;
     ndst = 1;
   } else {
@@ -325,11 +369,12 @@ __global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __
       const int pid = r * k + lane;
       const int e = idx[pid];
       dst = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
+      if (act_static) sg = act_static[2 * e];
     }
     row = src + (int64_t)r * K;
     ndst = k;
   }
-  quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, codes, scales, glob, nt);
+  quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, sg, act_static != nullptr, codes, scales, glob, nt);
 }
 
 constexpr int kWarpRowsFrom = 2048;  // rows from which one warp per row is used
@@ -449,29 +494,29 @@ int grid_1d(int64_t n, int threads) {
 
 cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
                            const int32_t* pair_pos, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
-                           float* glob, cudaStream_t st, bool pdl) {
+                           float* glob, const float* act_static, cudaStream_t st, bool pdl) {
   if (c.T >= kWarpRowsFrom) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((c.T + 7) / 8), dim3(256), 0, st, pdl, x, c.T, c.H, c.k, 0, c.mx_scale_mode, idx, offsets,
-                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob, tile_rows(c));
+                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob, act_static, tile_rows(c));
   }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_x<MOE_FMT_NVFP4> : k_quant_x<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(c.T), dim3(kQThreads), 0, st, pdl, x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
-                  seg_start, codes, scales, glob, tile_rows(c));
+                  seg_start, codes, scales, glob, act_static, tile_rows(c));
 }
 
 cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx, const int32_t* offsets,
                            const int32_t* perm, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
-                           float* glob, cudaStream_t st, bool pdl) {
+                           float* glob, const float* act_static, cudaStream_t st, bool pdl) {
   int P = c.T * c.k;
   if (P >= kWarpRowsFrom) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((P + 7) / 8), dim3(256), 0, st, pdl, h, P, c.F, c.k, 1, c.mx_scale_mode, idx, offsets,
-                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob, tile_rows(c));
+                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob, act_static, tile_rows(c));
   }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_h<MOE_FMT_NVFP4> : k_quant_h<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(P), dim3(kQThreads), 0, st, pdl, h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
-                  codes, scales, glob, tile_rows(c));
+                  codes, scales, glob, act_static, tile_rows(c));
 }
 
 cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,

@@ -85,6 +85,15 @@ typedef enum { MOE_SCALES_ROWMAJOR = 0, MOE_SCALES_TILED = 1 } moe_scale_layout;
  *     pre-activations; 0 disables the cap.  Default 10.  [TS MoE row and MI 1
  *     call the activation a capped / soft-capped SwiGLU but give neither the
  *     form nor the constant, so both are this parameter.]
+ *   act_global_mode: NVFP4 only.  The FP32 global scale of the activations
+ *     (x and h rows): 0 = dynamic, from each row's absolute maximum over its
+ *     full width (default; G = 2688 / amax, decode factor g = 1/G); 1 =
+ *     static per expert: the caller passes decode factors g_x[e], g_h[e]
+ *     (act_static_scales of moe_expert_ffn / moe_forward) and a row routed to
+ *     expert e is encoded with G = 1/g (fp32), block maxima beyond 2688 g
+ *     saturating.  [CB Parallelism paragraph: the activation scales must
+ *     cover an expert's full input width; the pages fix no granularity, so
+ *     both readings are offered.]  MXFP8 requires 0.
  *   mx_scale_mode: MXFP8 only.  0 = OCP rule X = 2^(floor(log2 amax) - 8)
  *     (default; block maxima in (448, 512)*X saturate); 1 = X =
  *     2^ceil(log2(amax/448)) (never saturates).
@@ -96,6 +105,7 @@ typedef struct {
   int T, H, E, k, F;
   moe_format fmt;
   float swiglu_cap;
+  int act_global_mode;
   int mx_scale_mode;
   int bias_in_weights;
   float routed_scale;
@@ -180,7 +190,8 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_d
  * GEMMs and the capped SwiGLU between them; TS: the expert GEMMs run on
  * block-scaled tensor cores; SGL kernel-fusion bullet: activation
  * quantisation lives inside the expert GEMMs; MI 5.3: W4A4 / W8A8]:
- *   a   = quantise(x_t) per token over the full H (NVFP4: per-row global)
+ *   a   = quantise(x_t) per token over the full H (NVFP4: per-row global,
+ *         or expert e's static global in act_global_mode 1)
  *   g,u = W_gate,e a , W_up,e a          (tcgen05 block-scaled MMA, fp32)
  *   h   = bf16( silu(cap g) * cap u )
  *   y_p = W_down,e quantise(h)           (NVFP4: per-row global over F;
@@ -189,11 +200,14 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_d
  *   topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev: from moe_route /
  *                moe_dispatch (the tile plan is rebuilt from offsets_dev)
  *   gate/up/down quantised weights (see moe_qweight)
+ *   act_static_scales fp32 [E, 2] (g_x[e], g_h[e]) when act_global_mode = 1,
+ *                else NULL (ignored)
  *   y_perm_dev   fp32 [P, H] (out), row p = perm order. */
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
                           const int32_t* offsets_dev, const int32_t* perm_dev,
                           const int32_t* pair_pos_dev, const moe_qweight* gate,
-                          const moe_qweight* up, const moe_qweight* down, float* y_perm_dev,
+                          const moe_qweight* up, const moe_qweight* down,
+                          const float* act_static_scales, float* y_perm_dev,
                           void* ws_dev, size_t ws_bytes, void* stream);
 
 /* Weighted combine [CB MegaMoE: the combine ends the fused unit]:
@@ -207,11 +221,12 @@ MOE_API moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, c
 /* The whole layer in one call: moe_route, moe_dispatch, moe_expert_ffn and
  * moe_combine chained on `stream` with every intermediate in the workspace
  * [CB MegaMoE: one fused unit per layer; SGL: programmatic dependent
- * launch between kernels].  out_dev bf16 [T, H]. */
+ * launch between kernels].  act_static_scales as for moe_expert_ffn.
+ * out_dev bf16 [T, H]. */
 MOE_API moe_status moe_forward(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                        const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
-                       const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes,
-                       void* stream);
+                       const moe_qweight* down, const float* act_static_scales, void* out_dev,
+                       void* ws_dev, size_t ws_bytes, void* stream);
 
 /* Number of kernels one moe_forward call launches for this configuration
  * (2 router + 1 or 3 dispatch + x quantisation + GEMM1 + h quantisation
@@ -230,8 +245,8 @@ MOE_API moe_status moe_forward_kernel_count(const moe_config* cfg, int* count);
 #define MOE_NUM_STAGES 7
 MOE_API moe_status moe_forward_profiled(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                                         const float* bias_dev, const moe_qweight* gate, const moe_qweight* up,
-                                        const moe_qweight* down, void* out_dev, void* ws_dev, size_t ws_bytes,
-                                        void* stream, void* const* events);
+                                        const moe_qweight* down, const float* act_static_scales, void* out_dev,
+                                        void* ws_dev, size_t ws_bytes, void* stream, void* const* events);
 
 /* Block quantiser [MI 1 and 5.2: weight sync re-encodes experts in the layer's
  * format and recomputes NVFP4 global scales].  Encodes rows x cols values.

@@ -63,7 +63,8 @@ def lib():
             L.orc_router_logits.argtypes = [i64, i64, i64, P, P, P, P]
             L.orc_router_select.argtypes = [i64, i64, i64, P, P, c_int, d, P, P, P]
             L.orc_dispatch.argtypes = [i64, i64, i64, P, P, P, P, P]
-            L.orc_expert_ffn.argtypes = [c_int, i64, i64, d, c_int, c_int, P, P, P, i64, P, P, P, P, P, P]
+            L.orc_expert_ffn.argtypes = [c_int, i64, i64, d, c_int, c_int, P, P, P, i64, P, P, P, P, P, P, P]
+            L.orc_nvfp4_quantize_static.argtypes = [P, i64, i64, P, P, P, P]
             L.orc_combine.argtypes = [i64, i64, i64, P, P, P, P]
             L.orc_num_threads.restype = c_int
             _lib = L
@@ -131,6 +132,20 @@ def nvfp4_quantize(v: np.ndarray, per_tensor: bool = False):
     sf = np.empty((rows, K // 16), np.uint8)
     g = np.empty(1 if per_tensor else rows, np.float32)
     lib().orc_nvfp4_quantize(_p(v), rows, K, int(per_tensor), _p(codes), _p(sf), _p(g))
+    return codes, sf, g
+
+
+def nvfp4_quantize_static(v: np.ndarray, g_rows):
+    """Rows of v with given decode factors g_rows (static activation globals:
+    G = 1/g in fp32, block maxima beyond 2688 g saturate)."""
+    v = _c(v, np.float32)
+    rows, K = v.shape
+    assert K % 16 == 0
+    g_rows = _c(np.broadcast_to(np.asarray(g_rows, np.float32), (rows,)), np.float32)
+    codes = np.empty((rows, K // 2), np.uint8)
+    sf = np.empty((rows, K // 16), np.uint8)
+    g = np.empty(rows, np.float32)
+    lib().orc_nvfp4_quantize_static(_p(v), rows, K, _p(g_rows), _p(codes), _p(sf), _p(g))
     return codes, sf, g
 
 
@@ -219,8 +234,10 @@ def dispatch(idx: np.ndarray, E: int):
     return dict(counts=counts, offsets=offsets, perm=perm, pair_pos=pair_pos)
 
 
-def expert_ffn(fmt: str, Wg, Wu, Wd, a, cap: float = 10.0, h_round_bf16: bool = True, mx_mode: int = 0):
+def expert_ffn(fmt: str, Wg, Wu, Wd, a, cap: float = 10.0, h_round_bf16: bool = True, mx_mode: int = 0,
+               h_static_g=None):
     """One expert over n pairs.  Wg, Wu [F,H], Wd [H,F], a [n,H] fp64 decoded.
+    h_static_g: NVFP4 static h global of this expert (act_global_mode 1), or None.
     Returns y [n,H] fp64, h_bf16 [n,F], and h's codes / scales / globals."""
     Wg, Wu, Wd, a = (_c(m, np.float64) for m in (Wg, Wu, Wd, a))
     F, H = Wg.shape
@@ -231,8 +248,9 @@ def expert_ffn(fmt: str, Wg, Wu, Wd, a, cap: float = 10.0, h_round_bf16: bool = 
     hq_codes = np.empty((n, F // 2 if f == FMT_NVFP4 else F), np.uint8)
     hq_sf = np.empty((n, F // 16 if f == FMT_NVFP4 else F // 32), np.uint8)
     hq_g = np.empty(n, np.float32)
+    hs = None if h_static_g is None else np.array([h_static_g], np.float32)
     lib().orc_expert_ffn(f, H, F, float(cap), int(h_round_bf16), int(mx_mode), _p(Wg), _p(Wu), _p(Wd), n,
-                         _p(a), _p(y), _p(hb), _p(hq_codes), _p(hq_sf), _p(hq_g))
+                         _p(a), _p(y), _p(hb), _p(hq_codes), _p(hq_sf), _p(hq_g), _p(hs))
     return dict(y=y, h_bf16=hb, hq_codes=hq_codes, hq_sf=hq_sf, hq_g=hq_g)
 
 
@@ -271,7 +289,7 @@ def quantize_x(w: dict, x_bf16: np.ndarray, mx_mode: int = 0):
 
 
 def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mode: int = 0,
-              expert_cache=None, keep_pairs: bool = False, inputs=None, max_pairs=None):
+              expert_cache=None, keep_pairs: bool = False, inputs=None, max_pairs=None, act_static=None):
     """Run the whole layer for the given token rows (default: all T).
 
     idx_override: optional {token_row_index_in_sample: int32[k]} replacing the
@@ -281,6 +299,9 @@ def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mod
     max_pairs: compute only the first max_pairs (token, slot) pairs of the
     sample's dispatch order (a bounded sample of the work; the output rows are
     then partial sums).
+    act_static: NVFP4 static activation globals [E, 2] (decode factors g_x,
+    g_h per expert; act_global_mode 1): the x rows routed to expert e are
+    encoded with g_x[e] and its h rows with g_h[e].
     Returns dict with x codes, routing, dispatch (over the sample), y per pair
     and the fp64 output [n, H].
     """
@@ -323,7 +344,15 @@ def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mod
         lo, hi = d["offsets"][e], min(d["offsets"][e + 1], budget)
         pids = d["perm"][lo:hi]
         rows = pids // k
-        res = expert_ffn(w["fmt"], dec["gate"], dec["up"], dec["down"], a_all[rows], cap=cap, mx_mode=mx_mode)
+        if act_static is None:
+            a_e = a_all[rows]
+            hs = None
+        else:
+            xs = nvfp4_quantize_static(bf16_bits_to_f32(x[rows]), act_static[e, 0])
+            a_e = decode("nvfp4", *xs, per_tensor=False)
+            hs = float(act_static[e, 1])
+        res = expert_ffn(w["fmt"], dec["gate"], dec["up"], dec["down"], a_e, cap=cap, mx_mode=mx_mode,
+                         h_static_g=hs)
         y[lo:hi] = res["y"]
         if keep_pairs:
             pairs[e] = res

@@ -194,6 +194,19 @@ void orc_nvfp4_quantize(const float* v, int64_t rows, int64_t K, int per_tensor,
   }
 }
 
+/* Static activation globals (act_global_mode 1): row r is encoded with the
+ * given decode factor g_rows[r], G = 1/g (fp32); block maxima beyond
+ * 2688 g saturate.  g_out[r] = g_rows[r]. */
+void orc_nvfp4_quantize_static(const float* v, int64_t rows, int64_t K, const float* g_rows, uint8_t* codes,
+                               uint8_t* sf, float* g_out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    float G = 1.0f / g_rows[r];
+    g_out[r] = g_rows[r];
+    nvfp4_row(v + r * K, K, G, codes + r * (K / 2), sf + r * (K / 16));
+  }
+}
+
 void orc_nvfp4_decode(const uint8_t* codes, const uint8_t* sf, const float* g, int64_t rows, int64_t K,
                       int per_tensor, double* out) {
 #pragma omp parallel for schedule(static)
@@ -354,7 +367,8 @@ void orc_dispatch(int64_t T, int64_t E, int64_t k, const int32_t* idx, int32_t* 
 /*   cap(v) = c * tanh(v / c)  (c = 0: no cap)   [reading: form and c]       */
 /*   h = silu(cap g) * cap u = cap g / (1 + exp(-cap g)) * cap u             */
 /*   h rounded to bf16 [reading: the unfused path's rounding point]          */
-/*   h quantised along F (NVFP4 per-row global, or MXFP8), decoded           */
+/*   h quantised along F (NVFP4 per-row global or the expert's static one,   */
+/*   or MXFP8), decoded                                                      */
 /*   y = W_down h^                                                           */
 /* Wg, Wu: [F,H] decoded fp64; Wd: [H,F]; a: [n,H] decoded activations.      */
 /* Optional outputs: h_bf16 [n,F]; h codes / scales / globals.              */
@@ -363,7 +377,7 @@ void orc_dispatch(int64_t T, int64_t E, int64_t k, const int32_t* idx, int32_t* 
 void orc_expert_ffn(int fmt /*0 nvfp4, 1 mxfp8*/, int64_t H, int64_t F, double cap, int h_round_bf16,
                     int mx_mode, const double* Wg, const double* Wu, const double* Wd, int64_t n,
                     const double* a, double* y, uint16_t* h_bf16_out, uint8_t* hq_codes, uint8_t* hq_sf,
-                    float* hq_g) {
+                    float* hq_g, const float* h_static_g /* NVFP4: the expert's static h global, or NULL */) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int64_t p = 0; p < n; ++p) {
     const double* ap = a + p * H;
@@ -391,7 +405,10 @@ void orc_expert_ffn(int fmt /*0 nvfp4, 1 mxfp8*/, int64_t H, int64_t F, double c
         hrow[f] = (float)hv;
       }
     }
-    if (fmt == 0) {
+    if (fmt == 0 && h_static_g) {
+      orc_nvfp4_quantize_static(hrow, 1, F, h_static_g, codes, sf, &gq);
+      orc_nvfp4_decode(codes, sf, &gq, 1, F, 0, hdec);
+    } else if (fmt == 0) {
       orc_nvfp4_quantize(hrow, 1, F, 0, codes, sf, &gq);
       orc_nvfp4_decode(codes, sf, &gq, 1, F, 0, hdec);
     } else {

@@ -17,14 +17,18 @@ def workload(spec) -> dict:
 
 class GpuWorkload:
     def __init__(self, spec, torch, device="cuda", cap=10.0, mx_scale_mode=0, chunk_experts=8,
-                 with_weights=True):
+                 with_weights=True, act_static=None):
         import block_scaled_fp4_route_gb300 as moe
         self.torch = torch
         self.moe = moe
         self.w = w = workload(spec)
         T, H, E, k, F = w["T"], w["H"], w["E"], w["k"], w["F"]
         self.fmt = w["fmt"]
-        self.cfg = moe.make_config(T, H, E, k, F, w["fmt"], swiglu_cap=cap, mx_scale_mode=mx_scale_mode)
+        # act_static: NVFP4 static activation globals fp32 [E, 2] (numpy), or None
+        self.act_static = None if act_static is None else torch.from_numpy(
+            np.ascontiguousarray(act_static, np.float32)).to(device)
+        self.cfg = moe.make_config(T, H, E, k, F, w["fmt"], swiglu_cap=cap, mx_scale_mode=mx_scale_mode,
+                                   act_global_mode=0 if act_static is None else 1)
         self.x = synth.dev_x(w, torch, device)
         self.w_router = synth.dev_router_weight(w, torch, device)
         self.bias = torch.from_numpy(synth.router_bias(w)).to(device)
@@ -66,7 +70,7 @@ class GpuWorkload:
 
     def forward(self, stream=None):
         self.moe.moe_forward(self.cfg, self.x, self.w_router, self.bias, self.qw["gate"], self.qw["up"],
-                             self.qw["down"], self.out, self.ws, stream)
+                             self.qw["down"], self.out, self.ws, stream, act_static_scales=self.act_static)
         return self.out
 
     def ws_view(self, name, dtype, count):

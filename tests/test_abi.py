@@ -68,7 +68,8 @@ def test_workspace_size_and_layout():
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), 2), (dict(T=70000), 2), (dict(k=0), 2), (dict(k=33), 2), (dict(E=4, k=8), 2),
     (dict(E=2000), 2), (dict(H=4608 + 128), 2), (dict(F=128), 2), (dict(fmt="mxfp8", F=128 + 64), 2),
-    (dict(swiglu_cap=-1.0), 1), (dict(mx_scale_mode=2), 1),
+    (dict(swiglu_cap=-1.0), 1), (dict(mx_scale_mode=2), 1), (dict(act_global_mode=2), 1),
+    (dict(fmt="mxfp8", act_global_mode=1), 1),
 ])
 def test_config_validation(kw, status):
     with pytest.raises(moe.MoeError) as ei:
@@ -113,6 +114,14 @@ def test_argument_validation_without_a_device():
     with pytest.raises(moe.MoeError) as ei:
         moe.moe_forward(c, ok, ok, ok, qw, qw, qw, ok, ws, stream=0)
     assert ei.value.status == 1
+    cs = cfg(act_global_mode=1)                # static activation globals: the scales are required
+    qg = moe.qweight(0x20000, 0x30000, 0x40000)
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_forward(cs, ok, ok, ok, qg, qg, qg, ok, ws, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(moe.MoeError) as ei:   # and 4-byte aligned
+        moe.moe_forward(cs, ok, ok, ok, qg, qg, qg, ok, ws, stream=0, act_static_scales=0x10002)
+    assert ei.value.status == 3
     with pytest.raises(moe.MoeError) as ei:   # tiled scales need rows % 128 == 0
         moe.lib()
         st = moe.lib().moe_quantize(0, 0, 1, 0x10000, 100, 256, 0, 1, 0x20000, 0x30000, 0x40000, 0)

@@ -404,3 +404,26 @@ def test_generator_moments_and_bounds():
     w = synth.WORKLOADS["decode192_mxfp8_outliers"]
     flags = synth.outlier_flags(w)
     assert flags.sum() == 2
+
+
+def test_nvfp4_static_global_saturates_at_2688_g():
+    # act_global_mode 1: a row encoded with a given decode factor g (G = 1/g).
+    # The worked block [10.5, 0 x 15]: with g = 2^-7 (G = 128) the block scale
+    # is E4M3(10.5 / 6 * 128 = 224) = 0x76 and 10.5 * 128/224 = 6 -> code 7,
+    # decoding to 6 * 224 * 2^-7 = 10.5 exactly; with g = 2^-10 (G = 1024) the
+    # block scale saturates at 448 (0x7E) and the value at code 7, decoding to
+    # 6 * 448 * 2^-10 = 2688 g = 2.625.
+    v = np.zeros((1, 16), np.float32)
+    v[0, 0] = 10.5
+    c, s, g = oracle.nvfp4_quantize_static(v, 2.0 ** -7)
+    assert s[0, 0] == 0x76 and (c[0, 0] & 0xF) == 7 and g[0] == np.float32(2.0 ** -7)
+    assert oracle.nvfp4_decode(c, s, g)[0, 0] == 10.5
+    c, s, g = oracle.nvfp4_quantize_static(v, 2.0 ** -10)
+    assert s[0, 0] == 0x7E and (c[0, 0] & 0xF) == 7
+    assert oracle.nvfp4_decode(c, s, g)[0, 0] == 2688 * 2.0 ** -10
+    # the dynamic global is the static one at g = amax / 2688
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal((4, 64)) * 3).astype(np.float32)
+    dyn = oracle.nvfp4_quantize(x)
+    sta = oracle.nvfp4_quantize_static(x, dyn[2])
+    assert all(np.array_equal(a, b) for a, b in zip(dyn, sta))

@@ -25,6 +25,8 @@
 // Three kernels: k_router_prep (||w_e|| for every expert; clears the status
 // word), k_router_tc (one 128-token x 128-expert tile per CTA, TMA -> smem ->
 // tcgen05.mma -> TMEM -> fp32 logits), k_router_select (one warp per token).
+#include <type_traits>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -371,24 +373,28 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
   }
   __syncwarp();
 
-  // exact keys of the candidates, four at a time
-  constexpr int G = 4;
-  for (int i0 = 0; i0 < nc; i0 += G) {
+  // exact keys of the candidates: four at a time, the last one to three in a
+  // group of their own size (no padded dot products)
+  auto exact_group = [&](auto g_tag, int i0) {
+    constexpr int G = decltype(g_tag)::value;
     const __nv_bfloat16* rows[G];
 #pragma unroll
-    for (int n = 0; n < G; ++n) rows[n] = wr + (int64_t)cid[min(i0 + n, nc - 1)] * H;
+    for (int n = 0; n < G; ++n) rows[n] = wr + (int64_t)cid[i0 + n] * H;
     float l[G];
     exact_logits<G>(xr, rows, H, lane, l);
 #pragma unroll
-    for (int n = 0; n < G; ++n) {
-      const int i = i0 + n;
-      if (lane == n && i < nc) {
+    for (int n = 0; n < G; ++n)
+      if (lane == n) {
         const float sg = router_sigmoid(l[n]);
-        cs[i] = sg;
-        ckey[i] = __fadd_rn(sg, bias[cid[i]]);
+        cs[i0 + n] = sg;
+        ckey[i0 + n] = __fadd_rn(sg, bias[cid[i0 + n]]);
       }
-    }
-  }
+  };
+  int i0 = 0;
+  for (; i0 + 4 <= nc; i0 += 4) exact_group(std::integral_constant<int, 4>{}, i0);
+  if (nc - i0 == 3) exact_group(std::integral_constant<int, 3>{}, i0);
+  else if (nc - i0 == 2) exact_group(std::integral_constant<int, 2>{}, i0);
+  else if (nc - i0 == 1) exact_group(std::integral_constant<int, 1>{}, i0);
   __syncwarp();
 
   // top-k of the candidates by exact key, ties to the lower expert index

@@ -152,8 +152,10 @@ __device__ void quant_row(const Src* row, int K, float G, int mx_mode, int ndst,
 
 // Activation rows (x, h): each thread keeps its blocks of the row in
 // registers, so the row is read once: absolute maximum (NVFP4 global), then
-// the codes.  Rows of up to kRowRounds * kQThreads blocks (16384 elements).
-constexpr int kRowRounds = 2;
+// the codes.  Rows of up to kRowRounds<FMT> * kQThreads blocks: 16384
+// elements in both formats (the largest H and F the API accepts).
+template <int FMT>
+constexpr int kRowRounds = FMT == MOE_FMT_NVFP4 ? 4 : 2;
 
 // sg (NVFP4, static activation globals): the decode factor of each
 // destination (its expert's); nullptr = dynamic, from the row maximum.
@@ -165,10 +167,10 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
   const int nb = K / BS;
   const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
   const int64_t C = nb;
-  float v[kRowRounds][BS];
+  float v[kRowRounds<FMT>][BS];
   float m = 0.0f;
 #pragma unroll
-  for (int r = 0; r < kRowRounds; ++r) {
+  for (int r = 0; r < kRowRounds<FMT>; ++r) {
     const int b = threadIdx.x + r * blockDim.x;
     if (b < nb) {
       load_block_bf16(row + (int64_t)b * BS, BS, v[r]);
@@ -184,7 +186,7 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
         const float Gd = __fdiv_rn(1.0f, sg[d]);
         const int64_t rr = dst[d];
 #pragma unroll
-        for (int r = 0; r < kRowRounds; ++r) {
+        for (int r = 0; r < kRowRounds<FMT>; ++r) {
           const int b = threadIdx.x + r * blockDim.x;
           if (b >= nb) continue;
           uint2 c;
@@ -199,7 +201,7 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
     if (threadIdx.x < ndst) glob[dst[threadIdx.x]] = __fdiv_rn(1.0f, G);
   }
 #pragma unroll
-  for (int r = 0; r < kRowRounds; ++r) {
+  for (int r = 0; r < kRowRounds<FMT>; ++r) {
     const int b = threadIdx.x + r * blockDim.x;
     if (b >= nb) continue;
     if constexpr (FMT == MOE_FMT_NVFP4) {

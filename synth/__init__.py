@@ -14,7 +14,8 @@ seeded tensors stand in for real activations and trained weights):
 * W_r[e,h] = bf16(z * fp32(1/sqrt(H))).
 * bias b[e] = fp32(-0.1 + 0.2*u), u a 24-bit uniform; or the Zipf recipe:
   b[e] = -c*s*ln(rank_e) with s = 1.1, rank a seeded permutation, and the 32
-  least popular experts at -2 so that they receive no tokens.
+  least popular experts at -2 so that they receive no tokens; or "hot": the
+  uniform bias + 10 on the first k experts (every token routes to them).
 * expert master weights W[e,n,k] = z * fp32(1/sqrt(fan_in)), fp32, quantised
   afterwards by the method's own encoder.
 """
@@ -69,6 +70,8 @@ WORKLOADS = {
     "profile_decode16_nvfp4_e96": dict(T=16, H=4608, E=96, k=8, F=2304, fmt="nvfp4", seed=21,
                                        outlier_frac=0.0, bias="uniform"),
     "profile_prefill2048_mxfp8_e64": dict(T=2048, H=4608, E=64, k=8, F=2304, fmt="mxfp8", seed=22,
+                                          outlier_frac=0.0, bias="uniform"),
+    "profile_prefill2048_nvfp4_e64": dict(T=2048, H=4608, E=64, k=8, F=2304, fmt="nvfp4", seed=23,
                                           outlier_frac=0.0, bias="uniform"),
 }
 
@@ -190,6 +193,11 @@ def router_bias(w: dict) -> np.ndarray:
     out = np.empty(w["E"], np.float32)
     if w["bias"] == "uniform":
         host_lib().synth_host_bias_uniform(w["seed"], w["E"], -0.1, 0.1, _ptr(out))
+    elif w["bias"] == "hot":
+        # degenerate routing: the first k experts outrank every other key, so
+        # each of them receives every token and the rest none
+        host_lib().synth_host_bias_uniform(w["seed"], w["E"], -0.1, 0.1, _ptr(out))
+        out[:w["k"]] += np.float32(10.0)
     elif w["bias"] == "zipf":
         host_lib().synth_host_bias_zipf(w["seed"], w["E"], ZIPF_C, ZIPF_S, ZIPF_N_COLD,
                                         ZIPF_COLD_BIAS, _ptr(out))

@@ -1,6 +1,7 @@
 """The largest shapes the API accepts, each in one dimension at a time: 1024
 experts with k = 32, hidden and FFN widths of 16384 (rows quantised in
-registers by one CTA), and 65536 tokens.  Same checks as the layer tests:
+registers by one CTA), and 65536 tokens; and degenerate routing (every token
+on the same k experts).  Same checks as the layer tests:
 routing against the oracle, dispatch and x codes bit-exact, h near-exact,
 the output within tolerance (sampled tokens for the largest batch)."""
 import numpy as np
@@ -18,6 +19,10 @@ LIMITS = {
     "H16384_nvfp4": dict(T=3, H=16384, E=4, k=2, F=256, fmt="nvfp4", seed=41, **U),
     "F16384_nvfp4": dict(T=2, H=256, E=2, k=1, F=16384, fmt="nvfp4", seed=42, **U),
     "F16384_mxfp8": dict(T=5, H=256, E=2, k=2, F=16384, fmt="mxfp8", seed=43, **U),
+    # degenerate routing: all 300 tokens on the same 4 of 64 experts (one
+    # expert with every token, 60 with none; 128-row tiles)
+    "all_tokens_4_experts_nvfp4": dict(T=300, H=512, E=64, k=4, F=256, fmt="nvfp4", seed=45, outlier_frac=0.0,
+                                       bias="hot"),
 }
 
 

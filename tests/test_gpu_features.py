@@ -69,8 +69,13 @@ def test_forward_replays_as_cuda_graph(name):
     assert torch.equal(out2.view(torch.int16), eager.view(torch.int16))
 
 
-def test_bounded_wait_timeout_is_reported_and_device_stays_usable():
-    gw = GpuWorkload("tiny_mxfp8", torch)
+WIDE_MXFP8 = dict(T=1100, H=384, E=5, k=3, F=384, fmt="mxfp8", seed=19, outlier_frac=0.0, bias="uniform")
+
+
+# tiny: 64-row weight-major tiles; WIDE_MXFP8: 128-row token-major tiles
+@pytest.mark.parametrize("spec", ["tiny_mxfp8", WIDE_MXFP8], ids=["decode_tiles", "token_major_tiles"])
+def test_bounded_wait_timeout_is_reported_and_device_stays_usable(spec):
+    gw = GpuWorkload(spec, torch)
     ref = gw.forward().clone()
     assert moe.moe_poll_device_status(gw.ws) == 0
     # ~1 ms of SM clock per wait; every wait of the kernel runs out

@@ -29,6 +29,12 @@ SMALL = {
     "tc_router_nvfp4": dict(T=600, H=512, E=48, k=4, F=256, fmt="nvfp4", seed=16, **U),
     "tc_router_mxfp8_outliers": dict(T=520, H=384, E=160, k=6, F=128, fmt="mxfp8", seed=17, outlier_frac=0.02,
                                      bias="uniform"),
+    # hundreds of tokens per expert on 128-row token tiles: 4-10 tiles per
+    # expert with ragged tails, H % 256 == 128 (down: no second weight block
+    # in the last tile), empty experts ("hot": two experts take every token)
+    "deep_nvfp4": dict(T=1200, H=512, E=4, k=2, F=256, fmt="nvfp4", seed=18, **U),
+    "deep_mxfp8": dict(T=1100, H=384, E=5, k=3, F=384, fmt="mxfp8", seed=19, **U),
+    "deep_hot_nvfp4": dict(T=1100, H=512, E=8, k=2, F=256, fmt="nvfp4", seed=20, outlier_frac=0.0, bias="hot"),
 }
 
 

@@ -17,12 +17,15 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const float* __restric
   __shared__ int pos[kMaxK];
   __shared__ float ww[kMaxK];
   const int t = blockIdx.x;
+  // the routing weights and pair positions come from kernels that had
+  // completed before the previous kernel's threads passed their own
+  // dependency wait: read (through L2) before this one's
+  if (threadIdx.x < k) {
+    pos[threadIdx.x] = __ldcg(pair_pos + (int64_t)t * k + threadIdx.x);
+    ww[threadIdx.x] = __ldcg(w + (int64_t)t * k + threadIdx.x);
+  }
   pdl_wait();
   pdl_trigger();
-  if (threadIdx.x < k) {
-    pos[threadIdx.x] = pair_pos[(int64_t)t * k + threadIdx.x];
-    ww[threadIdx.x] = w[(int64_t)t * k + threadIdx.x];
-  }
   __syncthreads();
   for (int c = blockIdx.y * kCombThreads + threadIdx.x; c < H / 4; c += gridDim.y * kCombThreads) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);

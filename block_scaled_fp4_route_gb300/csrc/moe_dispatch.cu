@@ -163,27 +163,31 @@ __global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __res
 }
 
 constexpr int kSmallWords = 12288;  // 48 KB of token bitmaps
+constexpr int kSmallPairs = 8192;   // 32 KB of staged expert ids (T <= 256, k <= 32)
 
-// Whole dispatch for small batches in one CTA of 1024 threads: token bitmaps
-// of every expert in shared memory, counts / offsets / segments / tiles by
-// block scans, then each expert's thread ranks its tokens in order.
+// Whole dispatch for small batches in one CTA of 1024 threads: the expert
+// ids and token bitmaps of every expert in shared memory, counts / offsets /
+// segments / tiles by block scans, then each expert's thread ranks its tokens
+// in order (finding each token's slot among the staged ids).
 __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restrict__ idx, int T, int k, int E,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos,
                                                          int32_t* __restrict__ seg_start, RowTile* __restrict__ tiles,
                                                          int32_t* __restrict__ rt_base, uint32_t* __restrict__ status,
                                                          int nt) {
-  extern __shared__ uint32_t sbm[];  // [E][W]
+  extern __shared__ uint32_t sbm[];  // [E][W] bitmaps, then the ids [T*k]
   __shared__ int sh[32];
   const int W = (T + 31) / 32;
+  int32_t* sidx = reinterpret_cast<int32_t*>(sbm + E * W);
   pdl_wait();
   pdl_trigger();
   if (status && threadIdx.x == 0) *status = 0u;
   for (int i = threadIdx.x; i < E * W; i += blockDim.x) sbm[i] = 0u;
-  __syncthreads();
   const int P = T * k;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) sidx[p] = idx[p];
+  __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const int t = p / k, e = idx[p];
+    const int t = p / k, e = sidx[p];
     if ((unsigned)e < (unsigned)E) atomicOr(&sbm[e * W + (t >> 5)], 1u << (t & 31));
   }
   __syncthreads();
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
         v &= v - 1;
         int t = i * 32 + b;
         int j = 0;
-        while (j < k && idx[t * k + j] != e) ++j;
+        while (j < k && sidx[t * k + j] != e) ++j;
         perm[off + rank] = t * k + j;
         pair_pos[t * k + j] = off + rank;
         ++rank;
@@ -238,17 +242,19 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
 // The one-CTA path ranks each expert's tokens serially, so it is kept for
 // decode batches (up to 256 tokens).
 bool dispatch_fits_one_cta(const moe_config& c) {
-  return c.T <= 256 && c.E <= 1024 && (int64_t)c.E * ((c.T + 31) / 32) <= kSmallWords;
+  return c.T <= 256 && c.E <= 1024 && (int64_t)c.E * ((c.T + 31) / 32) <= kSmallWords &&
+         (int64_t)c.T * c.k <= kSmallPairs;
 }
 
 cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
                                   int32_t* perm, int32_t* pair_pos, int32_t* seg_start, RowTile* tiles,
                                   int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
   if (!dispatch_fits_one_cta(c)) return cudaErrorNotSupported;
-  const size_t smem = (size_t)c.E * ((c.T + 31) / 32) * 4;
+  const size_t smem = ((size_t)c.E * ((c.T + 31) / 32) + (size_t)c.T * c.k) * 4;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmallWords * 4);
+    cudaError_t e = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (kSmallWords + kSmallPairs) * 4);
     if (e != cudaSuccess) return e;
     attr = true;
   }

@@ -139,6 +139,13 @@ __device__ __forceinline__ void map_tile(int t, int MT, const int32_t* rtb, int 
   rt = rtb[lo] + l % nrt;
 }
 
+// A tile descriptor through L2 (it may be read before this grid's dependency
+// wait, when this SM's L1 could still hold an older copy).
+__device__ __forceinline__ RowTile load_tile(const RowTile* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  return RowTile{v.x, v.y, v.z, v.w};
+}
+
 template <int FMT, bool GATED>
 __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
     k_moe_gemm(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -178,14 +185,19 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
     prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
   }
-  // everything above is independent of the previous kernel; from here on
-  // the tile plan and the activations it wrote are read
-  pdl_wait();
-  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = a.rt_base[i];
+  // The tile plan was written by the dispatch, which had completed before
+  // the previous kernel's threads passed their own dependency wait, and this
+  // grid starts only after all of them have: it is read now (through L2).
+  // What the previous kernel writes is read only after pdl_wait; the
+  // producer waits after it has requested its first weight stages.
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = __ldcg(a.rt_base + i);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // warp 0 stays out: a wait taken by some of its lanes would hold the
+  // producer lane too (its other lanes read nothing the previous kernel wrote)
+  if (warp != 0) pdl_wait();
 
   const int MT = (a.NA + C::ROWS - 1) / C::ROWS;
   const int total = s_rtb[a.E] * MT;
@@ -205,14 +217,39 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
       RowTile rt{};
       if (blockIdx.x < total) {
         map_tile(blockIdx.x, MT, s_rtb, a.E, mt, rti);
-        rt = a.tiles[rti];
+        rt = load_tile(a.tiles + rti);
       }
+      // The first tile's weight blocks and their scales for the first stages
+      // do not depend on the previous kernel: requested before the wait, they
+      // stream while it finishes.
+      const int pre = (blockIdx.x < total && !a.withhold_loads) ? min(KB, C::STAGES) : 0;
+      if (pre > 0) {
+        const int N = (rt.n_valid + 15) & ~15;
+        const int arow = rt.e * a.NA + mt * C::ROWS;
+        const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+        const int arow1 = (GATED || !second) ? arow : arow + 128;
+        const uint8_t* sfa0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
+        const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
+        const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
+#pragma unroll 1
+        for (int kb = 0; kb < pre; ++kb) {  // fresh stages, phase 0
+          uint8_t* sbase = smem + kb * C::STAGE_BYTES;
+          uint8_t* sSF = sbase + C::NA * C::A_BYTES + C::B_BYTES;
+          mbar_expect_tx(&full[kb], bytes);
+          armed |= 1u << kb;
+          tma_load_2d(sbase, &tmA0, &full[kb], kb * 128, arow);
+          tma_load_2d(sbase + C::A_BYTES, &tmA1, &full[kb], kb * 128, arow1);
+          bulk_load(sSF, sfa0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[kb]);
+          bulk_load(sSF + C::SF_BYTES, sfa1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[kb]);
+        }
+      }
+      pdl_wait();
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
         int mt_n = 0, rti_n = 0;
         RowTile rt_n{};
         if (t + (int)gridDim.x < total) {
           map_tile(t + gridDim.x, MT, s_rtb, a.E, mt_n, rti_n);
-          rt_n = a.tiles[rti_n];
+          rt_n = load_tile(a.tiles + rti_n);
         }
         const int N = (rt.n_valid + 15) & ~15;
         const int arow = rt.e * a.NA + mt * C::ROWS;
@@ -225,7 +262,19 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
         const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
         const uint8_t* sfb = a.sfB + (int64_t)(rt.row / C::NT) * atoms_per_row * 512;
         const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
+        const bool first = t == (int)blockIdx.x;
         for (int kb = 0; kb < KB; ++kb) {
+          if (first && kb < pre) {  // weights requested before the wait: now the token rows and scales
+            uint8_t* sB = smem + stage * C::STAGE_BYTES + C::NA * C::A_BYTES;
+            uint8_t* sSF = sB + C::B_BYTES;
+            for (int i = 0; i < N / 16; ++i) tma_load_2d(sB + i * 2048, &tmB, &full[stage], kb * 128, rt.row + 16 * i);
+            bulk_load(sSF + C::NA * C::SF_BYTES, sfb + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
             ok = false;
             break;
@@ -549,6 +598,105 @@ __device__ __forceinline__ void store_rows32(float* base, int stride, int nv, co
     if (i < nv) base[(int64_t)i * stride] = __uint_as_float(i < 16 ? lo[i] : hi[i - 16]);
 }
 
+// Token-major epilogue after the TMEM copy: r0 / r1 hold this thread's 64
+// columns of weight block 0 / 1 (token row n of the tile, features
+// 64 hc .. 64 hc + 63 of each block); s0 / s1 the global scales.  Gated:
+// capped SwiGLU, bf16 h (MXFP8: quantised here); down: y rows, transposed
+// across the warp so that each store writes 128 contiguous bytes.
+template <int FMT, bool GATED>
+__device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r0)[4][16], uint32_t (&r1)[4][16],
+                                                 const RowTile& rt, int mt, int n, bool valid, int q, int hc,
+                                                 int lane, float s0, float s1) {
+  constexpr int ROWS = GATED ? 128 : 256;
+  constexpr int NT = kNTWide;
+  const bool second = GATED || (mt * ROWS + 128 < a.NA);
+  // every lane stays on the same path below (the down epilogue shuffles
+  // across the warp); lanes past n_valid only skip their stores
+  if constexpr (GATED) {
+    if (!valid) return;  // no warp-collective operation in the gated epilogue
+    const bool capped = a.cap > 0.0f;
+    const int64_t row = (int64_t)rt.row + n;
+    const int f0 = mt * ROWS + 64 * hc;  // first feature of this thread's share
+    // two 32-feature blocks (one MXFP8 scale block each), one unrolled
+#pragma unroll 1
+    for (int b = 0; b < 2; ++b) {
+      uint32_t pk[16];  // 32 bf16 h values
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        const int c = j >> 4, jj = j & 15;
+        float g0 = __uint_as_float(r0[c][jj]) * s0, g1 = __uint_as_float(r0[c][jj + 1]) * s0;
+        float u0 = __uint_as_float(r1[c][jj]) * s1, u1 = __uint_as_float(r1[c][jj + 1]) * s1;
+        if (capped) {
+          g0 = a.cap * tanh_soft(g0 * a.inv_cap);
+          g1 = a.cap * tanh_soft(g1 * a.inv_cap);
+          u0 = a.cap * tanh_soft(u0 * a.inv_cap);
+          u1 = a.cap * tanh_soft(u1 * a.inv_cap);
+        }
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(silu(g0) * u0, silu(g1) * u1);
+        pk[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+      }
+      const int f = f0 + 32 * b;
+      if constexpr (FMT == MOE_FMT_MXFP8) {
+        // the block's 32 features are this thread's: amax, E8M0 scale and
+        // E4M3 codes in registers
+        float m = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(pk[i] << 16)), fabsf(__uint_as_float(pk[i] & 0xFFFF0000u))));
+        uint32_t sc = 0, q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (m != 0.0f) {
+          sc = mx_scale_code(m, a.mx_mode);
+          const float mul = exp2i(127 - (int)sc);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            q[i / 2] |= e4m3x2_encode(__fmul_rn(__uint_as_float(pk[i] << 16), mul),
+                                      __fmul_rn(__uint_as_float(pk[i] & 0xFFFF0000u), mul))
+                        << (16 * (i & 1));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(a.hq_codes + row * a.NA + f);
+        dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        a.hq_scales[act_scale_offset(row, f >> 5, a.NA >> 5, NT)] = (uint8_t)sc;
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(a.h_out + row * a.NA + f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+      }
+      // the next block moves to the front (register moves, no indexing)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        r0[0][j] = r0[2][j];
+        r0[1][j] = r0[3][j];
+        r1[0][j] = r1[2][j];
+        r1[1][j] = r1[3][j];
+      }
+    }
+  } else {
+    // y rows are written feature-contiguously: each 32 x 32 (token x
+    // feature) group of the warp is transposed with xor shuffles, then
+    // lane L stores feature L of one token row per instruction
+    const int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile
+    float* ybase = a.y_out + ((int64_t)rt.canon + q * 32) * a.NA + mt * ROWS + 64 * hc + lane;
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch)
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        r0[ch][j] = __float_as_uint(__uint_as_float(r0[ch][j]) * s0);
+        r1[ch][j] = __float_as_uint(__uint_as_float(r1[ch][j]) * s1);
+      }
+    warp_transpose32(r0[0], r0[1], lane);
+    warp_transpose32(r0[2], r0[3], lane);
+    store_rows32(ybase, a.NA, nv, r0[0], r0[1]);
+    store_rows32(ybase + 32, a.NA, nv, r0[2], r0[3]);
+    if (second) {
+      warp_transpose32(r1[0], r1[1], lane);
+      warp_transpose32(r1[2], r1[3], lane);
+      store_rows32(ybase + 128, a.NA, nv, r1[0], r1[1]);
+      store_rows32(ybase + 160, a.NA, nv, r1[2], r1[3]);
+    }
+  }
+}
+
 template <int FMT, bool GATED>
 struct CfgTM {
   static constexpr int NT = kNTWide;               // token rows per tile (MMA M)
@@ -616,12 +764,15 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
     prefetch_tmap(&tmA1);
     prefetch_tmap(&tmB);
   }
-  pdl_wait();
-  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = a.rt_base[i];
+  // the tile plan is read before the dependency wait, as in k_moe_gemm
+  for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = __ldcg(a.rt_base + i);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // warp 0 stays out: a wait taken by some of its lanes would hold the
+  // producer lane too (its other lanes read nothing the previous kernel wrote)
+  if (warp != 0) pdl_wait();
 
   const int MT = (a.NA + C::ROWS - 1) / C::ROWS;
   const int total = s_rtb[a.E] * MT;
@@ -639,14 +790,36 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
       RowTile rt{};
       if (blockIdx.x < total) {
         map_tile(blockIdx.x, MT, s_rtb, a.E, mt, rti);
-        rt = a.tiles[rti];
+        rt = load_tile(a.tiles + rti);
       }
+      // the first tile's weight stages go out before the dependency wait
+      const int pre = (blockIdx.x < total && !a.withhold_loads) ? min(KB, C::STAGES) : 0;
+      if (pre > 0) {
+        const int arow = rt.e * a.NA + mt * C::ROWS;
+        const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
+        const int arow1 = (GATED || !second) ? arow : arow + 128;
+        const uint8_t* sfw0 = a.sfA0 + (int64_t)(arow >> 7) * atoms_per_row * 512;
+        const uint8_t* sfw1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
+        constexpr uint32_t bytes = C::A_BYTES + C::B_BYTES + 3 * C::SF_BYTES;
+#pragma unroll 1
+        for (int kb = 0; kb < pre; ++kb) {  // fresh stages, phase 0
+          uint8_t* sW = smem + kb * C::STAGE_BYTES + C::A_BYTES;
+          uint8_t* sSF = sW + C::B_BYTES;
+          mbar_expect_tx(&full[kb], bytes);
+          armed |= 1u << kb;
+          tma_load_2d(sW, &tmA0, &full[kb], kb * 128, arow);
+          tma_load_2d(sW + C::B_BYTES / 2, &tmA1, &full[kb], kb * 128, arow1);
+          bulk_load(sSF + C::SF_BYTES, sfw0 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[kb]);
+          bulk_load(sSF + 2 * C::SF_BYTES, sfw1 + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[kb]);
+        }
+      }
+      pdl_wait();
       for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
         int mt_n = 0, rti_n = 0;
         RowTile rt_n{};
         if (t + (int)gridDim.x < total) {
           map_tile(t + gridDim.x, MT, s_rtb, a.E, mt_n, rti_n);
-          rt_n = a.tiles[rti_n];
+          rt_n = load_tile(a.tiles + rti_n);
         }
         const int arow = rt.e * a.NA + mt * C::ROWS;
         // down: the second block of the last tile lies past the expert when
@@ -658,7 +831,19 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
         const uint8_t* sfw1 = a.sfA1 + (int64_t)(arow1 >> 7) * atoms_per_row * 512;
         const uint8_t* sft = a.sfB + (int64_t)(rt.row / C::NT) * atoms_per_row * 512;
         constexpr uint32_t bytes = C::A_BYTES + C::B_BYTES + 3 * C::SF_BYTES;
+        const bool first = t == (int)blockIdx.x;
         for (int kb = 0; kb < KB; ++kb) {
+          if (first && kb < pre) {  // weights requested before the wait: now the token rows and scales
+            uint8_t* sTok = smem + stage * C::STAGE_BYTES;
+            uint8_t* sSF = sTok + C::A_BYTES + C::B_BYTES;
+            tma_load_2d(sTok, &tmB, &full[stage], kb * 128, rt.row);
+            bulk_load(sSF, sft + (int64_t)kb * C::SF_BYTES, C::SF_BYTES, &full[stage]);
+            if (++stage == C::STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, a.status, ST_TIMEOUT_PRODUCER, a.limit)) {
             ok = false;
             break;
@@ -771,7 +956,6 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
       map_tile(t, MT, s_rtb, a.E, mt, rti);
       const RowTile rt = a.tiles[rti];
       const bool valid = n < rt.n_valid;
-      const bool second = GATED || (mt * C::ROWS + 128 < a.NA);
       float sA0 = 1.0f, sA1 = 1.0f, gb = 1.0f;
       if constexpr (FMT == MOE_FMT_NVFP4) {
         sA0 = a.gA0[rt.e];
@@ -792,92 +976,7 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty);
-      const float s0 = sA0 * gb, s1 = sA1 * gb;
-      // every lane stays on the same path below (the down epilogue shuffles
-      // across the warp); lanes past n_valid only skip their stores
-      if constexpr (GATED) {
-        if (!valid) continue;  // no warp-collective operation in the gated epilogue
-        const bool capped = a.cap > 0.0f;
-        const int64_t row = (int64_t)rt.row + n;
-        const int f0 = mt * C::ROWS + 64 * hc;  // first feature of this thread's share
-        // two 32-feature blocks (one MXFP8 scale block each), one unrolled
-#pragma unroll 1
-        for (int b = 0; b < 2; ++b) {
-          uint32_t pk[16];  // 32 bf16 h values
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int c = j >> 4, jj = j & 15;
-            float g0 = __uint_as_float(r0[c][jj]) * s0, g1 = __uint_as_float(r0[c][jj + 1]) * s0;
-            float u0 = __uint_as_float(r1[c][jj]) * s1, u1 = __uint_as_float(r1[c][jj + 1]) * s1;
-            if (capped) {
-              g0 = a.cap * tanh_soft(g0 * a.inv_cap);
-              g1 = a.cap * tanh_soft(g1 * a.inv_cap);
-              u0 = a.cap * tanh_soft(u0 * a.inv_cap);
-              u1 = a.cap * tanh_soft(u1 * a.inv_cap);
-            }
-            const __nv_bfloat162 hv = __floats2bfloat162_rn(silu(g0) * u0, silu(g1) * u1);
-            pk[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
-          }
-          const int f = f0 + 32 * b;
-          if constexpr (FMT == MOE_FMT_MXFP8) {
-            // the block's 32 features are this thread's: amax, E8M0 scale and
-            // E4M3 codes in registers
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              m = fmaxf(m, fmaxf(fabsf(__uint_as_float(pk[i] << 16)), fabsf(__uint_as_float(pk[i] & 0xFFFF0000u))));
-            uint32_t sc = 0, q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            if (m != 0.0f) {
-              sc = mx_scale_code(m, a.mx_mode);
-              const float mul = exp2i(127 - (int)sc);
-#pragma unroll
-              for (int i = 0; i < 16; ++i)
-                q[i / 2] |= e4m3x2_encode(__fmul_rn(__uint_as_float(pk[i] << 16), mul),
-                                          __fmul_rn(__uint_as_float(pk[i] & 0xFFFF0000u), mul))
-                            << (16 * (i & 1));
-            }
-            uint4* dst = reinterpret_cast<uint4*>(a.hq_codes + row * a.NA + f);
-            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-            a.hq_scales[act_scale_offset(row, f >> 5, a.NA >> 5, C::NT)] = (uint8_t)sc;
-          } else {
-            uint4* dst = reinterpret_cast<uint4*>(a.h_out + row * a.NA + f);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-          // the next block moves to the front (register moves, no indexing)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            r0[0][j] = r0[2][j];
-            r0[1][j] = r0[3][j];
-            r1[0][j] = r1[2][j];
-            r1[1][j] = r1[3][j];
-          }
-        }
-      } else {
-        // y rows are written feature-contiguously: each 32 x 32 (token x
-        // feature) group of the warp is transposed with xor shuffles, then
-        // lane L stores feature L of one token row per instruction
-        const int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile
-        float* ybase = a.y_out + ((int64_t)rt.canon + q * 32) * a.NA + mt * C::ROWS + 64 * hc + lane;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch)
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            r0[ch][j] = __float_as_uint(__uint_as_float(r0[ch][j]) * s0);
-            r1[ch][j] = __float_as_uint(__uint_as_float(r1[ch][j]) * s1);
-          }
-        warp_transpose32(r0[0], r0[1], lane);
-        warp_transpose32(r0[2], r0[3], lane);
-        store_rows32(ybase, a.NA, nv, r0[0], r0[1]);
-        store_rows32(ybase + 32, a.NA, nv, r0[2], r0[3]);
-        if (second) {
-          warp_transpose32(r1[0], r1[1], lane);
-          warp_transpose32(r1[2], r1[3], lane);
-          store_rows32(ybase + 128, a.NA, nv, r1[0], r1[1]);
-          store_rows32(ybase + 160, a.NA, nv, r1[2], r1[3]);
-        }
-      }
+      tm_epilogue_math<FMT, GATED>(a, r0, r1, rt, mt, n, valid, q, hc, lane, sA0 * gb, sA1 * gb);
     }
   }
   __syncthreads();

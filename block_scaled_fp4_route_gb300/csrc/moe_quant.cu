@@ -160,14 +160,14 @@ constexpr int kRowRounds = FMT == MOE_FMT_NVFP4 ? 4 : 2;
 // sg (NVFP4, static activation globals): the decode factor of each
 // destination (its expert's); nullptr = dynamic, from the row maximum.
 template <int FMT>
-__device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
-                                               const int64_t* dst, const float* sg, uint8_t* codes, uint8_t* scales,
-                                               float* glob, float* red, int nt) {
-  constexpr int BS = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+constexpr int kBlockOf = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+
+// This thread's blocks of the row into registers; returns their |max|.
+template <int FMT>
+__device__ __forceinline__ float quant_row_load(const __nv_bfloat16* __restrict__ row, int K,
+                                                float (&v)[kRowRounds<FMT>][kBlockOf<FMT>]) {
+  constexpr int BS = kBlockOf<FMT>;
   const int nb = K / BS;
-  const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
-  const int64_t C = nb;
-  float v[kRowRounds<FMT>][BS];
   float m = 0.0f;
 #pragma unroll
   for (int r = 0; r < kRowRounds<FMT>; ++r) {
@@ -178,6 +178,18 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
       for (int i = 0; i < BS; ++i) m = fmaxf(m, fabsf(v[r][i]));
     }
   }
+  return m;
+}
+
+// Codes and scales of the row loaded by quant_row_load (m: this thread's
+// |max|) to the ndst destination rows.
+template <int FMT>
+__device__ __forceinline__ void quant_row_encode(float (&v)[kRowRounds<FMT>][kBlockOf<FMT>], float m, int K,
+                                                 int mx_mode, int ndst, const int64_t* dst, const float* sg,
+                                                 uint8_t* codes, uint8_t* scales, float* glob, float* red, int nt) {
+  const int nb = K / kBlockOf<FMT>;
+  const int64_t cbytes = FMT == MOE_FMT_NVFP4 ? K / 2 : K;
+  const int64_t C = nb;
   float G = 1.0f;
   if constexpr (FMT == MOE_FMT_NVFP4) {
     if (sg) {  // static: each destination encodes with its own expert's global
@@ -226,7 +238,18 @@ __device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__
   }
 }
 
+template <int FMT>
+__device__ __forceinline__ void quant_row_regs(const __nv_bfloat16* __restrict__ row, int K, int mx_mode, int ndst,
+                                               const int64_t* dst, const float* sg, uint8_t* codes, uint8_t* scales,
+                                               float* glob, float* red, int nt) {
+  float v[kRowRounds<FMT>][kBlockOf<FMT>];
+  const float m = quant_row_load<FMT>(row, K, v);
+  quant_row_encode<FMT>(v, m, K, mx_mode, ndst, dst, sg, codes, scales, glob, red, nt);
+}
+
 // x: one CTA per token; written to the k expert-grouped rows of the token.
+// x is the layer's input, not the previous kernel's output: its row is read
+// before the dependency wait.
 template <int FMT>
 __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __restrict__ x, int H, int k,
                                                        int mx_mode, const int32_t* __restrict__ idx,
@@ -238,6 +261,8 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
   __shared__ int64_t dst[kMaxK];
   __shared__ float sg[kMaxK];
   const int t = blockIdx.x;
+  float v[kRowRounds<FMT>][kBlockOf<FMT>];
+  const float m = quant_row_load<FMT>(x + (int64_t)t * H, H, v);
   pdl_wait();
   pdl_trigger();
   if (threadIdx.x < k) {
@@ -247,7 +272,7 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
     if (act_static) sg[threadIdx.x] = act_static[2 * e];
   }
   __syncthreads();
-  quant_row_regs<FMT>(x + (int64_t)t * H, H, mx_mode, k, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
+  quant_row_encode<FMT>(v, m, H, mx_mode, k, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
 }
 
 // h: one CTA per canonical pair position p; row = its padded row.
@@ -262,13 +287,16 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
   __shared__ int64_t dst[1];
   __shared__ float sg[1];
   const int p = blockIdx.x;
-  pdl_wait();
-  pdl_trigger();
+  // The row's place comes from the routing and the dispatch, which had
+  // completed before the previous kernel's threads passed their own
+  // dependency wait: looked up (through L2) before this one's.
   if (threadIdx.x == 0) {
-    const int e = idx[perm[p]];
-    dst[0] = (int64_t)seg_start[e] + (p - offsets[e]);
+    const int e = __ldcg(idx + __ldcg(perm + p));
+    dst[0] = (int64_t)__ldcg(seg_start + e) + (p - __ldcg(offsets + e));
     if (act_static) sg[0] = act_static[2 * e + 1];
   }
+  pdl_wait();
+  pdl_trigger();
   __syncthreads();
   quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
 }

@@ -165,25 +165,27 @@ __global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __res
 constexpr int kSmallWords = 12288;  // 48 KB of token bitmaps
 constexpr int kSmallPairs = 8192;   // 32 KB of staged expert ids (T <= 256, k <= 32)
 
-// Whole dispatch for small batches in one CTA of 1024 threads: the expert
-// ids and token bitmaps of every expert in shared memory, counts / offsets /
-// segments / tiles by block scans, then each expert's thread ranks its tokens
-// in order (finding each token's slot among the staged ids).
+// Whole dispatch for small batches in one CTA of 1024 threads: the expert ids
+// and a token bitmap per expert in shared memory; counts and row tiles of all
+// experts in one block scan (a packed (pairs, row tiles) sum); then every pair
+// finds its rank among its expert's tokens by counting the bitmap bits below
+// its token.
 __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restrict__ idx, int T, int k, int E,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos,
                                                          int32_t* __restrict__ seg_start, RowTile* __restrict__ tiles,
                                                          int32_t* __restrict__ rt_base, uint32_t* __restrict__ status,
                                                          int nt) {
-  extern __shared__ uint32_t sbm[];  // [E][W] bitmaps, then the ids [T*k]
+  extern __shared__ uint32_t sbm[];  // [E][W] bitmaps, then the ids [T*k], then the offsets [E]
   __shared__ int sh[32];
   const int W = (T + 31) / 32;
+  const int P = T * k;
   int32_t* sidx = reinterpret_cast<int32_t*>(sbm + E * W);
+  int32_t* soff = sidx + P;
   pdl_wait();
   pdl_trigger();
   if (status && threadIdx.x == 0) *status = 0u;
   for (int i = threadIdx.x; i < E * W; i += blockDim.x) sbm[i] = 0u;
-  const int P = T * k;
   for (int p = threadIdx.x; p < P; p += blockDim.x) sidx[p] = idx[p];
   __syncthreads();
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
@@ -195,18 +197,19 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
   int c = 0;
   if (e < E)
     for (int i = 0; i < W; ++i) c += __popc(sbm[e * W + i]);
-  int tot;
-  const int off = block_exclusive_scan(c, &tot, sh);
   const int nrt = (c + nt - 1) / nt;
-  int ptot;
-  const int seg = block_exclusive_scan(nrt * nt, &ptot, sh);
-  int rtot;
-  const int rt0 = block_exclusive_scan(nrt, &rtot, sh);
+  // pairs in the high half, row tiles in the low half: at most T*k <= 8192
+  // pairs and T*k/nt + E <= 1152 row tiles, so the halves never carry
+  int tot;
+  const int pre = block_exclusive_scan((c << 16) | nrt, &tot, sh);
+  const int off = pre >> 16, rt0 = pre & 0xFFFF;
+  const int seg = rt0 * nt;  // each expert's rows start at its first row tile
   if (e < E) {
     counts[e] = c;
     offsets[e] = off;
     seg_start[e] = seg;
     rt_base[e] = rt0;
+    soff[e] = off;
     for (int i = 0; i < nrt; ++i) {
       RowTile tl;
       tl.e = e;
@@ -215,25 +218,28 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
       tl.canon = off + nt * i;
       tiles[rt0 + i] = tl;
     }
-    int rank = 0;
-    for (int i = 0; i < W; ++i) {
-      uint32_t v = sbm[e * W + i];
-      while (v) {
-        int b = __ffs(v) - 1;
-        v &= v - 1;
-        int t = i * 32 + b;
-        int j = 0;
-        while (j < k && sidx[t * k + j] != e) ++j;
-        perm[off + rank] = t * k + j;
-        pair_pos[t * k + j] = off + rank;
-        ++rank;
-      }
-    }
   }
   if (e == 0) {
-    offsets[E] = tot;
-    seg_start[E] = ptot;
-    rt_base[E] = rtot;
+    offsets[E] = tot >> 16;
+    seg_start[E] = (tot & 0xFFFF) * nt;
+    rt_base[E] = tot & 0xFFFF;
+  }
+  __syncthreads();
+  // pair (t, j) of expert e: its rank is the number of e's tokens below t
+  // (a token's first slot holding e; later duplicates are not dispatched)
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const int ee = sidx[p];
+    if ((unsigned)ee >= (unsigned)E) continue;
+    const int t = p / k, j = p - t * k;
+    bool first = true;
+    for (int jj = 0; jj < j; ++jj) first = first && sidx[t * k + jj] != ee;
+    if (!first) continue;
+    const uint32_t* bm = sbm + ee * W;
+    int rank = __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
+    for (int i = 0; i < (t >> 5); ++i) rank += __popc(bm[i]);
+    const int pos = soff[ee] + rank;
+    perm[pos] = p;
+    pair_pos[p] = pos;
   }
 }
 
@@ -250,11 +256,11 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
                                   int32_t* perm, int32_t* pair_pos, int32_t* seg_start, RowTile* tiles,
                                   int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
   if (!dispatch_fits_one_cta(c)) return cudaErrorNotSupported;
-  const size_t smem = ((size_t)c.E * ((c.T + 31) / 32) + (size_t)c.T * c.k) * 4;
+  const size_t smem = ((size_t)c.E * ((c.T + 31) / 32) + (size_t)c.T * c.k + c.E) * 4;
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (kSmallWords + kSmallPairs) * 4);
+                                         (kSmallWords + kSmallPairs + kMaxE) * 4);
     if (e != cudaSuccess) return e;
     attr = true;
   }

@@ -156,6 +156,8 @@ constexpr int kMaxSplits = 24;
 // shared memory; then warp 0 runs k rounds of a warp arg-max over them (ties
 // in the key go to the lower expert index) and normalises the weights over
 // the winners in selection order.
+// KPL: keys per lane of the selection warp (E <= 32 KPL).
+template <int KPL>
 __global__ void __launch_bounds__(1024) k_router_topk(const float* __restrict__ part, int nsplit,
                                                       const float* __restrict__ bias, int T, int E, int k,
                                                       int bias_in_weights, float routed_scale,
@@ -182,16 +184,33 @@ __global__ void __launch_bounds__(1024) k_router_topk(const float* __restrict__ 
   }
   __syncthreads();
   if (threadIdx.x >= 32) return;
+  // warp 0: lane l holds the keys of experts l, l + 32, ... in registers and
+  // its best one; each round the warp takes the best of the lanes' bests (ties
+  // in the key go to the lower expert index) and only the winner's lane drops
+  // it and rescans its own keys
+  float kv[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) kv[i] = lane + 32 * i < E ? key[lane + 32 * i] : -INFINITY;
+  auto lane_best = [&](float& bv, int& be) {
+    bv = -INFINITY;
+    be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      if (32 * i >= E) break;
+      if (kv[i] > bv) {  // ascending index: the first of equal keys stays
+        bv = kv[i];
+        be = lane + 32 * i;
+      }
+    }
+  };
+  float lb;
+  int le;
+  lane_best(lb, le);
   float num = 0.0f;  // lane j keeps winner j's numerator
   int win = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int i = lane; i < E; i += 32)
-      if (key[i] > bv) {  // ascending index: the first of equal keys stays
-        bv = key[i];
-        be = i;
-      }
+    float bv = lb;
+    int be = le;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -206,9 +225,12 @@ __global__ void __launch_bounds__(1024) k_router_topk(const float* __restrict__ 
       win = be;
       num = bias_in_weights ? key[be] : sgm[be];
     }
-    __syncwarp();
-    if (lane == (be & 31)) key[be] = -INFINITY;
-    __syncwarp();
+    if (lane == (be & 31)) {
+#pragma unroll
+      for (int i = 0; i < KPL; ++i)
+        if (i == (be >> 5)) kv[i] = -INFINITY;
+      lane_best(lb, le);
+    }
   }
   float den = 0.0f;
   for (int j = 0; j < k; ++j) den = __fadd_rn(den, __shfl_sync(0xffffffffu, num, j));
@@ -262,8 +284,11 @@ cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __n
                  router_smem_bytes(4, 4), st, pdl, x, wr, logits, c.T, c.H, c.E, k_len, status);
   }
   if (e != cudaSuccess) return e;
-  return launch_k(k_router_topk, dim3(c.T), dim3((c.E + 31) / 32 * 32), (size_t)2 * c.E * 4, st, true,
-                  (const float*)logits, ns, bias, c.T, c.E, c.k, c.bias_in_weights, c.routed_scale, idx, w);
+  auto topk = c.E <= 128 ? k_router_topk<4> : c.E <= 256 ? k_router_topk<8> : c.E <= 512 ? k_router_topk<16>
+                                                                                  : k_router_topk<32>;
+  static_assert(32 * 32 >= kMaxE, "selection keys per lane");
+  return launch_k(topk, dim3(c.T), dim3((c.E + 31) / 32 * 32), (size_t)2 * c.E * 4, st, true, (const float*)logits,
+                  ns, bias, c.T, c.E, c.k, c.bias_in_weights, c.routed_scale, idx, w);
 }
 
 // ----------------------------------------------------------------------------

@@ -302,22 +302,28 @@ __device__ __forceinline__ void warp_argmax(float& v, int& e) {
   }
 }
 
+// KPL: experts per lane (E <= 32 KPL); lane l holds experts l, l + 32, ...
+template <int KPL>
 __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ wr, const float* __restrict__ lt,
     const float* __restrict__ wnorm, const float* __restrict__ bias, int T, int H, int E, int k,
     int bias_in_weights, float routed_scale, int32_t* __restrict__ idx, float* __restrict__ w) {
-  extern __shared__ float sel_smem[];  // per warp: lo[E], hi[E], ckey[E], cs[E], cid[E]
+  extern __shared__ float sel_smem[];  // per warp: ckey[E], cs[E], cid[E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kSelWarps + warp;
   pdl_wait();
   pdl_trigger();
   if (t >= T) return;  // whole warp
-  float* lo = sel_smem + (size_t)warp * 5 * E;
-  float* hi = lo + E;
-  float* ckey = hi + E;
+  float* ckey = sel_smem + (size_t)warp * 3 * E;
   float* cs = ckey + E;
   int* cid = reinterpret_cast<int*>(cs + E);
   const __nv_bfloat16* xr = x + (int64_t)t * H;
+
+  // this lane's tensor-core logits, requested together (they land while
+  // ||x|| is summed)
+  float ltv[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) ltv[i] = lane + 32 * i < E ? lt[(int64_t)t * E + lane + 32 * i] : 0.0f;
 
   // ||x|| (upper bound)
   float ss = 0.0f;
@@ -335,41 +341,62 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float xn = sqrtf(ss) * kNormInflate;
 
-  // approximate keys and their margins
-#pragma unroll 4
-  for (int e = lane; e < E; e += 32) {
-    const float a = __fadd_rn(router_sigmoid(lt[(int64_t)t * E + e]), bias[e]);
-    const float m = 0.25f * kTcGamma * xn * wnorm[e] + kKeySlack;
-    lo[e] = a - m;
-    hi[e] = a + m;
+  // approximate keys and their margins, in registers
+  float lov[KPL], hiv[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int e = lane + 32 * i;
+    lov[i] = -INFINITY;
+    hiv[i] = -INFINITY;
+    if (e < E) {
+      const float a = __fadd_rn(router_sigmoid(ltv[i]), bias[e]);
+      const float m = 0.25f * kTcGamma * xn * wnorm[e] + kKeySlack;
+      lov[i] = a - m;
+      hiv[i] = a + m;
+    }
   }
-  __syncwarp();
 
-  // L = k-th largest lower bound (the entries are consumed)
+  // L = k-th largest lower bound: each round the warp takes the best of the
+  // lanes' bests (ties to the lower expert index); only the winner's lane
+  // drops it and rescans its own bounds
+  float lb;
+  int le;
+  auto lane_best = [&]() {
+    lb = -INFINITY;
+    le = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      if (32 * i >= E) break;
+      if (lov[i] > lb) {
+        lb = lov[i];
+        le = lane + 32 * i;
+      }
+    }
+  };
+  lane_best();
   float L = -INFINITY;
   for (int r = 0; r < k; ++r) {
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-    for (int e = lane; e < E; e += 32)
-      if (lo[e] > bv) {
-        bv = lo[e];
-        be = e;
-      }
+    float bv = lb;
+    int be = le;
     warp_argmax(bv, be);
     L = bv;
-    __syncwarp();
-    if (be != 0x7fffffff && (be & 31) == lane) lo[be] = -INFINITY;
-    __syncwarp();
+    if (be != 0x7fffffff && (be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < KPL; ++i)
+        if (i == (be >> 5)) lov[i] = -INFINITY;
+      lane_best();
+    }
   }
 
   // candidates, in expert order
   int nc = 0;
-  for (int base = 0; base < E; base += 32) {
-    const int e = base + lane;
-    const bool cand = e < E && hi[e] >= L;
-    const unsigned b = __ballot_sync(0xffffffffu, cand);
-    if (cand) cid[nc + __popc(b & ((1u << lane) - 1u))] = e;
-    nc += __popc(b);
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    if (32 * i >= E) break;
+    const bool cand = lane + 32 * i < E && hiv[i] >= L;
+    const unsigned bal = __ballot_sync(0xffffffffu, cand);
+    if (cand) cid[nc + __popc(bal & ((1u << lane) - 1u))] = lane + 32 * i;
+    nc += __popc(bal);
   }
   __syncwarp();
 
@@ -440,12 +467,15 @@ cudaError_t launch_router_tc(const moe_config& c, const __nv_bfloat16* x, const 
                              const float* bias, float* scratch, int32_t* idx, float* w, uint32_t* status,
                              cudaStream_t st, bool pdl) {
   static bool attr = false;
-  const size_t sel_smem = (size_t)kSelWarps * 5 * c.E * 4;
+  const size_t sel_smem = (size_t)kSelWarps * 3 * c.E * 4;
+  auto select = c.E <= 128 ? k_router_select<4> : c.E <= 256 ? k_router_select<8>
+                : c.E <= 512 ? k_router_select<16> : k_router_select<32>;
+  static_assert(32 * 32 >= kMaxE, "selection experts per lane");
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_router_select, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSelWarps * 5 * kMaxE * 4);
+    for (auto kern : {k_router_select<4>, k_router_select<8>, k_router_select<16>, k_router_select<32>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelWarps * 3 * kMaxE * 4);
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -459,7 +489,7 @@ cudaError_t launch_router_tc(const moe_config& c, const __nv_bfloat16* x, const 
   e = launch_k(k_router_tc, dim3((c.E + 127) / 128, (c.T + 127) / 128), dim3(256), kRtSmem, st, true, tmx, tmw, lt,
                c.T, c.E, c.H, status, 4000000000LL);
   if (e != cudaSuccess) return e;
-  return launch_k(k_router_select, dim3((c.T + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32), sel_smem, st, true,
+  return launch_k(select, dim3((c.T + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32), sel_smem, st, true,
                   x, wr, (const float*)lt, (const float*)wnorm, bias, c.T, c.H, c.E, c.k, c.bias_in_weights,
                   c.routed_scale, idx, w);
 }

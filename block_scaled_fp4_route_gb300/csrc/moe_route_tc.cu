@@ -400,7 +400,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
   }
   __syncwarp();
 
-  // exact keys of the candidates: four at a time, the last one to three in a
+  // exact keys of the candidates: three at a time (larger groups measured
+  // slower: their registers cost resident warps), the last one or two in a
   // group of their own size (no padded dot products)
   auto exact_group = [&](auto g_tag, int i0) {
     constexpr int G = decltype(g_tag)::value;
@@ -418,9 +419,8 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
       }
   };
   int i0 = 0;
-  for (; i0 + 4 <= nc; i0 += 4) exact_group(std::integral_constant<int, 4>{}, i0);
-  if (nc - i0 == 3) exact_group(std::integral_constant<int, 3>{}, i0);
-  else if (nc - i0 == 2) exact_group(std::integral_constant<int, 2>{}, i0);
+  for (; i0 + 3 <= nc; i0 += 3) exact_group(std::integral_constant<int, 3>{}, i0);
+  if (nc - i0 == 2) exact_group(std::integral_constant<int, 2>{}, i0);
   else if (nc - i0 == 1) exact_group(std::integral_constant<int, 1>{}, i0);
   __syncwarp();
 

@@ -407,7 +407,11 @@ __global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __
   quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, sg, act_static != nullptr, codes, scales, glob, nt);
 }
 
-constexpr int kWarpRowsFrom = 2048;  // rows from which one warp per row is used
+constexpr int kWarpRowsFrom = 2048;  // x rows from which one warp per row is used
+// h rows from which one warp per row is used: a CTA for each of a few hundred
+// rows fills the SMs and holds back the down GEMM's CTAs (decode64: the layer
+// 2.8 us faster with warps)
+constexpr int kWarpRowsFromH = 256;
 
 // --- general API quantiser -------------------------------------------------
 __global__ void k_zero_f32(float* p, int64_t n) {
@@ -539,7 +543,7 @@ cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const in
                            const int32_t* perm, const int32_t* seg_start, uint8_t* codes, uint8_t* scales,
                            float* glob, const float* act_static, cudaStream_t st, bool pdl) {
   int P = c.T * c.k;
-  if (P >= kWarpRowsFrom) {
+  if (P >= kWarpRowsFromH) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((P + 7) / 8), dim3(256), 0, st, pdl, h, P, c.F, c.k, 1, c.mx_scale_mode, idx, offsets,
                     (const int32_t*)nullptr, perm, seg_start, codes, scales, glob, act_static, tile_rows(c));

@@ -356,14 +356,32 @@ __device__ __forceinline__ void quant_row_warp(const __nv_bfloat16* __restrict__
     } else {
       uint4 c[2];
       const uint32_t sc = mxfp8_block(v, mx_mode, c);
+      // the scales of lanes 4j .. 4j + 3 (four consecutive blocks) are four
+      // consecutive bytes of the scale layout: lane 4j stores them as one
+      // word (nb is a multiple of 4, so the four are valid together)
+      const uint32_t sw = sc | (__shfl_down_sync(0xffffffffu, sc, 1) << 8) |
+                          (__shfl_down_sync(0xffffffffu, sc, 2) << 16) | (__shfl_down_sync(0xffffffffu, sc, 3) << 24);
+      // the warp's 32 blocks are 1 KB of consecutive codes: lane L stores the
+      // 16 bytes at 16 L (half L & 1 of block L >> 1) and at 512 + 16 L (of
+      // block 16 + (L >> 1)), so that every store instruction writes 512
+      // consecutive bytes
+      const bool odd = lane & 1;
+      const int s0 = lane >> 1, s1 = 16 + (lane >> 1);
+      auto pick = [&](uint32_t lo, uint32_t hi, int src) {
+        const uint32_t a = __shfl_sync(0xffffffffu, lo, src), bb = __shfl_sync(0xffffffffu, hi, src);
+        return odd ? bb : a;
+      };
+      const uint4 w0 = make_uint4(pick(c[0].x, c[1].x, s0), pick(c[0].y, c[1].y, s0), pick(c[0].z, c[1].z, s0),
+                                  pick(c[0].w, c[1].w, s0));
+      const uint4 w1 = make_uint4(pick(c[0].x, c[1].x, s1), pick(c[0].y, c[1].y, s1), pick(c[0].z, c[1].z, s1),
+                                  pick(c[0].w, c[1].w, s1));
+      const bool in0 = b0 + s0 < nb, in1 = b0 + s1 < nb;
       for (int d = 0; d < ndst; ++d) {
         const int64_t rr = __shfl_sync(0xffffffffu, dst_lane, d);
-        if (in) {
-          uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b * 32);
-          o[0] = c[0];
-          o[1] = c[1];
-          scales[act_scale_offset(rr, b, nb, nt)] = (uint8_t)sc;
-        }
+        uint4* o = reinterpret_cast<uint4*>(codes + rr * cbytes + (int64_t)b0 * 32);
+        if (in0) o[lane] = w0;
+        if (in1) o[32 + lane] = w1;
+        if (in && (lane & 3) == 0) *reinterpret_cast<uint32_t*>(scales + act_scale_offset(rr, b, nb, nt)) = sw;
       }
     }
   }

@@ -35,6 +35,10 @@ SMALL = {
     "deep_nvfp4": dict(T=1200, H=512, E=4, k=2, F=256, fmt="nvfp4", seed=18, **U),
     "deep_mxfp8": dict(T=1100, H=384, E=5, k=3, F=384, fmt="mxfp8", seed=19, **U),
     "deep_hot_nvfp4": dict(T=1100, H=512, E=8, k=2, F=256, fmt="nvfp4", seed=20, outlier_frac=0.0, bias="hot"),
+    # T >= 2048: x quantised a warp per row, the row held in registers (H =
+    # 1024: four 32-lane slots; H = 384: the last slot half full)
+    "warp_x_nvfp4": dict(T=2100, H=1024, E=8, k=2, F=256, fmt="nvfp4", seed=21, **U),
+    "warp_x_mxfp8": dict(T=2080, H=384, E=6, k=3, F=128, fmt="mxfp8", seed=22, **U),
 }
 
 
@@ -110,6 +114,15 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
         # block scales.  Near-exact: the GEMM accumulation order differs from
         # the oracle's.
         h_in_ws = gw.layout["hq_codes"] > gw.layout["h_bf16"]
+        # NVFP4 with per-row globals: the row pass's codes, block scales and
+        # global of the GPU's own h rows, bit-exact against the oracle's
+        # quantiser of the same bf16 values
+        hq_exact = h_in_ws and gw.act_static is None
+        if hq_exact:
+            hqc = gw.ws_view("hq_codes", torch.uint8, R * (F // 2)).view(R, F // 2)
+            hqs = untile_scales(gw.ws_view("hq_scales", torch.uint8, (R // nt) * (F // 16 // 4) * 512).cpu().numpy(),
+                                R, F // 16, tile_rows=nt)
+            hqg = gw.ws_view("hq_global", torch.float32, R).cpu().numpy()
         if h_in_ws:
             hbuf = gw.ws_view("h_bf16", torch.int16, R * F).view(R, F)
         else:
@@ -125,6 +138,12 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
             gh = hbuf[torch.from_numpy(grow).cuda()].cpu().numpy()
             if h_in_ws:
                 flips += int((gh.view(np.uint16) != pr["h_bf16"]).sum())
+                if hq_exact:
+                    q = oracle.quantize("nvfp4", oracle.bf16_bits_to_f32(gh.view(np.uint16)))
+                    gi = torch.from_numpy(grow).cuda()
+                    assert np.array_equal(hqc[gi].cpu().numpy(), q[0])
+                    assert np.array_equal(hqs[grow], q[1])
+                    assert np.array_equal(hqg[grow].view(np.uint32), q[2].view(np.uint32))
             else:
                 flips += int((gh != pr["hq_codes"]).sum())
                 sflips += int((hs[grow] != pr["hq_sf"]).sum())

@@ -305,6 +305,19 @@ def main():
     value = job_tokens_per_s(T, args.steps, world, ms)
     launches_per_step = moe.moe_forward_kernel_count(gw.cfg)
 
+    # ---- distribution of single steps (an event between consecutive steps;
+    # the timed region above gives `value`) ----
+    n_dist = min(args.steps, 200)
+    sev = [torch.cuda.Event(enable_timing=True) for _ in range(n_dist + 1)]
+    sev[0].record(st)
+    for i in range(n_dist):
+        gw.forward()
+        sev[i + 1].record(st)
+    torch.cuda.synchronize()
+    step_us = np.array([sev[i].elapsed_time(sev[i + 1]) * 1e3 for i in range(n_dist)])
+    step_dist = {"steps": n_dist, "median": float(np.median(step_us)), "p10": float(np.percentile(step_us, 10)),
+                 "p90": float(np.percentile(step_us, 90))}
+
     # ---- per-stage device times (events between the stages, same stream) ----
     n_prof = min(args.steps, 200)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(n_prof)]
@@ -403,7 +416,7 @@ def main():
     layer = {"us_per_layer": ms_per_step * 1e3, "alg_bytes": layer_bytes,
              "hbm_frac_whole_layer": layer_bytes / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"],
              "tensor_frac_whole_layer": (g1_flops + g2_flops) / (ms_per_step / 1e3) / 1e12 / tpeak,
-             "stage_ms": stage_ms}
+             "step_us": step_dist, "stage_ms": stage_ms}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
     cpu = None

@@ -29,11 +29,11 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const float* __restric
   __syncthreads();
   for (int c = blockIdx.y * kCombThreads + threadIdx.x; c < H / 4; c += gridDim.y * kCombThreads) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int j0 = 0; j0 < k; j0 += 8) {  // slot order; 8 loads in flight per group
+  for (int j0 = 0; j0 < k; j0 += 8) {  // slot order; 8 loads in flight per group (read once: evict first)
     float4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (j0 + i < k) v[i] = reinterpret_cast<const float4*>(y + (int64_t)pos[j0 + i] * H)[c];
+      if (j0 + i < k) v[i] = __ldcs(reinterpret_cast<const float4*>(y + (int64_t)pos[j0 + i] * H) + c);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if (j0 + i < k) {

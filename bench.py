@@ -242,6 +242,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
+                    help="timed steps as CUDA-graph replays of captured moe_forward calls (default) or eager calls")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -283,6 +285,30 @@ def main():
     counts = gw.routing()["counts"]
     n_touched = int((counts > 0).sum())
 
+    # ---- the step as a serving loop runs it: moe_forward calls captured in a
+    # CUDA graph (G per graph), each a whole forward that reads its inputs ----
+    G = max(d for d in range(1, 21) if args.steps % d == 0)
+    graph = None
+    if args.launch == "graph":
+        side = torch.cuda.Stream()
+        side.wait_stream(st)
+        with torch.cuda.stream(side):
+            gw.forward()
+        st.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(G):
+                gw.forward()
+        graph.replay()
+        torch.cuda.synchronize()
+        status = moe.moe_poll_device_status(gw.ws)
+        if status != 0:
+            raise RuntimeError(f"device status {status} after the graph warm-up replay")
+        launch = f"cuda_graph: {G} moe_forward calls per graph, {args.steps // G} replays"
+    else:
+        launch = "eager: one moe_forward call per step"
+
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_index = int(vis.split(",")[local]) if vis else local
     clocks = ClockSampler(gpu_index)
@@ -294,8 +320,12 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     start.record(st)
-    for _ in range(args.steps):
-        gw.forward()
+    if graph is not None:
+        for _ in range(args.steps // G):
+            graph.replay()
+    else:
+        for _ in range(args.steps):
+            gw.forward()
     end.record(st)
     torch.cuda.synchronize()
     clocks.stop()
@@ -305,8 +335,8 @@ def main():
     value = job_tokens_per_s(T, args.steps, world, ms)
     launches_per_step = moe.moe_forward_kernel_count(gw.cfg)
 
-    # ---- distribution of single steps (an event between consecutive steps;
-    # the timed region above gives `value`) ----
+    # ---- distribution of single eager steps (an event between consecutive
+    # calls; the timed region above gives `value`) ----
     n_dist = min(args.steps, 200)
     sev = [torch.cuda.Event(enable_timing=True) for _ in range(n_dist + 1)]
     sev[0].record(st)
@@ -315,8 +345,8 @@ def main():
         sev[i + 1].record(st)
     torch.cuda.synchronize()
     step_us = np.array([sev[i].elapsed_time(sev[i + 1]) * 1e3 for i in range(n_dist)])
-    step_dist = {"steps": n_dist, "median": float(np.median(step_us)), "p10": float(np.percentile(step_us, 10)),
-                 "p90": float(np.percentile(step_us, 90))}
+    step_dist = {"steps": n_dist, "launch": "eager", "median": float(np.median(step_us)),
+                 "p10": float(np.percentile(step_us, 10)), "p90": float(np.percentile(step_us, 90))}
 
     # ---- per-stage device times (events between the stages, same stream) ----
     n_prof = min(args.steps, 200)
@@ -440,6 +470,7 @@ def main():
                 "vs_baseline": None, "dtype": w["fmt"], "data": "synthetic",
                 "config": {"workload": args.workload, "T": T, "H": w["H"], "E": w["E"], "k": k, "F": w["F"],
                            "fmt": w["fmt"], "touched_experts": n_touched, "parallelism": f"replicas{world}",
+                           "launch": launch,
                            "l2": f"inputs larger than L2: {layer_bytes / 1e9:.2f} GB of touched expert weights "
                                  f"per step against a 129 MB L2; no flush"},
                 "layer": layer, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,

@@ -392,7 +392,6 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   int32_t* offsets = at<int32_t>(ws_dev, L.offsets);
   int32_t* perm = at<int32_t>(ws_dev, L.perm);
   int32_t* pair_pos = at<int32_t>(ws_dev, L.pair_pos);
-  uint32_t* bm = at<uint32_t>(ws_dev, L.bitmap);
   float* y = at<float>(ws_dev, L.y_perm);
   mark(ev, 0, st);
   // the router's first kernel clears the status word of the call
@@ -402,7 +401,6 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   mark(ev, 1, st);
   s = dispatch_impl(c, idx, counts, offsets, perm, pair_pos, ws_dev, nullptr, st, true);
   if (s != MOE_OK) return s;
-  (void)bm;
   s = ffn_core(c, sms, (const __nv_bfloat16*)x_dev, idx, offsets, perm, pair_pos, gate, up, down, act_static, y, ws_dev,
                st, ev);
   if (s != MOE_OK) return s;

@@ -91,6 +91,7 @@ def lib():
 
 
 def library_path() -> str:
+    """Path of the in-tree libmoe.so (built by lib() when stale)."""
     return _build.LIB
 
 
@@ -116,12 +117,18 @@ def _stream(stream):
 
 def make_config(T, H, E, k, F, fmt, swiglu_cap=10.0, mx_scale_mode=0, bias_in_weights=0, routed_scale=1.0,
                 act_global_mode=0):
+    """A moe_config: T tokens, hidden H, E experts, top-k, FFN width F; fmt "nvfp4" / "mxfp8" (or
+    FMT_*); swiglu_cap c of c*tanh(v/c) (0 = none); mx_scale_mode 0 = OCP floor, 1 = round-up;
+    bias_in_weights 0 = the bias steers selection only; act_global_mode 1 = static per-expert NVFP4
+    activation globals."""
     if isinstance(fmt, str):
         fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
     return moe_config(T, H, E, k, F, fmt, swiglu_cap, act_global_mode, mx_scale_mode, bias_in_weights, routed_scale)
 
 
 def qweight(codes, scales, global_scale=None) -> moe_qweight:
+    """One quantised expert matrix for all experts: codes u8 [E, N, K/2] (NVFP4) or [E, N, K]
+    (MXFP8), block scales in the tiled layout, global_scale fp32 [E] (NVFP4) or None."""
     return moe_qweight(_ptr(codes), _ptr(scales), _ptr(global_scale))
 
 
@@ -130,24 +137,29 @@ def qweight(codes, scales, global_scale=None) -> moe_qweight:
 # ----------------------------------------------------------------------------
 
 def moe_workspace_size(cfg: moe_config) -> int:
+    """Bytes of device workspace every call with this configuration needs."""
     n = ctypes.c_size_t(0)
     _check("moe_workspace_size", lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)))
     return n.value
 
 
 def moe_forward_kernel_count(cfg: moe_config) -> int:
+    """Number of kernels one moe_forward launches for this configuration (host only)."""
     n = ctypes.c_int(0)
     _check("moe_forward_kernel_count", lib().moe_forward_kernel_count(ctypes.byref(cfg), ctypes.byref(n)))
     return n.value
 
 
 def moe_workspace_layout(cfg: moe_config) -> dict:
+    """Byte offsets of the intermediates inside the workspace, plus R and tile_rows."""
     L = moe_ws_layout()
     _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)))
     return {f: getattr(L, f) for f in ["R", "tile_rows"] + _LAYOUT_FIELDS}
 
 
 def moe_route(cfg, x, w_router, bias, topk_idx, topk_w, ws, stream=None):
+    """Router: x bf16 [T, H], w_router bf16 [E, H], bias fp32 [E] -> topk_idx int32 [T, k]
+    (descending key, ties to the lower expert) and topk_w fp32 [T, k]."""
     _check("moe_route", lib().moe_route(ctypes.byref(cfg), _ptr(x), _ptr(w_router), _ptr(bias), _ptr(topk_idx),
                                         _ptr(topk_w), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -161,6 +173,8 @@ def moe_route_noalloc(cfg, x, w_router, bias, topk_idx, topk_w, stream=None):
 
 
 def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None):
+    """Dispatch: counts int32 [E], offsets int32 [E + 1], perm int32 [T * k] (pairs t * k + j
+    sorted by expert, then token) and its inverse pair_pos int32 [T, k]; the tile plan goes to ws."""
     _check("moe_dispatch", lib().moe_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(counts), _ptr(offsets),
                                               _ptr(perm), _ptr(pair_pos), _ptr(ws), ws.numel() * ws.element_size(),
                                               _stream(stream)))
@@ -168,6 +182,8 @@ def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None
 
 def moe_expert_ffn(cfg, x, topk_idx, offsets, perm, pair_pos, gate, up, down, y_perm, ws, stream=None,
                    act_static_scales=None):
+    """Expert FFN of every pair: y_perm fp32 [T * k, H] (out), rows in dispatch order; gate / up /
+    down from qweight(); act_static_scales as for moe_forward."""
     _check("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(offsets),
                                                   _ptr(perm), _ptr(pair_pos), ctypes.byref(gate), ctypes.byref(up),
                                                   ctypes.byref(down), _ptr(act_static_scales), _ptr(y_perm),
@@ -175,6 +191,7 @@ def moe_expert_ffn(cfg, x, topk_idx, offsets, perm, pair_pos, gate, up, down, y_
 
 
 def moe_combine(cfg, y_perm, topk_w, pair_pos, out, stream=None):
+    """out bf16 [T, H] = sum over slots (in slot order, fp32) of topk_w * y_perm[pair_pos]."""
     _check("moe_combine", lib().moe_combine(ctypes.byref(cfg), _ptr(y_perm), _ptr(topk_w), _ptr(pair_pos),
                                             _ptr(out), _stream(stream)))
 
@@ -227,12 +244,15 @@ def moe_fake_quantize(fmt, src, out, global_scale=None, group_rows=0, mx_scale_m
 
 
 def moe_selftest_bounded_wait(cfg, gate, up, ws, limit_cycles, stream=None):
+    """Test hook: GEMM1 over the tile plan in ws with its loads withheld, so that every bounded wait
+    runs out after limit_cycles; moe_poll_device_status then reports the timeout."""
     _check("moe_selftest_bounded_wait", lib().moe_selftest_bounded_wait(
         ctypes.byref(cfg), ctypes.byref(gate), ctypes.byref(up), _ptr(ws), ws.numel() * ws.element_size(),
         limit_cycles, _stream(stream)))
 
 
 def moe_pack_scales(rowmajor, rows, scale_cols, tiled, stream=None):
+    """Row-major block scales -> the tiled layout the GEMMs read (rows % 128 == 0, scale_cols % 4 == 0)."""
     _check("moe_pack_scales", lib().moe_pack_scales(_ptr(rowmajor), rows, scale_cols, _ptr(tiled), _stream(stream)))
 
 
@@ -242,4 +262,5 @@ def moe_poll_device_status(ws, stream=None) -> int:
 
 
 def moe_status_string(status: int) -> str:
+    """The library's text for a status code."""
     return lib().moe_status_string(status).decode()

@@ -15,7 +15,9 @@ Every function is pinned by ``tests/test_oracle_pins.py``.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -29,16 +31,25 @@ _lib = None
 FMT_NVFP4, FMT_MXFP8 = 0, 1
 
 
+_CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math", "-fopenmp", "-fPIC", "-shared"]
+
+
 def build() -> str:
-    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    """Compile the oracle with gcc (no fast-math, no FMA contraction).  The
+    build is skipped only when a stamp beside the library holds the hash of
+    the source, the flags and the machine it was built for."""
     os.makedirs(_BUILD, exist_ok=True)
     out = os.path.join(_BUILD, "libmoe_oracle.so")
     src = os.path.join(_HERE, "moe_oracle.c")
-    if not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(src):
+    h = hashlib.sha256(open(src, "rb").read())
+    h.update(" ".join(_CFLAGS + [platform.machine()]).encode())
+    key, stamp = h.hexdigest(), out + ".key"
+    if not (os.path.exists(out) and os.path.exists(stamp) and open(stamp).read().strip() == key):
         tmp = out + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math",
-                               "-fopenmp", "-fPIC", "-shared", "-o", tmp, src, "-lm"])
+        subprocess.check_call(["gcc", *_CFLAGS, "-o", tmp, src, "-lm"])
         os.replace(tmp, out)
+        with open(stamp, "w") as f:
+            f.write(key + "\n")
     return out
 
 
@@ -288,12 +299,31 @@ def quantize_x(w: dict, x_bf16: np.ndarray, mx_mode: int = 0):
     return quantize(w["fmt"], bf16_bits_to_f32(x_bf16), per_tensor=False, mx_mode=mx_mode)
 
 
+def selected_weights(logits_row: np.ndarray, bias: np.ndarray, sel, bias_in_weights: bool = False,
+                     routed_scale: float = 1.0) -> np.ndarray:
+    """Routing weights of one token for a given ordered choice of experts
+    (used where a certified near-tie replaces the oracle's own choice):
+    routed_scale * v_j / sum_i v_i over the chosen experts, v = the sigmoid
+    score s (bias steers selection only) or the key s + b with
+    bias_in_weights.  The same rule as the selection's weights."""
+    sel = np.asarray(sel, np.int64)
+    s = 1.0 / (1.0 + np.exp(-np.asarray(logits_row, np.float64)[sel]))
+    v = s + np.asarray(bias, np.float32)[sel].astype(np.float64) if bias_in_weights else s
+    den = 0.0
+    for x in v:          # slot order, as the selection sums them
+        den += x
+    return routed_scale * (v / den)
+
+
 def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mode: int = 0,
-              expert_cache=None, keep_pairs: bool = False, inputs=None, max_pairs=None, act_static=None):
+              expert_cache=None, keep_pairs: bool = False, inputs=None, max_pairs=None, act_static=None,
+              bias_in_weights: bool = False, routed_scale: float = 1.0):
     """Run the whole layer for the given token rows (default: all T).
 
     idx_override: optional {token_row_index_in_sample: int32[k]} replacing the
-    oracle's own top-k for certified near-tie tokens.
+    oracle's own top-k for certified near-tie tokens (their weights follow
+    the same rule, selected_weights).
+    bias_in_weights, routed_scale: the router options of moe_config.
     expert_cache: optional dict e -> quantized_expert(...) to reuse encodings.
     inputs: optional (x rows of the tokens, W_r, bias) already generated.
     max_pairs: compute only the first max_pairs (token, slot) pairs of the
@@ -316,13 +346,12 @@ def moe_layer(w: dict, tokens=None, idx_override=None, cap: float = 10.0, mx_mod
         bias = synth.router_bias(w)
     else:
         x, wr, bias = inputs
-    r = route(x, wr, bias, k)
+    r = route(x, wr, bias, k, bias_in_weights, routed_scale)
     idx = r["idx"].copy()
     if idx_override:
         for i, sel in idx_override.items():
             idx[i] = np.asarray(sel, np.int32)
-            s = 1.0 / (1.0 + np.exp(-r["logits"][i, idx[i]]))
-            r["w"][i] = s / s.sum()
+            r["w"][i] = selected_weights(r["logits"][i], bias, idx[i], bias_in_weights, routed_scale)
     d = dispatch(idx, E)
     xq = quantize_x(w, x, mx_mode)
     a_all = decode(w["fmt"], *xq, per_tensor=False)

@@ -22,8 +22,10 @@ seeded tensors stand in for real activations and trained weights):
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import math
 import os
+import platform
 import subprocess
 import threading
 
@@ -76,6 +78,11 @@ WORKLOADS = {
 }
 
 
+def workload_spec(spec) -> dict:
+    """A workload dict: the name of one above, or a dict of the same keys."""
+    return dict(WORKLOADS[spec]) if isinstance(spec, str) else dict(spec)
+
+
 def inv_sqrt_f32(n: int) -> float:
     """fp32(1/sqrt(n)), computed in fp64 and rounded once."""
     return float(np.float32(1.0 / math.sqrt(n)))
@@ -85,30 +92,35 @@ def n_outliers(T: int, frac: float) -> int:
     return int(math.floor(frac * T + 0.5))
 
 
-def _build_host() -> str:
+def _build_one(out_name: str, src_name: str, cmd: list, libs=()) -> str:
+    """Build one library unless a stamp beside it holds the hash of its
+    sources, the command and the machine it was built for."""
     os.makedirs(_BUILD, exist_ok=True)
-    out = os.path.join(_BUILD, "libsynth_host.so")
-    src = os.path.join(_HERE, "synth_host.c")
-    hdr = os.path.join(_HERE, "synth_gen.h")
-    if (not os.path.exists(out) or os.path.getmtime(out) < max(os.path.getmtime(src), os.path.getmtime(hdr))):
+    out = os.path.join(_BUILD, out_name)
+    src = os.path.join(_HERE, src_name)
+    h = hashlib.sha256()
+    for f in (src, os.path.join(_HERE, "synth_gen.h")):
+        h.update(open(f, "rb").read())
+    h.update(" ".join(cmd + list(libs) + [platform.machine()]).encode())
+    key, stamp = h.hexdigest(), out + ".key"
+    if not (os.path.exists(out) and os.path.exists(stamp) and open(stamp).read().strip() == key):
         tmp = out + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fopenmp", "-fPIC",
-                               "-shared", "-o", tmp, src, "-lm"])
+        subprocess.check_call(cmd + ["-o", tmp, src] + list(libs))
         os.replace(tmp, out)
+        with open(stamp, "w") as f:
+            f.write(key + "\n")
     return out
+
+
+def _build_host() -> str:
+    return _build_one("libsynth_host.so", "synth_host.c",
+                      ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared"], libs=["-lm"])
 
 
 def _build_dev() -> str:
-    os.makedirs(_BUILD, exist_ok=True)
-    out = os.path.join(_BUILD, "libsynth_dev.so")
-    src = os.path.join(_HERE, "synth_dev.cu")
-    hdr = os.path.join(_HERE, "synth_gen.h")
-    if (not os.path.exists(out) or os.path.getmtime(out) < max(os.path.getmtime(src), os.path.getmtime(hdr))):
-        tmp = out + f".tmp{os.getpid()}"
-        subprocess.check_call(["nvcc", "-O3", "-gencode", "arch=compute_103a,code=sm_103a",
-                               "-Xcompiler", "-fPIC", "-shared", "-o", tmp, src])
-        os.replace(tmp, out)
-    return out
+    return _build_one("libsynth_dev.so", "synth_dev.cu",
+                      ["nvcc", "-O3", "-gencode", "arch=compute_103a,code=sm_103a", "-Xcompiler", "-fPIC",
+                       "-shared"])
 
 
 _host = None

@@ -12,12 +12,12 @@ import synth
 
 
 def workload(spec) -> dict:
-    return dict(synth.WORKLOADS[spec]) if isinstance(spec, str) else dict(spec)
+    return synth.workload_spec(spec)
 
 
 class GpuWorkload:
     def __init__(self, spec, torch, device="cuda", cap=10.0, mx_scale_mode=0, chunk_experts=8,
-                 with_weights=True, act_static=None):
+                 with_weights=True, act_static=None, bias_in_weights=0, routed_scale=1.0):
         import block_scaled_fp4_route_gb300 as moe
         self.torch = torch
         self.moe = moe
@@ -27,8 +27,10 @@ class GpuWorkload:
         # act_static: NVFP4 static activation globals fp32 [E, 2] (numpy), or None
         self.act_static = None if act_static is None else torch.from_numpy(
             np.ascontiguousarray(act_static, np.float32)).to(device)
+        self.route_opts = dict(bias_in_weights=bool(bias_in_weights), routed_scale=float(routed_scale))
         self.cfg = moe.make_config(T, H, E, k, F, w["fmt"], swiglu_cap=cap, mx_scale_mode=mx_scale_mode,
-                                   act_global_mode=0 if act_static is None else 1)
+                                   act_global_mode=0 if act_static is None else 1,
+                                   bias_in_weights=int(bias_in_weights), routed_scale=routed_scale)
         self.x = synth.dev_x(w, torch, device)
         self.w_router = synth.dev_router_weight(w, torch, device)
         self.bias = torch.from_numpy(synth.router_bias(w)).to(device)

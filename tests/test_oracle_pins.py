@@ -205,6 +205,24 @@ def test_router_worked_example():
         idx, w, keys = oracle.router_select(logits, bias, 2)
         assert list(idx[0]) == [int(s) for s in g[case + "_idx"]]
         assert np.allclose(w[0], [float(s) for s in g[case + "_w"]], rtol=0, atol=1e-7)
+    # case 1 under the two router options (weights worked by hand in the fixture)
+    logits = np.array([[float(s) for s in g["case1_logits"]]])
+    bias = np.array([float(s) for s in g["case1_bias"]], np.float32)
+    idx, w, _ = oracle.router_select(logits, bias, 2, bias_in_weights=True)
+    assert list(idx[0]) == [int(s) for s in g["case1_biw_idx"]]
+    # the fixture's bias is fp32(.3), fp32(.6): the keys carry its rounding (~1e-8)
+    assert np.allclose(w[0], [float(s) for s in g["case1_biw_w"]], rtol=0, atol=1e-7)
+    rs = float(g["case1_scaled_routed_scale"][0])
+    idx, w, _ = oracle.router_select(logits, bias, 2, routed_scale=rs)
+    assert list(idx[0]) == [int(s) for s in g["case1_idx"]]
+    assert np.allclose(w[0], [float(s) for s in g["case1_scaled_w"]], rtol=0, atol=1e-7)
+    # the weight rule for a given choice (near-tie overrides) is the
+    # selection's own: re-deriving case 1's weights from its choice
+    for biw in (False, True):
+        for scale in (1.0, rs):
+            idx, w, _ = oracle.router_select(logits, bias, 2, bias_in_weights=biw, routed_scale=scale)
+            assert np.allclose(oracle.selected_weights(logits[0], bias, idx[0], biw, scale), w[0],
+                               rtol=1e-15, atol=0)
 
 
 def test_router_logits_one_hot_and_brute_force():
@@ -350,9 +368,9 @@ def test_ffn_brute_force_tiny(fmt):
         assert np.allclose(res["y"], hdec @ Wd.T, rtol=1e-12, atol=1e-12)
 
 
-def test_moe_layer_tiny_pipeline_consistency():
-    # the assembled layer on the tiny workload: y of every pair equals the
-    # single-expert FFN, and out is the weighted sum in slot order
+def test_moe_layer_combine_is_the_weighted_slot_sum():
+    # the assembled layer on the tiny workload: out is the weighted sum of
+    # each token's pair rows in slot order (the combine's definition)
     w = synth.WORKLOADS["tiny_mxfp8"]
     res = oracle.moe_layer(w)
     T, k, H = w["T"], w["k"], w["H"]
@@ -364,6 +382,46 @@ def test_moe_layer_tiny_pipeline_consistency():
             acc += res["route"]["w"][t, j] * res["y"][d["pair_pos"][t, j]]
         assert np.array_equal(acc, res["out"][t])
     assert np.isfinite(res["out"]).all() and np.abs(res["out"]).max() > 0
+
+
+LAYER_PIN_SHAPES = {
+    "tiny_mxfp8": "tiny_mxfp8",
+    "ragged_nvfp4": dict(T=11, H=256, E=6, k=3, F=256, fmt="nvfp4", seed=41, outlier_frac=0.0, bias="uniform"),
+    "ragged_mxfp8_outliers": dict(T=13, H=256, E=5, k=2, F=128, fmt="mxfp8", seed=42, outlier_frac=0.1,
+                                  bias="uniform"),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_PIN_SHAPES))
+def test_moe_layer_pair_rows_rederived_token_by_token(name):
+    # The layer gathers each expert's pair rows through the dispatch order.
+    # Re-derive every pair without it, one (token, slot) at a time: the
+    # token's own x row quantised alone, the slot's expert from the router's
+    # choice, that expert's encoded weights and the single-pair FFN.  A wrong
+    # gather (the pair id instead of its token, the slot instead of the token,
+    # a transposed expert or segment) moves some y row to another token or
+    # expert and fails here.
+    w = synth.workload_spec(LAYER_PIN_SHAPES[name])
+    T, k, E = w["T"], w["k"], w["E"]
+    res = oracle.moe_layer(w)
+    r = oracle.route(synth.x_rows(w, np.arange(T)), synth.router_weight(w), synth.router_bias(w), k)
+    assert np.array_equal(res["idx"], r["idx"])
+    used = set()
+    for t in range(T):
+        xq = oracle.quantize_x(w, synth.x_rows(w, [t]))
+        a_t = oracle.decode(w["fmt"], *xq)
+        acc = np.zeros(w["H"])
+        for j in range(k):
+            e = int(r["idx"][t, j])
+            dec = oracle.decoded_expert(w, oracle.quantized_expert(w, e))
+            y = oracle.expert_ffn(w["fmt"], dec["gate"], dec["up"], dec["down"], a_t)["y"][0]
+            p = int(res["dispatch"]["pair_pos"][t, j])
+            assert res["dispatch"]["offsets"][e] <= p < res["dispatch"]["offsets"][e + 1]
+            assert np.array_equal(res["y"][p], y), (t, j, e)
+            used.add(p)
+            acc += r["w"][t, j] * y
+        assert np.array_equal(res["out"][t], acc)
+    assert used == set(range(T * k))
 
 
 # ----------------------------------------------------------------------------

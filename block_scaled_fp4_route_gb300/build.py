@@ -6,7 +6,9 @@ runtime dynamically so that it shares one runtime with PyTorch.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -17,7 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["moe_api.cu", "moe_route.cu", "moe_route_tc.cu", "moe_dispatch.cu", "moe_quant.cu", "moe_gemm.cu", "moe_combine.cu"]
+SOURCES = ["moe_api.cu", "moe_route.cu", "moe_route_tc.cu", "moe_dispatch.cu", "moe_quant.cu", "moe_gemm.cu", "moe_combine.cu",
+           "moe_kv.cu", "moe_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I" + INCLUDE]
@@ -30,16 +33,27 @@ def nvcc() -> str:
     return p
 
 
-def _deps_mtime() -> float:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "moe.h"), __file__]
-    return max(os.path.getmtime(f) for f in files)
+def _key(cc: str, defines=()) -> str:
+    """Hash of every source, the header, the flags and the host machine: a
+    library built from other sources, with other flags or for another
+    machine is rebuilt, whatever the file times say."""
+    h = hashlib.sha256()
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)) + [os.path.join(INCLUDE, "moe.h"), __file__]
+    for f in files:
+        h.update(os.path.basename(f).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join([cc, *ARCH, *NVCC_FLAGS, *defines, platform.machine()]).encode())
+    return h.hexdigest()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime():
-        return LIB
     cc = nvcc()
+    key = _key(cc)
+    stamp = LIB + ".key"
+    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read().strip() == key:
+        return LIB
 
     def one(src):
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
@@ -59,6 +73,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link of libmoe.so failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(stamp, "w") as fh:
+        fh.write(key + "\n")
     return LIB
 
 

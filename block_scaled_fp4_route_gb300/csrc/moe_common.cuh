@@ -8,9 +8,38 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "moe_internal.h"
 
 namespace moe {
+
+// ----------------------------------------------------------------------------
+// host: per-device one-time set-up (kernel attributes are per device)
+// ----------------------------------------------------------------------------
+struct PerDeviceOnce {
+  static constexpr int kMaxDevices = 64;
+  std::atomic<bool> done[kMaxDevices] = {};
+  std::mutex mu;
+};
+
+// Runs `fn` (returning cudaError_t) once for the current device; later calls
+// on that device return cudaSuccess without running it.  A failed `fn` is
+// retried on the next call.  Thread-safe.
+template <typename Fn>
+inline cudaError_t once_per_device(PerDeviceOnce& o, Fn fn) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= PerDeviceOnce::kMaxDevices) return cudaErrorInvalidDevice;
+  if (o.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lk(o.mu);
+  if (o.done[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  e = fn();
+  if (e == cudaSuccess) o.done[dev].store(true, std::memory_order_release);
+  return e;
+}
 
 // ----------------------------------------------------------------------------
 // status word bits written by kernels whose bounded waits ran out

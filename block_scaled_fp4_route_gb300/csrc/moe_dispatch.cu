@@ -257,13 +257,12 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
                                   int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
   if (!dispatch_fits_one_cta(c)) return cudaErrorNotSupported;
   const size_t smem = ((size_t)c.E * ((c.T + 31) / 32) + (size_t)c.T * c.k + c.E) * 4;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (kSmallWords + kSmallPairs + kMaxE) * 4);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t e = once_per_device(attr, [] {
+    return cudaFuncSetAttribute(k_dispatch_small, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (kSmallWords + kSmallPairs + kMaxE) * 4);
+  });
+  if (e != cudaSuccess) return e;
   return launch_k(k_dispatch_small, dim3(1), dim3(1024), smem, st, pdl, idx, c.T, c.k, c.E, counts, offsets, perm,
                   pair_pos, seg_start, tiles, rt_base, status, tile_rows(c));
 }

@@ -547,12 +547,10 @@ GemmArgs gemm_args(const GemmLaunch& g) {
 template <int FMT, bool GATED>
 cudaError_t launch_t(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   using C = Cfg<FMT, GATED>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t e = once_per_device(
+      attr, [] { return cudaFuncSetAttribute(k_moe_gemm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
+  if (e != cudaSuccess) return e;
   const GemmArgs a = gemm_args(g);
   return launch_k(k_moe_gemm<FMT, GATED>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
                   *g.tmB, a);
@@ -990,12 +988,10 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
 template <int FMT, bool GATED>
 cudaError_t launch_tm(const GemmLaunch& g, cudaStream_t st, bool pdl) {
   using C = CfgTM<FMT, GATED>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_moe_gemm_tm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDeviceOnce attr;
+  cudaError_t e = once_per_device(
+      attr, [] { return cudaFuncSetAttribute(k_moe_gemm_tm<FMT, GATED>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM); });
+  if (e != cudaSuccess) return e;
   const GemmArgs a = gemm_args(g);
   return launch_k(k_moe_gemm_tm<FMT, GATED>, dim3(g.num_sms), dim3(C::THREADS), C::SMEM, st, pdl, *g.tmA0, *g.tmA1,
                   *g.tmB, a);

@@ -263,19 +263,18 @@ cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __n
   if (router_uses_tc(c)) return launch_router_tc(c, x, wr, bias, logits, idx, w, status, st, pdl);
   const int ns = router_splits(c);
   const int k_len = c.H / ns;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDeviceOnce attr;
+  cudaError_t e = once_per_device(attr, [] {
+    cudaError_t r = cudaFuncSetAttribute(k_router_logits<4, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          router_smem_bytes(4, 4));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_router_logits<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(k_router_logits<1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                router_smem_bytes(1, 4));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+    return r;
+  });
+  if (e != cudaSuccess) return e;
   // token tiles of 16 rows for the smallest batches (a quarter of the FMAs
   // of the 64-row tile; every logit's arithmetic is the same)
-  cudaError_t e;
   if (c.T <= 16) {
     e = launch_k(k_router_logits<1, 4>, dim3((c.E + 63) / 64, 1, ns), dim3(256), router_smem_bytes(1, 4), st, pdl, x,
                  wr, logits, c.T, c.H, c.E, k_len, status);
@@ -348,6 +347,15 @@ moe_status noalloc_setup(float** scratch) {
 }  // namespace
 
 }  // namespace moe
+
+extern "C" moe_status moe_route_noalloc_poll_status(void* stream) {
+  using namespace moe;
+  float* scratch = nullptr;
+  moe_status s = noalloc_setup(&scratch);
+  if (s != MOE_OK) return s;
+  // the status word is the first word of the array's header area
+  return moe_poll_device_status(scratch, stream);
+}
 
 extern "C" moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                                         const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,

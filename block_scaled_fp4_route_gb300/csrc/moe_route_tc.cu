@@ -466,19 +466,19 @@ size_t router_tc_scratch_floats(const moe_config& c) {
 cudaError_t launch_router_tc(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr,
                              const float* bias, float* scratch, int32_t* idx, float* w, uint32_t* status,
                              cudaStream_t st, bool pdl) {
-  static bool attr = false;
+  static PerDeviceOnce attr;
   const size_t sel_smem = (size_t)kSelWarps * 3 * c.E * 4;
   auto select = c.E <= 128 ? k_router_select<4> : c.E <= 256 ? k_router_select<8>
                 : c.E <= 512 ? k_router_select<16> : k_router_select<32>;
   static_assert(32 * 32 >= kMaxE, "selection experts per lane");
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+  cudaError_t ea = once_per_device(attr, [] {
+    cudaError_t r = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
     for (auto kern : {k_router_select<4>, k_router_select<8>, k_router_select<16>, k_router_select<32>})
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelWarps * 3 * kMaxE * 4);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+      if (r == cudaSuccess)
+        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelWarps * 3 * kMaxE * 4);
+    return r;
+  });
+  if (ea != cudaSuccess) return ea;
   CUtensorMap tmx, tmw;
   if (!make_map(&tmx, x, c.T, (int64_t)c.H * 2, 128) || !make_map(&tmw, wr, c.E, (int64_t)c.H * 2, 128))
     return cudaErrorInvalidValue;

@@ -142,3 +142,43 @@ def test_forward_kernel_count():
     assert moe.moe_forward_kernel_count(cfg(T=4096, E=376)) == 10  # E % 16 != 0: CUDA-core router
     with pytest.raises(moe.MoeError):
         moe.moe_forward_kernel_count(cfg(T=0))
+
+
+def test_noalloc_router_refuses_batches_beyond_its_scratch_before_any_launch():
+    # moe_route_noalloc's fixed scratch holds 2^20 floats: a 64-float status
+    # area, then the router's scratch.  For T > 256 (tensor-core router) that
+    # is the logits [T, E] and ||w_e|| padded to 64: at E = 384 the largest
+    # batch is T = 2729 (64 + 2729*384 + 384 = 1,048,384 <= 1,048,576), and
+    # T = 2730 needs 1,048,768.  The refusal comes before the device is
+    # touched (these addresses are never dereferenced).
+    ok = FakeTensor(0x10000)
+    for T in (2730, 4096):
+        with pytest.raises(moe.MoeError) as ei:
+            moe.moe_route_noalloc(cfg(T=T), ok, ok, ok, ok, ok, stream=0)
+        assert ei.value.status == 4
+    assert 64 + 2729 * 384 + 384 <= 1 << 20 < 64 + 2730 * 384 + 384
+    # E not a multiple of 16: the CUDA-core router (one K split above 256
+    # tokens), 64 + T*E floats; E = 376: T <= 2788
+    with pytest.raises(moe.MoeError) as ei:
+        moe.moe_route_noalloc(cfg(T=2789, E=376), ok, ok, ok, ok, ok, stream=0)
+    assert ei.value.status == 4
+    assert 64 + 2788 * 376 <= 1 << 20 < 64 + 2789 * 376
+    with pytest.raises(moe.MoeError) as ei:   # pointers are validated first
+        moe.moe_route_noalloc(cfg(T=64), ok, ok, FakeTensor(0x10004), ok, ok, stream=0)
+    assert ei.value.status == 3
+
+
+def test_kv_quantize_validation_without_a_device():
+    L = moe.lib()
+    ok = 0x10000
+    call = lambda **kw: L.moe_kv_quantize_mxfp8(*[kw.get(n, d) for n, d in [
+        ("kv", ok), ("tokens", 16), ("heads", 8), ("head_dim", 128), ("stride", 8 * 128), ("slot", None),
+        ("num_slots", 16), ("mode", 0), ("codes", ok), ("scales", ok), ("stream", None)]])
+    assert call(head_dim=100) == 2 and call(head_dim=16) == 2 and call(head_dim=2048) == 2
+    assert call(stride=8 * 128 - 8) == 2 and call(stride=8 * 128 + 4) == 2
+    assert call(heads=0) == 2 and call(tokens=-1) == 2
+    assert call(mode=2) == 1
+    assert call(num_slots=15) == 1                  # identity slots need num_slots >= tokens
+    assert call(tokens=0) == 0                      # nothing to do, nothing enqueued
+    assert call(kv=ok + 8) == 3 and call(codes=ok + 4) == 3 and call(scales=None) == 1
+    assert call(slot=ok + 4) == 3                   # int64 slots, 8-byte aligned

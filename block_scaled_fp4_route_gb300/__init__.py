@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
-            "moe_route_noalloc", "moe_fake_quantize", "moe_selftest_bounded_wait", "moe_forward_kernel_count",
+            "moe_route_noalloc", "moe_route_noalloc_poll_status", "moe_fake_quantize", "moe_kv_quantize_mxfp8", "moe_bench_mma_peak", "moe_selftest_bounded_wait", "moe_forward_kernel_count",
             "moe_status_string"]
 
 
@@ -69,6 +69,7 @@ def lib():
             L.moe_workspace_size.argtypes = [cfgp, ctypes.POINTER(sz)]
             L.moe_route.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
             L.moe_route_noalloc.argtypes = [cfgp, P, P, P, P, P, P]
+            L.moe_route_noalloc_poll_status.argtypes = [P]
             L.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
             L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, P, sz, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
@@ -79,6 +80,10 @@ def lib():
                                        P, P, P, P]
             L.moe_pack_scales.argtypes = [P, i64, i64, P, P]
             L.moe_fake_quantize.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, P, i64, i64, i64, P, P, P]
+            L.moe_kv_quantize_mxfp8.argtypes = [P, i64, ctypes.c_int, ctypes.c_int, i64, P, i64, ctypes.c_int, P, P,
+                                                P]
+            L.moe_bench_mma_peak.argtypes = [ctypes.c_int, i64, P, P, ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_double), P]
             L.moe_selftest_bounded_wait.argtypes = [cfgp, qwp, qwp, P, sz, i64, P]
             L.moe_poll_device_status.argtypes = [P, P]
             L.moe_workspace_layout.argtypes = [cfgp, ctypes.POINTER(moe_ws_layout)]
@@ -172,6 +177,13 @@ def moe_route_noalloc(cfg, x, w_router, bias, topk_idx, topk_w, stream=None):
                                                         _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
 
 
+def moe_route_noalloc_poll_status(stream=None) -> int:
+    """Synchronises the stream; the status of the allocation-free router's
+    last calls on the current device (0 = no timeout; 7 = a bounded wait ran
+    out), cleared by the read."""
+    return int(lib().moe_route_noalloc_poll_status(_stream(stream)))
+
+
 def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None):
     """Dispatch: counts int32 [E], offsets int32 [E + 1], perm int32 [T * k] (pairs t * k + j
     sorted by expert, then token) and its inverse pair_pos int32 [T, k]; the tile plan goes to ws."""
@@ -241,6 +253,32 @@ def moe_fake_quantize(fmt, src, out, global_scale=None, group_rows=0, mx_scale_m
     _check("moe_fake_quantize", lib().moe_fake_quantize(fmt, mx_scale_mode, int(src.dtype == torch.float32), _ptr(src),
                                                         rows, cols, group_rows, _ptr(out), _ptr(global_scale),
                                                         _stream(stream)))
+
+
+def moe_kv_quantize_mxfp8(kv, codes, scales, slots=None, token_stride=None, mx_scale_mode=0, stream=None):
+    """New K or V rows kv bf16 [tokens, heads, head_dim] (a view whose token
+    stride may exceed heads * head_dim) -> MXFP8 cache codes u8
+    [num_slots, heads, head_dim] and E8M0 scales u8 [num_slots, heads,
+    head_dim / 32] at slots int64 [tokens] (None: slot t; negative: skipped)."""
+    tokens, heads, head_dim = kv.shape
+    if token_stride is None:
+        token_stride = kv.stride(0)
+    num_slots = codes.shape[0]
+    _check("moe_kv_quantize_mxfp8", lib().moe_kv_quantize_mxfp8(
+        _ptr(kv), tokens, heads, head_dim, token_stride, _ptr(slots), num_slots, mx_scale_mode, _ptr(codes),
+        _ptr(scales), _stream(stream)))
+
+
+def moe_bench_mma_peak(fmt, mmas_per_cta, status, cycles=None, stream=None):
+    """Launch the block-scaled MMA peak kernel (one CTA per SM, operands on
+    chip); returns (ctas, flops_per_mma).  status: a device int32 tensor of
+    >= 1 element; cycles: None or a device int64 tensor of >= ctas elements."""
+    if isinstance(fmt, str):
+        fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
+    n, f = ctypes.c_int(0), ctypes.c_double(0.0)
+    _check("moe_bench_mma_peak", lib().moe_bench_mma_peak(fmt, mmas_per_cta, _ptr(cycles), _ptr(status),
+                                                          ctypes.byref(n), ctypes.byref(f), _stream(stream)))
+    return n.value, f.value
 
 
 def moe_selftest_bounded_wait(cfg, gate, up, ws, limit_cycles, stream=None):

@@ -501,6 +501,44 @@ moe_status moe_fake_quantize(moe_format fmt, int mx_scale_mode, int src_is_fp32,
                                        global_dev, (cudaStream_t)stream));
 }
 
+moe_status moe_kv_quantize_mxfp8(const void* kv_dev, int64_t tokens, int heads, int head_dim, int64_t token_stride,
+                                 const int64_t* slot_dev, int64_t num_slots, int mx_scale_mode, void* codes_dev,
+                                 void* scales_dev, void* stream) {
+  if (tokens < 0 || tokens > (int64_t)INT32_MAX || heads < 1 || heads > 4096 || head_dim < 32 || head_dim > 1024 ||
+      head_dim % 32 != 0)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (token_stride < (int64_t)heads * head_dim || token_stride % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (mx_scale_mode != 0 && mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;
+  if (num_slots < 0 || (!slot_dev && num_slots < tokens)) return MOE_ERR_INVALID_ARG;
+  if (tokens == 0) return MOE_OK;
+  moe_status s = check_ptrs({kv_dev, codes_dev});
+  if (s == MOE_OK && !scales_dev) s = MOE_ERR_INVALID_ARG;
+  if (s == MOE_OK && slot_dev && (reinterpret_cast<uintptr_t>(slot_dev) & 7u) != 0) s = MOE_ERR_MISALIGNED;
+  int sms = 0;
+  if (s == MOE_OK) s = device_check(&sms);
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_kv_quant_mxfp8((const __nv_bfloat16*)kv_dev, tokens, heads, head_dim, token_stride,
+                                           slot_dev, num_slots, mx_scale_mode, (uint8_t*)codes_dev,
+                                           (uint8_t*)scales_dev, sms, (cudaStream_t)stream));
+}
+
+moe_status moe_bench_mma_peak(moe_format fmt, int64_t mmas_per_cta, unsigned long long* cycles_dev, void* status_dev,
+                              int* ctas, double* flops_per_mma, void* stream) {
+  if (fmt != MOE_FMT_NVFP4 && fmt != MOE_FMT_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (mmas_per_cta < 4 || mmas_per_cta % 4 != 0 || mmas_per_cta > ((int64_t)1 << 40)) return MOE_ERR_INVALID_ARG;
+  if (!status_dev || !ctas || !flops_per_mma) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(status_dev) & 3u) != 0 || (reinterpret_cast<uintptr_t>(cycles_dev) & 7u) != 0)
+    return MOE_ERR_MISALIGNED;
+  int sms = 0;
+  moe_status s = device_check(&sms);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(status_dev, 0, 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+  *ctas = sms;
+  *flops_per_mma = (double)mma_peak_flops_per_mma(fmt);
+  return cuda_status(launch_mma_peak(fmt, sms, mmas_per_cta, cycles_dev, (uint32_t*)status_dev, st));
+}
+
 moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qweight* gate, const moe_qweight* up,
                                      void* ws_dev, size_t ws_bytes, int64_t limit_cycles, void* stream) {
   moe_status s = check_cfg(cfg);

@@ -117,6 +117,18 @@ cudaError_t launch_pack_scales(const uint8_t* src, int64_t rows, int64_t cols, u
 cudaError_t launch_fake_quant(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,
                               int64_t group_rows, float* out, float* glob, cudaStream_t st);
 
+// MXFP8 KV-cache rows: bf16 [tokens, heads, head_dim] (token stride in
+// elements) -> codes [num_slots, heads, head_dim], E8M0 scales
+// [num_slots, heads, head_dim/32] at slot[t] (nullptr: slot t).
+cudaError_t launch_kv_quant_mxfp8(const __nv_bfloat16* kv, int64_t tokens, int heads, int head_dim,
+                                  int64_t token_stride, const int64_t* slot, int64_t num_slots, int mode,
+                                  uint8_t* codes, uint8_t* scales, int sms, cudaStream_t st);
+
+// Tensor-core peak microbenchmark (one CTA per SM; n_mma MMAs each).
+int mma_peak_flops_per_mma(moe_format fmt);
+cudaError_t launch_mma_peak(moe_format fmt, int ctas, long long n_mma, unsigned long long* cycles, uint32_t* status,
+                            cudaStream_t st);
+
 struct GemmLaunch {
   const moe_config* cfg;
   bool gated;          // GEMM1 (gate+up, SwiGLU epilogue) vs GEMM2 (down)

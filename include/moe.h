@@ -19,7 +19,10 @@
  * Conventions for every call:
  *   - Pointers named *_dev are device pointers; the caller owns every buffer,
  *     the workspace and the stream.  The library allocates no device memory
- *     and keeps no state besides cached device attributes.
+ *     and keeps no state besides per-device set-up done on first use (kernel
+ *     shared-memory limits, the device address of moe_route_noalloc's
+ *     scratch).  That set-up belongs to the device's current context: after
+ *     cudaDeviceReset the library must not be called again in the process.
  *   - Calls are asynchronous on `stream` (a cudaStream_t, passed as void*).
  *   - On invalid arguments a call returns a non-zero status and enqueues
  *     nothing.  Checks: shapes (see moe_config), 16-byte alignment of every
@@ -157,19 +160,29 @@ MOE_API moe_status moe_route(const moe_config* cfg, const void* x_dev, const voi
  *   Its scratch (a status word area and the fp32 logits) is a fixed 4 MiB
  *   array inside the library, reserved on every device that loads the
  *   library until the process exits.  Configurations whose scratch does not
- *   fit return MOE_ERR_WORKSPACE_TOO_SMALL: 64 + splits * T * E <= 2^20
- *   floats, where splits is the largest s <= 24 (T <= 64) or <= 8 (T <= 256)
- *   with H % (64*s) == 0; for T > 256 with E % 16 == 0, 64 + T * E +
- *   ceil(E/64)*64 <= 2^20 (e.g. T <= 2560 at E = 384); e.g. every T <= 256 at
- *   E = 384, H = 4608.
+ *   fit return MOE_ERR_WORKSPACE_TOO_SMALL before anything is enqueued:
+ *     T <= 256 (CUDA-core router): 64 + splits * T * E <= 2^20 floats, where
+ *       splits is the largest s <= 24 (T <= 64) or <= 8 (T <= 256) with
+ *       H % (64*s) == 0; every T <= 256 fits at E = 384, H = 4608;
+ *     T > 256 with E % 16 == 0 and H % 64 == 0 (tensor-core router):
+ *       64 + T * E + ceil(E/64)*64 <= 2^20; at E = 384 exactly T <= 2729.
  *   The first call on a device looks up the array's device address; make that
  *   first call before any stream capture.
  *   Every call uses the same array: calls that may overlap on the GPU (other
  *   streams, other threads) race and must be serialised by the caller.  No
- *   call allocates or frees memory. */
+ *   call allocates or frees memory.
+ *   A bounded wait of the tensor-core router that ran out is recorded in the
+ *   array's status word: moe_route_noalloc_poll_status reads it. */
 MOE_API moe_status moe_route_noalloc(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
                                      const float* bias_dev, int32_t* topk_idx_dev, float* topk_w_dev,
                                      void* stream);
+
+/* Status of the last moe_route_noalloc call(s) on the current device:
+ * synchronises `stream`, reads and clears the status word of the library's
+ * fixed router scratch.  Returns MOE_ERR_DEVICE_TIMEOUT if a bounded wait ran
+ * out (topk_idx / topk_w are then unspecified), MOE_OK otherwise.  Allocates
+ * nothing. */
+MOE_API moe_status moe_route_noalloc_poll_status(void* stream);
 
 /* Token dispatch [CB MegaMoE: dispatch is a step of the fused unit]: groups
  * the P = T*k pairs (t, j)
@@ -279,6 +292,28 @@ MOE_API moe_status moe_fake_quantize(moe_format fmt, int mx_scale_mode, int src_
                                      int64_t rows, int64_t cols, int64_t group_rows, float* out_dev,
                                      float* global_dev, void* stream);
 
+/* MXFP8 KV-cache quantiser [SGL features table: a block-scaled MXFP8 KV cache
+ * on Blackwell]: the new K (or V) rows of a batch are encoded along head_dim
+ * with the layer's MXFP8 rule (32-element blocks, E8M0 scale as
+ * mx_scale_mode, E4M3 codes, round to nearest even, saturating) and written to
+ * their slots of a cache.
+ *   kv_dev       bf16 [tokens, heads, head_dim]; token t's row starts at
+ *                element t * token_stride (token_stride >= heads * head_dim,
+ *                a multiple of 8, e.g. K inside a fused [tokens, 3, heads,
+ *                head_dim] projection); 16-byte aligned.
+ *   slot_dev     int64 [tokens] (nullable, 8-byte aligned): the cache slot of
+ *                token t; slots < 0 or >= num_slots are skipped (padding
+ *                tokens).  NULL: token t goes to slot t (num_slots >= tokens).
+ *   codes_dev    u8 E4M3 [num_slots, heads, head_dim] (16-byte aligned)
+ *   scales_dev   u8 E8M0 [num_slots, heads, head_dim / 32]
+ *   value = e4m3(code) * 2^(scale - 127); an all-zero block has scale 0.
+ * head_dim % 32 == 0, 32..1024; heads 1..4096; tokens 0..2^31-1 (0 enqueues
+ * nothing).  Slots of other tokens are left untouched; two tokens mapped to
+ * one slot race. */
+MOE_API moe_status moe_kv_quantize_mxfp8(const void* kv_dev, int64_t tokens, int heads, int head_dim,
+                                         int64_t token_stride, const int64_t* slot_dev, int64_t num_slots,
+                                         int mx_scale_mode, void* codes_dev, void* scales_dev, void* stream);
+
 /* ROWMAJOR -> TILED scale re-layout (rows % 128 == 0, scale columns % 4 == 0). */
 MOE_API moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64_t scale_cols, void* tiled_dev,
                            void* stream);
@@ -286,6 +321,24 @@ MOE_API moe_status moe_pack_scales(const void* rowmajor_dev, int64_t rows, int64
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns MOE_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out. */
 MOE_API moe_status moe_poll_device_status(void* ws_dev, void* stream);
+
+/* Block-scaled tensor-core peak, measured [TS serving section: the expert
+ * GEMMs run on block-scaled tensor cores; the prefill roofline divides by
+ * this rate].  Launches one CTA on every SM (*ctas receives the count); each
+ * issues mmas_per_cta (a multiple of 4) back-to-back tcgen05 block-scaled
+ * MMAs of M = 128, N = 256 from one thread into one TMEM accumulator, the
+ * operands and scales resident in shared memory and TMEM (no global memory
+ * traffic): NVFP4 kind::mxf4nvf4 scale_vec::4X (K = 64), MXFP8
+ * kind::mxf8f6f4 scale_vec::1X (K = 32), the forms the expert GEMMs issue.
+ * *flops_per_mma receives 2*128*256*K.  The caller times the launch with
+ * events on `stream`: rate = ctas * mmas_per_cta * flops_per_mma / time.
+ *   cycles_dev   u64 [*ctas] (nullable): each CTA's SM cycles from its first
+ *                MMA to the completion of its last
+ *   status_dev   a 4-byte word (4-byte aligned), cleared here; a bounded wait
+ *                that ran out sets it (read it with moe_poll_device_status).
+ * Allocates nothing. */
+MOE_API moe_status moe_bench_mma_peak(moe_format fmt, int64_t mmas_per_cta, unsigned long long* cycles_dev,
+                                      void* status_dev, int* ctas, double* flops_per_mma, void* stream);
 
 /* Test hook for the device-side failure detection: launches the gate/up GEMM
  * over the tile plan already in the workspace (a moe_forward or

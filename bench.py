@@ -2,7 +2,12 @@
 
 One step = one moe_forward over one seeded token batch (router, dispatch,
 activation quantisation, GEMM1 + capped SwiGLU, h quantisation, GEMM2,
-combine), inputs resident in HBM.  Prints one JSON line.
+combine), inputs resident in HBM.  Prints one JSON line.  The line's workload
+is the largest single-GPU configuration (a 16384-token MXFP8 prefill chunk
+with Zipf-skewed expert load); the other configurations (the tiny case, the
+64- and 192-token decode batches, the 4096-token NVFP4 prefill chunk) are
+measured in the same run under `per_workload`.  The tensor-core roofs are the
+block-scaled MMA rates measured in the same run (moe_bench_mma_peak).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
@@ -28,13 +33,18 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = ("MoE-layer tokens/s & µs/layer; % HBM roofline (decode) / % FP4-FP8 peak (prefill)")
-DEFAULT_WORKLOAD = "decode64_nvfp4"
+DEFAULT_WORKLOAD = "prefill16384_mxfp8_zipf"
+# the other configurations, measured beside the line's (timed steps, CPU work
+# kept small): name -> steps
+PER_WORKLOAD = {"tiny_mxfp8": 2000, "decode64_nvfp4": 1000, "decode192_mxfp8_outliers": 500,
+                "prefill4096_nvfp4": 200}
 UNIT = "tokens/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
 
 
 # dense tensor-core peak per dtype relative to bf16 (nominal GB300 figures:
-# 2.25 PFLOP/s bf16, 4.5 fp8, 13.5 fp4)
+# 2.25 PFLOP/s bf16, 4.5 fp8, 13.5 fp4); used only if the measurement of the
+# block-scaled MMA rate is switched off
 TENSOR_RATIO = {"nvfp4": 13.5 / 2.25, "mxfp8": 4.5 / 2.25}
 
 
@@ -230,6 +240,183 @@ def run_reference(args):
 
 
 # ----------------------------------------------------------------------------
+# measured block-scaled tensor-core rates (moe_bench_mma_peak)
+# ----------------------------------------------------------------------------
+
+def measure_tensor_peaks(moe, torch, gpu_index: int, burst_s: float = 0.1, sustained_s: float = 2.0):
+    """Dense block-scaled MMA rate of this GPU per format, measured with the
+    same MMA forms the expert GEMMs issue (one CTA per SM, operands on chip,
+    no HBM traffic): `burst` = one launch of ~burst_s after a warm-up launch,
+    `sustained` = back-to-back launches for ~sustained_s (the power cap's
+    steady state, the right denominator for a kernel timed inside a long
+    step), each with the SM clock sampled while it ran."""
+    out = {}
+    st = torch.cuda.current_stream()
+    status = torch.zeros(64, dtype=torch.int32, device="cuda")
+    for fmt in ("nvfp4", "mxfp8"):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+        def timed(n, reps):
+            ev[0].record(st)
+            for _ in range(reps):
+                ctas, fpm = moe.moe_bench_mma_peak(fmt, n, status)
+            ev[1].record(st)
+            torch.cuda.synchronize()
+            if moe.moe_poll_device_status(status) != 0:
+                raise RuntimeError(f"tensor-core peak kernel ({fmt}): a bounded wait ran out")
+            return ev[0].elapsed_time(ev[1]) * 1e-3, ctas, fpm
+
+        n = 1 << 14
+        t, ctas, fpm = timed(n, 1)
+        n = max(4, int(n * burst_s / max(t, 1e-6)) // 4 * 4)
+        timed(n, 1)                                   # warm-up at the burst length
+        clk = ClockSampler(gpu_index)
+        time.sleep(0.3)
+        clk.start()
+        tb, ctas, fpm = timed(n, 1)
+        clk.stop()
+        burst = {"tflops": ctas * n * fpm / tb / 1e12, "seconds": tb, "clocks": clk.summary()}
+        reps = max(1, int(round(sustained_s / tb)))
+        clk = ClockSampler(gpu_index)
+        time.sleep(0.3)
+        clk.start()
+        ts, ctas, fpm = timed(n, reps)
+        clk.stop()
+        sus = {"tflops": ctas * n * fpm * reps / ts / 1e12, "seconds": ts, "clocks": clk.summary()}
+        out[fmt] = {"burst": burst, "sustained": sus, "ctas": ctas, "mmas_per_cta": n, "flops_per_mma": fpm,
+                    "mma": "tcgen05 M=128 N=256 K=%d %s" % (64 if fmt == "nvfp4" else 32,
+                                                          "kind::mxf4nvf4 scale_vec::4X" if fmt == "nvfp4"
+                                                          else "kind::mxf8f6f4 scale_vec::1X")}
+    return out
+
+
+# ----------------------------------------------------------------------------
+# one workload on the GPU
+# ----------------------------------------------------------------------------
+
+def capture_graph(torch, gw, G: int):
+    """G moe_forward calls captured in one CUDA graph (a serving loop's
+    decode step); each captured call reads its inputs on every replay."""
+    st = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(st)
+    with torch.cuda.stream(side):
+        gw.forward()
+    st.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(G):
+            gw.forward()
+    graph.replay()
+    torch.cuda.synchronize()
+    return graph
+
+
+def stage_times(moe, torch, gw, n: int) -> dict:
+    """Mean device time of each stage (events between the stages of
+    moe_forward_profiled, same stream) over n calls."""
+    st = torch.cuda.current_stream()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(n)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(st)
+    for i in range(n):
+        moe.moe_forward_profiled(gw.cfg, gw.x, gw.w_router, gw.bias, gw.qw["gate"], gw.qw["up"], gw.qw["down"],
+                                 gw.out, gw.ws, evs[i])
+    torch.cuda.synchronize()
+    return {nm: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs])) for i, nm in enumerate(moe.STAGE_NAMES)}
+
+
+def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, hbm_gbs: float, tpeak: float):
+    """Roofline fractions of GEMM1, GEMM2 and the whole layer: algorithmic
+    bytes over the HBM copy bandwidth and useful flops over the dtype's
+    tensor-core rate (tpeak, TFLOP/s); `bound` is the roof that binds by
+    arithmetic intensity."""
+    g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"])
+    g1_flops, g2_flops = gemm_flops(w)
+    g1_s, g2_s = stage_ms["gemm1_gate_up_swiglu"] / 1e3, stage_ms["gemm2_down"] / 1e3
+    balance = tpeak * 1e12 / (hbm_gbs * 1e9)        # flop per byte at which the two roofs meet
+    T, H = w["T"], w["H"]
+    layer_bytes = g1_bytes + g2_bytes + w["E"] * H * 2 + T * H * 4
+    layer_flops = g1_flops + g2_flops + 2.0 * T * H * w["E"]
+    step_s = ms_per_step / 1e3
+
+    def roof(b, f, sec):
+        tensor_bound = f / b > balance
+        return {"bound": "tensor" if tensor_bound else "hbm", "hbm_frac": b / sec / 1e9 / hbm_gbs,
+                "tensor_frac": f / sec / 1e12 / tpeak, "gbs": b / sec / 1e9, "tflops": f / sec / 1e12,
+                "frac": (f / sec / 1e12 / tpeak) if tensor_bound else (b / sec / 1e9 / hbm_gbs),
+                "algorithmic_bytes": b, "flops": f}
+
+    return {"gemm1": roof(g1_bytes, g1_flops, g1_s), "gemm2": roof(g2_bytes, g2_flops, g2_s),
+            "layer": roof(layer_bytes, layer_flops, step_s), "machine_balance_flop_per_byte": balance}
+
+
+def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str, tensor_peaks: dict, hbm_gbs: float,
+                     gpu_index: int, dist=None, world: int = 1, n_prof: int = 200):
+    """Set up one seeded workload, time `steps` forwards (CUDA-graph replays
+    of captured calls, or eager calls) between events on the launching
+    stream, with the SM clock sampled, plus per-stage event times."""
+    import synth
+    from synth.gpu_workload import GpuWorkload
+    w = synth.WORKLOADS[name]
+    gw = GpuWorkload(name, torch)
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        gw.forward()
+    torch.cuda.synchronize()
+    status = moe.moe_poll_device_status(gw.ws)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status} after warmup")
+    n_touched = int((gw.routing()["counts"] > 0).sum())
+    G = max(d for d in range(1, 21) if steps % d == 0)
+    graph = None
+    if launch == "graph":
+        graph = capture_graph(torch, gw, G)
+        status = moe.moe_poll_device_status(gw.ws)
+        if status != 0:
+            raise RuntimeError(f"{name}: device status {status} after the graph warm-up replay")
+        how = f"cuda_graph: {G} moe_forward calls per graph, {steps // G} replays"
+    else:
+        how = "eager: one moe_forward call per step"
+    clocks = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record(st)
+    if graph is not None:
+        for _ in range(steps // G):
+            graph.replay()
+    else:
+        for _ in range(steps):
+            gw.forward()
+    end.record(st)
+    torch.cuda.synchronize()
+    clocks.stop()
+    if dist:
+        dist.barrier()
+    ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
+    status = moe.moe_poll_device_status(gw.ws)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {status} after the timed steps")
+    del graph
+    ms_per_step = ms / steps
+    stage_ms = stage_times(moe, torch, gw, min(steps, n_prof))
+    tpk = tensor_peaks[w["fmt"]]
+    roof = rooflines(w, gw, n_touched, ms_per_step, stage_ms, hbm_gbs, tpk)
+    res = {"workload": name, "T": w["T"], "fmt": w["fmt"], "touched_experts": n_touched, "steps": steps,
+           "launch": how, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+           "tokens_per_s": job_tokens_per_s(w["T"], steps, world, ms), "stage_ms": stage_ms,
+           "roofline": roof, "clocks": clocks.summary(),
+           "gpu_launches": moe.moe_forward_kernel_count(gw.cfg) * steps}
+    return gw, res
+
+
+# ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
 
@@ -242,6 +429,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true", help="skip the other configurations")
+    ap.add_argument("--no-tensor-peak", action="store_true",
+                    help="skip the MMA-rate measurement (tensor roofs from the bf16 rate x nominal ratio)")
     ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
                     help="timed steps as CUDA-graph replays of captured moe_forward calls (default) or eager calls")
     args = ap.parse_args()
@@ -254,7 +444,6 @@ def main():
 
     import block_scaled_fp4_route_gb300 as moe
     import synth
-    from synth.gpu_workload import GpuWorkload
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -266,74 +455,28 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     else:
         torch.cuda.set_device(0)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    gpu_index = int(vis.split(",")[local]) if vis else local
 
-    def barrier():
-        if dist:
-            dist.barrier()
+    pk = peaks()
+    # ---- the tensor-core roofs: measured block-scaled MMA rates ----
+    if args.no_tensor_peak:
+        mma = None
+        tpeak = {f: pk["bf16_tflops"] * TENSOR_RATIO[f] for f in TENSOR_RATIO}
+        tsrc = f"sustained bf16 ({pk['source']}) x nominal dtype ratio"
+    else:
+        mma = measure_tensor_peaks(moe, torch, gpu_index)
+        # the GEMMs are timed inside a long run of steps: the sustained rate
+        tpeak = {f: mma[f]["sustained"]["tflops"] for f in mma}
+        tsrc = "measured_tcgen05"
 
     w = synth.WORKLOADS[args.workload]
     T, k = w["T"], w["k"]
-    gw = GpuWorkload(args.workload, torch)
+    gw, main_res = measure_workload(moe, torch, args.workload, args.steps, args.warmup, args.launch, tpeak,
+                                    pk["hbm_gbs"], gpu_index, dist, world)
     st = torch.cuda.current_stream()
-
-    for _ in range(args.warmup):
-        gw.forward()
-    torch.cuda.synchronize()
-    status = moe.moe_poll_device_status(gw.ws)
-    if status != 0:
-        raise RuntimeError(f"device status {status} after warmup")
-    counts = gw.routing()["counts"]
-    n_touched = int((counts > 0).sum())
-
-    # ---- the step as a serving loop runs it: moe_forward calls captured in a
-    # CUDA graph (G per graph), each a whole forward that reads its inputs ----
-    G = max(d for d in range(1, 21) if args.steps % d == 0)
-    graph = None
-    if args.launch == "graph":
-        side = torch.cuda.Stream()
-        side.wait_stream(st)
-        with torch.cuda.stream(side):
-            gw.forward()
-        st.wait_stream(side)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for _ in range(G):
-                gw.forward()
-        graph.replay()
-        torch.cuda.synchronize()
-        status = moe.moe_poll_device_status(gw.ws)
-        if status != 0:
-            raise RuntimeError(f"device status {status} after the graph warm-up replay")
-        launch = f"cuda_graph: {G} moe_forward calls per graph, {args.steps // G} replays"
-    else:
-        launch = "eager: one moe_forward call per step"
-
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-    gpu_index = int(vis.split(",")[local]) if vis else local
-    clocks = ClockSampler(gpu_index)
-    time.sleep(0.3)
-
-    # ---- timed region: K steps, inputs resident (touched expert weights >> L2) ----
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    start.record(st)
-    if graph is not None:
-        for _ in range(args.steps // G):
-            graph.replay()
-    else:
-        for _ in range(args.steps):
-            gw.forward()
-    end.record(st)
-    torch.cuda.synchronize()
-    clocks.stop()
-    barrier()
-    ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
-    ms_per_step = ms / args.steps
-    value = job_tokens_per_s(T, args.steps, world, ms)
-    launches_per_step = moe.moe_forward_kernel_count(gw.cfg)
+    ms_per_step = main_res["ms_per_step"]
+    value = main_res["tokens_per_s"]
 
     # ---- distribution of single eager steps (an event between consecutive
     # calls; the timed region above gives `value`) ----
@@ -347,19 +490,6 @@ def main():
     step_us = np.array([sev[i].elapsed_time(sev[i + 1]) * 1e3 for i in range(n_dist)])
     step_dist = {"steps": n_dist, "launch": "eager", "median": float(np.median(step_us)),
                  "p10": float(np.percentile(step_us, 10)), "p90": float(np.percentile(step_us, 90))}
-
-    # ---- per-stage device times (events between the stages, same stream) ----
-    n_prof = min(args.steps, 200)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.NUM_STAGES + 1)] for _ in range(n_prof)]
-    for row in evs:          # torch creates the CUDA event on its first record
-        for e in row:
-            e.record(st)
-    for i in range(n_prof):
-        moe.moe_forward_profiled(gw.cfg, gw.x, gw.w_router, gw.bias, gw.qw["gate"], gw.qw["up"], gw.qw["down"],
-                                 gw.out, gw.ws, evs[i])
-    torch.cuda.synchronize()
-    stage_ms = {n: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs]))
-                for i, n in enumerate(moe.STAGE_NAMES)}
 
     # ---- end to end through host buffers ----
     # Every step copies its x from pinned host memory and reads its output
@@ -402,7 +532,8 @@ def main():
         for i in range(4):
             e2e_step(i)
         torch.cuda.synchronize()
-        barrier()
+        if dist:
+            dist.barrier()
         t0 = time.perf_counter()
         for i in range(n_e2e):
             e2e_step(i)
@@ -410,48 +541,42 @@ def main():
         dt = max_over_ranks(time.perf_counter() - t0, dist, "cuda")
         assert torch.equal(out_host[(n_e2e - 1) & 1].view(torch.int16), gw.out.cpu().view(torch.int16)), \
             "end-to-end output differs from the device-resident run"
-        e2e = {"value": job_tokens_per_s(T, n_e2e, world, dt * 1e3), "unit": UNIT, "h2d_bytes_per_step": int(gw.x.numel() * 2),
-               "d2h_bytes_per_step": int(gw.out.numel() * 2), "steps": n_e2e,
+        e2e = {"value": job_tokens_per_s(T, n_e2e, world, dt * 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(gw.x.numel() * 2), "d2h_bytes_per_step": int(gw.out.numel() * 2),
+               "steps": n_e2e,
                "method": "pinned host x -> device -> moe_forward -> pinned host out, every step; steps pipelined "
                          "two deep on copy streams (events), one host wait after the last step; wall clock"}
+        del x_host, out_host, x_dev, out_dev
 
     # ---- roofline of the dominant kernel (GEMM1: gate/up + SwiGLU) ----
-    pk = peaks()
-    g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"])
-    g1_flops, g2_flops = gemm_flops(w)
-    g1_ms, g2_ms = stage_ms["gemm1_gate_up_swiglu"], stage_ms["gemm2_down"]
-    achieved = g1_bytes / (g1_ms / 1e3) / 1e9
-    tpeak = pk["bf16_tflops"] * TENSOR_RATIO[w["fmt"]]   # TFLOP/s, the dtype's dense peak
-    t1 = g1_flops / (g1_ms / 1e3) / 1e12
-    # the binding roof of GEMM1: tensor when its flops per byte exceed the machine balance
-    tensor_bound = g1_flops / g1_bytes > tpeak * 1e12 / (pk["hbm_gbs"] * 1e9)
+    g1 = main_res["roofline"]["gemm1"]
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         tr = json.load(open(TRAFFIC_FILE))
         ent = tr.get(args.workload, {}).get("gemm1")
         if ent and tr.get("source_sha") == kernel_source_sha():
             traffic = ent
-    hbm = {"achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-           "algorithmic_bytes": g1_bytes}
-    tensor = {"achieved": t1, "peak": tpeak, "unit": "TFLOP/s", "frac": t1 / tpeak, "flops": g1_flops,
-              "peak_note": f"sustained bf16 x {TENSOR_RATIO[w['fmt']]:g} ({w['fmt']} / bf16 nominal dense ratio)"}
-    main = tensor if tensor_bound else hbm
+    tensor_bound = g1["bound"] == "tensor"
+    hbm = {"achieved": g1["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": g1["hbm_frac"],
+           "algorithmic_bytes": g1["algorithmic_bytes"], "peak_source": pk["source"]}
+    tensor = {"achieved": g1["tflops"], "peak": tpeak[w["fmt"]], "unit": "TFLOP/s", "frac": g1["tensor_frac"],
+              "flops": g1["flops"], "peak_source": tsrc,
+              "peak_note": "sustained block-scaled MMA rate of this GPU (moe_bench_mma_peak, "
+                           f"{(mma or {}).get(w['fmt'], {}).get('mma', 'nominal ratio')}); the GEMM runs inside a "
+                           "long run of steps"}
+    top = tensor if tensor_bound else hbm
     roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": "gemm1_gate_up_swiglu",
-                "achieved": main["achieved"], "peak": main["peak"], "unit": main["unit"], "frac": main["frac"],
-                "traffic": traffic, "peak_source": pk["source"], "hbm": hbm, "tensor": tensor,
-                "gemm2": {"hbm_frac": g2_bytes / (g2_ms / 1e3) / 1e9 / pk["hbm_gbs"],
-                          "tensor_frac": g2_flops / (g2_ms / 1e3) / 1e12 / tpeak,
-                          "algorithmic_bytes": g2_bytes, "flops": g2_flops}}
-    layer_bytes = g1_bytes + g2_bytes + w["E"] * w["H"] * 2 + T * w["H"] * 4
-    layer = {"us_per_layer": ms_per_step * 1e3, "alg_bytes": layer_bytes,
-             "hbm_frac_whole_layer": layer_bytes / (ms_per_step / 1e3) / 1e9 / pk["hbm_gbs"],
-             "tensor_frac_whole_layer": (g1_flops + g2_flops) / (ms_per_step / 1e3) / 1e12 / tpeak,
-             "step_us": step_dist, "stage_ms": stage_ms}
+                "achieved": top["achieved"], "peak": top["peak"], "unit": top["unit"], "frac": top["frac"],
+                "traffic": traffic, "peak_source": top["peak_source"], "hbm": hbm, "tensor": tensor,
+                "gemm2": main_res["roofline"]["gemm2"], "layer": main_res["roofline"]["layer"],
+                "machine_balance_flop_per_byte": main_res["roofline"]["machine_balance_flop_per_byte"]}
+    layer = {"us_per_layer": ms_per_step * 1e3, "step_us": step_dist, "stage_ms": main_res["stage_ms"]}
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1) ----
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        samp = OracleSample(w, 8)
+        n_tok = 8 if T <= 1000 else 2
+        samp = OracleSample(w, n_tok)
         # the same sample repeated until about 10 s of CPU work have been timed
         runs, t0 = 0, time.perf_counter()
         while True:
@@ -461,20 +586,45 @@ def main():
             if dt >= 10.0:
                 break
         cpu = {"value": samp.tokens_per_call() * runs / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"8 tokens of {args.workload} through the whole layer ({samp.pairs} expert pairs, "
+               "sample": f"{n_tok} tokens of {args.workload} through the whole layer ({samp.pairs} expert pairs, "
                          f"{len(samp.cache)} experts decoded on the fly), {runs} runs in {dt:.2f} s"}
+
+    # ---- the other configurations (rank 0 of a single-GPU run) ----
+    per = None
+    if world == 1 and not args.no_per_workload:
+        del gw
+        torch.cuda.empty_cache()
+        per = {}
+        for nm, n_steps in PER_WORKLOAD.items():
+            if nm == args.workload:
+                continue
+            g2w, r = measure_workload(moe, torch, nm, n_steps, max(args.warmup, 5), args.launch, tpeak,
+                                      pk["hbm_gbs"], gpu_index, n_prof=50)
+            rl = r["roofline"]
+            per[nm] = {"T": r["T"], "fmt": r["fmt"], "touched_experts": r["touched_experts"], "steps": n_steps,
+                       "us_per_layer": r["us_per_layer"], "tokens_per_s": r["tokens_per_s"],
+                       "bound": rl["layer"]["bound"],
+                       "gemm1_frac": rl["gemm1"]["frac"], "gemm2_frac": rl["gemm2"]["frac"],
+                       "layer_frac": rl["layer"]["frac"],
+                       "gemm1": {k_: rl["gemm1"][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")},
+                       "gemm2": {k_: rl["gemm2"][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")},
+                       "layer": {k_: rl["layer"][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")},
+                       "stage_ms": r["stage_ms"], "clocks": r["clocks"]}
+            del g2w
+            torch.cuda.empty_cache()
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": w["fmt"], "data": "synthetic",
                 "config": {"workload": args.workload, "T": T, "H": w["H"], "E": w["E"], "k": k, "F": w["F"],
-                           "fmt": w["fmt"], "touched_experts": n_touched, "parallelism": f"replicas{world}",
-                           "launch": launch,
-                           "l2": f"inputs larger than L2: {layer_bytes / 1e9:.2f} GB of touched expert weights "
-                                 f"per step against a 129 MB L2; no flush"},
-                "layer": layer, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "clocks": clocks.summary(), "gpu_launches": launches_per_step * args.steps}
+                           "fmt": w["fmt"], "touched_experts": main_res["touched_experts"],
+                           "parallelism": f"replicas{world}", "launch": main_res["launch"],
+                           "l2": "inputs larger than L2: the touched expert weights of one step "
+                                 f"({gemm_bytes(w, main_res['touched_experts'])[0] / 1e9:.2f} GB read by GEMM1 "
+                                 "alone) against a 129 MB L2; no flush"},
+                "layer": layer, "roofline": roofline, "tensor_peaks": mma, "cpu_baseline": cpu, "e2e": e2e,
+                "per_workload": per, "clocks": main_res["clocks"], "gpu_launches": main_res["gpu_launches"]}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

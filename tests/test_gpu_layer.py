@@ -53,7 +53,8 @@ def padded_rows_of(r, tokens, k):
     return rows
 
 
-def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=False, route_all=True):
+def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=False, route_all=True,
+                expert_cache=None):
     w, T, k, E, H, F = gw.w, gw.w["T"], gw.w["k"], gw.w["E"], gw.w["H"], gw.w["F"]
     out = gw.forward()
     assert moe.moe_poll_device_status(gw.ws) == 0
@@ -67,7 +68,7 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
     # routing: all tokens (or the sample), near-ties certified against the bound
     rows_r = np.arange(T) if route_all else tokens
     x_r = synth.x_rows(w, rows_r)
-    ro = oracle.route(x_r, synth.router_weight(w), synth.router_bias(w), k)
+    ro = oracle.route(x_r, synth.router_weight(w), synth.router_bias(w), k, **gw.route_opts)
     ties_all = parity.check_topk(r["idx"][rows_r], ro["idx"], ro["keys"], ro["absdot"])
     stats["near_ties"] = len(ties_all)
     same = [i for i in range(len(rows_r)) if i not in ties_all]
@@ -100,7 +101,8 @@ def check_layer(gw, tokens=None, cap=10.0, mx_mode=0, check_h=True, out_rowwise=
     # the layer on the sample, with the GPU's choice on certified near-ties
     pos = {int(t): i for i, t in enumerate(rows_r)}
     override = {i: ties_all[pos[int(t)]] for i, t in enumerate(tokens) if pos.get(int(t)) in ties_all}
-    res = oracle.moe_layer(w, tokens, idx_override=override, cap=cap, mx_mode=mx_mode, keep_pairs=check_h)
+    res = oracle.moe_layer(w, tokens, idx_override=override, cap=cap, mx_mode=mx_mode, keep_pairs=check_h,
+                           expert_cache=expert_cache, **gw.route_opts)
     if out_rowwise:
         stats["literal"] = parity.out_error(gpu_out[tokens], res["out"])[0] / parity.out_error(
             gpu_out[tokens], res["out"])[1]
@@ -171,6 +173,21 @@ def test_small_layer_uncapped_and_mx_round_up():
     print(check_layer(gw, cap=0.0))
 
 
+@pytest.mark.parametrize("name", ["tiny_nvfp4", "ragged_mxfp8", "tc_router_nvfp4", "tc_router_mxfp8_outliers"])
+@pytest.mark.parametrize("opts", [dict(bias_in_weights=1), dict(routed_scale=2.5),
+                                  dict(bias_in_weights=1, routed_scale=2.5)])
+def test_router_options_through_the_layer(name, opts):
+    # moe_config.bias_in_weights (weights from the biased keys) and
+    # routed_scale, on the decode router (T <= 256) and the tensor-core
+    # router (T > 256): routing bit-exact, weights within W_TOL, the output
+    # within tolerance
+    gw = GpuWorkload(SMALL[name], torch, **opts)
+    st = check_layer(gw, out_rowwise=gw.w["outlier_frac"] > 0, check_h=False)
+    w = gw.routing()["w"].astype(np.float64)
+    assert np.allclose(w.sum(1), opts.get("routed_scale", 1.0), atol=1e-5)
+    print(name, opts, st)
+
+
 @pytest.mark.parametrize("name", ["ragged_mxfp8", "tc_router_nvfp4"])
 def test_staged_calls_equal_forward(name):
     gw = GpuWorkload(SMALL[name], torch)
@@ -202,24 +219,122 @@ def sample_tokens(w, n, extra=()):
     toks = set(int(t) for t in extra)
     toks.add(0)
     toks.add(w["T"] - 1)
-    while len(toks) < n:
+    while len(toks) < min(n, w["T"]):
         toks.add(int(rng.integers(0, w["T"])))
     return np.array(sorted(toks))
 
 
-FULL = ["decode64_nvfp4", "decode192_mxfp8_outliers", "prefill4096_nvfp4", "prefill16384_mxfp8_zipf"]
+def tile_focus(r, nt, n_tail=4):
+    """The most loaded expert and n_tail more experts (the most loaded first)
+    whose last token tile is ragged (count % nt != 0) and which span more
+    than one tile."""
+    counts = r["counts"]
+    order = [int(e) for e in np.argsort(-counts, kind="stable")]
+    hot = order[0]
+    tails = [e for e in order[1:] if counts[e] > nt and counts[e] % nt][:n_tail]
+    if len(tails) < n_tail:
+        tails += [e for e in order[1:] if counts[e] % nt and e not in tails][:n_tail - len(tails)]
+    return hot, tails
+
+
+def focus_sample(w, r, nt, n=48):
+    """>= n tokens for the output check of a large batch: rows of the most
+    loaded expert (its first tile, a middle row, its last ragged tile), the
+    last ragged tile of four more experts, the outlier rows, the first and
+    last token; the rest filled with tokens (from a seeded pool) that add the
+    fewest experts not yet in the sample, so that the oracle decodes few
+    experts."""
+    T, k = w["T"], r["idx"].shape[1]
+    counts, offsets, perm, idx = r["counts"], r["offsets"], r["perm"], r["idx"]
+    hot, tails = tile_focus(r, nt)
+    toks = {0, T - 1}
+    c = int(counts[hot])
+    for p in sorted({0, 1, min(2, c - 1), c // 2, (c - 1) // nt * nt, c - 1}):
+        toks.add(int(perm[offsets[hot] + p]) // k)
+    for e in tails:
+        c = int(counts[e])
+        for p in ((c - 1) // nt * nt, c - 1):
+            toks.add(int(perm[offsets[e] + p]) // k)
+    if w["outlier_frac"] > 0:
+        toks.update(int(t) for t in np.nonzero(synth.outlier_flags(w))[0])
+    experts = set(int(e) for t in toks for e in idx[t])
+    pool = [int(t) for t in np.random.default_rng(2000 + w["seed"]).permutation(T)[:4096]]
+    while len(toks) < min(n, T):
+        best = min((t for t in pool if t not in toks), key=lambda t: len(set(idx[t].tolist()) - experts))
+        toks.add(best)
+        experts.update(int(e) for e in idx[best])
+    return np.array(sorted(toks)), hot, tails
+
+
+def check_pair_rows(gw, r, experts, cache, max_rows=256):
+    """y of the pairs in the first and the last token tile of each expert
+    (every row of a ragged tail) against the oracle's FFN of that expert on
+    the same tokens: max|dy| <= OUT_TOL * rms(y) per expert."""
+    w, k, H = gw.w, gw.w["k"], gw.w["H"]
+    nt = gw.layout["tile_rows"]
+    P = w["T"] * k
+    y_all = gw.ws_view("y_perm", torch.float32, P * H).view(P, H)
+    worst = 0.0
+    for e in experts:
+        c, lo = int(r["counts"][e]), int(r["offsets"][e])
+        ps = sorted(set(range(min(c, nt))) | set(range((c - 1) // nt * nt, c)))[:max_rows]
+        ps = np.asarray(ps, np.int64) + lo
+        toks = r["perm"][ps] // k
+        a = oracle.decode(w["fmt"], *oracle.quantize_x(w, synth.x_rows(w, toks)))
+        if e not in cache:
+            cache[e] = oracle.quantized_expert(w, e)
+        dec = oracle.decoded_expert(w, cache[e])
+        y_ref = oracle.expert_ffn(w["fmt"], dec["gate"], dec["up"], dec["down"], a)["y"]
+        y_gpu = y_all[torch.from_numpy(ps).cuda()].cpu().numpy().astype(np.float64)
+        mx, rms = parity.out_error(y_gpu, y_ref)
+        assert mx <= parity.OUT_TOL * rms, f"expert {e}: max|dy| {mx:.4g} > {parity.OUT_TOL} * rms {rms:.4g}"
+        worst = max(worst, mx / rms)
+    return worst
+
+
+def check_combine_rows(gw, r, out_gpu, tokens):
+    """The combine on the GPU's own y and weights: out[t] = bf16(sum_j w y)
+    within half a bf16 ulp plus the fp32 summation error."""
+    k, H = gw.w["k"], gw.w["H"]
+    P = gw.w["T"] * k
+    y_all = gw.ws_view("y_perm", torch.float32, P * H).view(P, H)
+    pp = r["pair_pos"][tokens]
+    y = y_all[torch.from_numpy(pp.ravel().astype(np.int64)).cuda()].cpu().numpy().astype(np.float64)
+    y = y.reshape(len(tokens), k, H)
+    wt = r["w"][tokens].astype(np.float64)
+    ref = np.einsum("tj,tjh->th", wt, y)
+    bound = 2.0 ** -8 * np.abs(ref) + 1e-6 * np.einsum("tj,tjh->th", np.abs(wt), np.abs(y)) + 1e-30
+    assert np.all(np.abs(out_gpu[tokens] - ref) <= bound)
+
+
+FULL = ["decode1_nvfp4", "decode8_nvfp4", "decode32_mxfp8", "decode64_nvfp4", "decode192_mxfp8_outliers",
+        "prefill4096_nvfp4", "prefill16384_mxfp8_zipf"]
 
 
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_workload(name):
+    # every token's routing and dispatch; x codes, output rows (and, above
+    # 1000 tokens, the y rows of the most loaded expert and of four ragged
+    # tile tails, and the combine of 1024 tokens) of a sample
     w = synth.WORKLOADS[name]
     gw = GpuWorkload(name, torch)
-    extra = []
-    if w["outlier_frac"] > 0:
-        extra = list(np.nonzero(synth.outlier_flags(w))[0])
-    n = 6 if w["T"] > 1000 else 8
-    tokens = sample_tokens(w, n, extra)
-    st = check_layer(gw, tokens, out_rowwise=w["outlier_frac"] > 0, route_all=w["T"] <= 4096)
+    big = w["T"] > 1000
+    cache = {}
+    if big:
+        gw.forward()
+        r = gw.routing()
+        tokens, hot, tails = focus_sample(w, r, gw.layout["tile_rows"], 48)
+    else:
+        extra = list(np.nonzero(synth.outlier_flags(w))[0]) if w["outlier_frac"] > 0 else []
+        tokens = sample_tokens(w, 8, extra)
+    st = check_layer(gw, tokens, out_rowwise=w["outlier_frac"] > 0, route_all=True, expert_cache=cache)
+    st["sample_tokens"] = len(tokens)
+    if big:
+        r = gw.routing()
+        st["pair_rows_err"] = check_pair_rows(gw, r, [hot] + tails, cache)
+        out = parity.bf16_to_f64(gw.out)
+        check_combine_rows(gw, r, out, np.sort(np.random.default_rng(3).choice(w["T"], 1024, replace=False)))
+        st["experts_decoded"] = len(cache)
     print(name, st)
     del gw
     torch.cuda.empty_cache()

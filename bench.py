@@ -328,11 +328,19 @@ def stage_times(moe, torch, gw, n: int) -> dict:
     return {nm: float(np.mean([e[i].elapsed_time(e[i + 1]) for e in evs])) for i, nm in enumerate(moe.STAGE_NAMES)}
 
 
+def ffn_fused(gw) -> bool:
+    """Decode batches (64-row tiles) run GEMM1, the h quantisation and GEMM2
+    as one kernel by default (moe_config.ffn_schedule 0)."""
+    return gw.layout["tile_rows"] == 64 and gw.cfg.ffn_schedule == 0
+
+
 def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, hbm_gbs: float, tpeak: float):
     """Roofline fractions of GEMM1, GEMM2 and the whole layer: algorithmic
     bytes over the HBM copy bandwidth and useful flops over the dtype's
     tensor-core rate (tpeak, TFLOP/s); `bound` is the roof that binds by
-    arithmetic intensity."""
+    arithmetic intensity.  Where one fused kernel runs both GEMMs (decode
+    batches) its roof ("ffn") counts the bytes and flops of both and the
+    separate GEMM entries are absent."""
     g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"])
     g1_flops, g2_flops = gemm_flops(w)
     g1_s, g2_s = stage_ms["gemm1_gate_up_swiglu"] / 1e3, stage_ms["gemm2_down"] / 1e3
@@ -349,19 +357,29 @@ def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, h
                 "frac": (f / sec / 1e12 / tpeak) if tensor_bound else (b / sec / 1e9 / hbm_gbs),
                 "algorithmic_bytes": b, "flops": f}
 
+    if ffn_fused(gw):
+        # the fused kernel's h round trip stays on chip or in L2 (its
+        # algorithmic bytes are GEMM1's input and GEMM2's weights and output)
+        P, F = w["T"] * w["k"], w["F"]
+        nv = w["fmt"] == "nvfp4"
+        bpe = 0.5 + 1 / 16 if nv else 1 + 1 / 32
+        h_write = P * F * (2 if nv else bpe)             # GEMM1's h out (bf16, or MXFP8 codes + scales)
+        h_read = P * (F * bpe + (4 if nv else 0))        # GEMM2's encoded h in
+        ffn = roof(g1_bytes + g2_bytes - h_write - h_read, g1_flops + g2_flops, g1_s)
+        return {"ffn": ffn, "layer": roof(layer_bytes, layer_flops, step_s), "machine_balance_flop_per_byte": balance}
     return {"gemm1": roof(g1_bytes, g1_flops, g1_s), "gemm2": roof(g2_bytes, g2_flops, g2_s),
             "layer": roof(layer_bytes, layer_flops, step_s), "machine_balance_flop_per_byte": balance}
 
 
 def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str, tensor_peaks: dict, hbm_gbs: float,
-                     gpu_index: int, dist=None, world: int = 1, n_prof: int = 200):
+                     gpu_index: int, dist=None, world: int = 1, n_prof: int = 200, ffn_schedule: int = 0):
     """Set up one seeded workload, time `steps` forwards (CUDA-graph replays
     of captured calls, or eager calls) between events on the launching
     stream, with the SM clock sampled, plus per-stage event times."""
     import synth
     from synth.gpu_workload import GpuWorkload
     w = synth.WORKLOADS[name]
-    gw = GpuWorkload(name, torch)
+    gw = GpuWorkload(name, torch, ffn_schedule=ffn_schedule)
     st = torch.cuda.current_stream()
     for _ in range(warmup):
         gw.forward()
@@ -409,7 +427,7 @@ def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str
     tpk = tensor_peaks[w["fmt"]]
     roof = rooflines(w, gw, n_touched, ms_per_step, stage_ms, hbm_gbs, tpk)
     res = {"workload": name, "T": w["T"], "fmt": w["fmt"], "touched_experts": n_touched, "steps": steps,
-           "launch": how, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+           "launch": how, "ffn": "fused decode kernel" if ffn_fused(gw) else "separate kernels", "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
            "tokens_per_s": job_tokens_per_s(w["T"], steps, world, ms), "stage_ms": stage_ms,
            "roofline": roof, "clocks": clocks.summary(),
            "gpu_launches": moe.moe_forward_kernel_count(gw.cfg) * steps}
@@ -432,6 +450,9 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other configurations")
     ap.add_argument("--no-tensor-peak", action="store_true",
                     help="skip the MMA-rate measurement (tensor roofs from the bf16 rate x nominal ratio)")
+    ap.add_argument("--ffn-schedule", type=int, default=0, choices=[0, 1],
+                    help="moe_config.ffn_schedule: 0 = decode batches run the expert FFN as one fused kernel, "
+                         "1 = separate kernels")
     ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
                     help="timed steps as CUDA-graph replays of captured moe_forward calls (default) or eager calls")
     args = ap.parse_args()
@@ -473,7 +494,7 @@ def main():
     w = synth.WORKLOADS[args.workload]
     T, k = w["T"], w["k"]
     gw, main_res = measure_workload(moe, torch, args.workload, args.steps, args.warmup, args.launch, tpeak,
-                                    pk["hbm_gbs"], gpu_index, dist, world)
+                                    pk["hbm_gbs"], gpu_index, dist, world, ffn_schedule=args.ffn_schedule)
     st = torch.cuda.current_stream()
     ms_per_step = main_res["ms_per_step"]
     value = main_res["tokens_per_s"]
@@ -548,12 +569,14 @@ def main():
                          "two deep on copy streams (events), one host wait after the last step; wall clock"}
         del x_host, out_host, x_dev, out_dev
 
-    # ---- roofline of the dominant kernel (GEMM1: gate/up + SwiGLU) ----
-    g1 = main_res["roofline"]["gemm1"]
+    # ---- roofline of the dominant kernel (GEMM1: gate/up + SwiGLU; for
+    # decode batches the fused expert FFN) ----
+    kname = "ffn" if "ffn" in main_res["roofline"] else "gemm1"
+    g1 = main_res["roofline"][kname]
     traffic = None
     if os.path.exists(TRAFFIC_FILE):
         tr = json.load(open(TRAFFIC_FILE))
-        ent = tr.get(args.workload, {}).get("gemm1")
+        ent = tr.get(args.workload, {}).get(kname)
         if ent and tr.get("source_sha") == kernel_source_sha():
             traffic = ent
     tensor_bound = g1["bound"] == "tensor"
@@ -565,10 +588,11 @@ def main():
                            f"{(mma or {}).get(w['fmt'], {}).get('mma', 'nominal ratio')}); the GEMM runs inside a "
                            "long run of steps"}
     top = tensor if tensor_bound else hbm
-    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": "gemm1_gate_up_swiglu",
+    roofline = {"bound": "tensor" if tensor_bound else "hbm",
+                "kernel": "ffn_decode_fused" if kname == "ffn" else "gemm1_gate_up_swiglu",
                 "achieved": top["achieved"], "peak": top["peak"], "unit": top["unit"], "frac": top["frac"],
                 "traffic": traffic, "peak_source": top["peak_source"], "hbm": hbm, "tensor": tensor,
-                "gemm2": main_res["roofline"]["gemm2"], "layer": main_res["roofline"]["layer"],
+                "gemm2": main_res["roofline"].get("gemm2"), "layer": main_res["roofline"]["layer"],
                 "machine_balance_flop_per_byte": main_res["roofline"]["machine_balance_flop_per_byte"]}
     layer = {"us_per_layer": ms_per_step * 1e3, "step_us": step_dist, "stage_ms": main_res["stage_ms"]}
 
@@ -599,17 +623,17 @@ def main():
             if nm == args.workload:
                 continue
             g2w, r = measure_workload(moe, torch, nm, n_steps, max(args.warmup, 5), args.launch, tpeak,
-                                      pk["hbm_gbs"], gpu_index, n_prof=50)
+                                      pk["hbm_gbs"], gpu_index, n_prof=50, ffn_schedule=args.ffn_schedule)
             rl = r["roofline"]
             per[nm] = {"T": r["T"], "fmt": r["fmt"], "touched_experts": r["touched_experts"], "steps": n_steps,
+                       "ffn": r["ffn"],
                        "us_per_layer": r["us_per_layer"], "tokens_per_s": r["tokens_per_s"],
-                       "bound": rl["layer"]["bound"],
-                       "gemm1_frac": rl["gemm1"]["frac"], "gemm2_frac": rl["gemm2"]["frac"],
-                       "layer_frac": rl["layer"]["frac"],
-                       "gemm1": {k_: rl["gemm1"][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")},
-                       "gemm2": {k_: rl["gemm2"][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")},
-                       "layer": {k_: rl["layer"][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")},
+                       "bound": rl["layer"]["bound"], "layer_frac": rl["layer"]["frac"],
                        "stage_ms": r["stage_ms"], "clocks": r["clocks"]}
+            for kn in ("ffn", "gemm1", "gemm2", "layer"):
+                if kn in rl:
+                    per[nm][kn + "_frac"] = rl[kn]["frac"]
+                    per[nm][kn] = {k_: rl[kn][k_] for k_ in ("bound", "hbm_frac", "tensor_frac")}
             del g2w
             torch.cuda.empty_cache()
 
@@ -620,6 +644,7 @@ def main():
                 "config": {"workload": args.workload, "T": T, "H": w["H"], "E": w["E"], "k": k, "F": w["F"],
                            "fmt": w["fmt"], "touched_experts": main_res["touched_experts"],
                            "parallelism": f"replicas{world}", "launch": main_res["launch"],
+                           "ffn": main_res["ffn"],
                            "l2": "inputs larger than L2: the touched expert weights of one step "
                                  f"({gemm_bytes(w, main_res['touched_experts'])[0] / 1e9:.2f} GB read by GEMM1 "
                                  "alone) against a 129 MB L2; no flush"},

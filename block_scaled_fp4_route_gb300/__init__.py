@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
-            "moe_route_noalloc", "moe_route_noalloc_poll_status", "moe_fake_quantize", "moe_kv_quantize_mxfp8", "moe_bench_mma_peak", "moe_selftest_bounded_wait", "moe_forward_kernel_count",
+            "moe_route_noalloc", "moe_route_noalloc_poll_status", "moe_fake_quantize", "moe_kv_quantize_mxfp8", "moe_bench_mma_peak", "moe_selftest_bounded_wait", "moe_selftest_dependency_wait", "moe_forward_kernel_count",
             "moe_status_string"]
 
 
@@ -36,7 +36,7 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
                 ("F", ctypes.c_int), ("fmt", ctypes.c_int), ("swiglu_cap", ctypes.c_float),
                 ("act_global_mode", ctypes.c_int), ("mx_scale_mode", ctypes.c_int), ("bias_in_weights", ctypes.c_int),
-                ("routed_scale", ctypes.c_float)]
+                ("routed_scale", ctypes.c_float), ("ffn_schedule", ctypes.c_int)]
 
 
 class moe_qweight(ctypes.Structure):
@@ -44,7 +44,7 @@ class moe_qweight(ctypes.Structure):
 
 
 _LAYOUT_FIELDS = ["status", "logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "pair_pos", "bitmap",
-                  "seg_start", "tiles", "rt_base", "xq_codes", "xq_scales", "xq_global", "h_bf16", "hq_codes",
+                  "seg_start", "tiles", "rt_base", "ffn_sync", "xq_codes", "xq_scales", "xq_global", "h_bf16", "hq_codes",
                   "hq_scales", "hq_global", "y_perm", "total"]
 
 
@@ -85,6 +85,7 @@ def lib():
             L.moe_bench_mma_peak.argtypes = [ctypes.c_int, i64, P, P, ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_double), P]
             L.moe_selftest_bounded_wait.argtypes = [cfgp, qwp, qwp, P, sz, i64, P]
+            L.moe_selftest_dependency_wait.argtypes = [cfgp, qwp, qwp, qwp, P, sz, i64, P]
             L.moe_poll_device_status.argtypes = [P, P]
             L.moe_workspace_layout.argtypes = [cfgp, ctypes.POINTER(moe_ws_layout)]
             L.moe_status_string.argtypes = [ctypes.c_int]
@@ -121,14 +122,16 @@ def _stream(stream):
 
 
 def make_config(T, H, E, k, F, fmt, swiglu_cap=10.0, mx_scale_mode=0, bias_in_weights=0, routed_scale=1.0,
-                act_global_mode=0):
+                act_global_mode=0, ffn_schedule=0):
     """A moe_config: T tokens, hidden H, E experts, top-k, FFN width F; fmt "nvfp4" / "mxfp8" (or
     FMT_*); swiglu_cap c of c*tanh(v/c) (0 = none); mx_scale_mode 0 = OCP floor, 1 = round-up;
     bias_in_weights 0 = the bias steers selection only; act_global_mode 1 = static per-expert NVFP4
-    activation globals."""
+    activation globals; ffn_schedule 0 = decode batches run the expert FFN as one fused kernel,
+    1 = separate kernels."""
     if isinstance(fmt, str):
         fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
-    return moe_config(T, H, E, k, F, fmt, swiglu_cap, act_global_mode, mx_scale_mode, bias_in_weights, routed_scale)
+    return moe_config(T, H, E, k, F, fmt, swiglu_cap, act_global_mode, mx_scale_mode, bias_in_weights, routed_scale,
+                      ffn_schedule)
 
 
 def qweight(codes, scales, global_scale=None) -> moe_qweight:
@@ -287,6 +290,15 @@ def moe_selftest_bounded_wait(cfg, gate, up, ws, limit_cycles, stream=None):
     _check("moe_selftest_bounded_wait", lib().moe_selftest_bounded_wait(
         ctypes.byref(cfg), ctypes.byref(gate), ctypes.byref(up), _ptr(ws), ws.numel() * ws.element_size(),
         limit_cycles, _stream(stream)))
+
+
+def moe_selftest_dependency_wait(cfg, gate, up, down, ws, limit_cycles, stream=None):
+    """Test hook: the fused decode FFN over the tile plan in ws with its gate/up completion reports
+    withheld, so that the down tiles' waits run out after limit_cycles; moe_poll_device_status then
+    reports the timeout."""
+    _check("moe_selftest_dependency_wait", lib().moe_selftest_dependency_wait(
+        ctypes.byref(cfg), ctypes.byref(gate), ctypes.byref(up), ctypes.byref(down), _ptr(ws),
+        ws.numel() * ws.element_size(), limit_cycles, _stream(stream)))
 
 
 def moe_pack_scales(rowmajor, rows, scale_cols, tiled, stream=None):

@@ -20,7 +20,8 @@ LIB = os.path.join(BUILD, "libmoe.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["moe_api.cu", "moe_route.cu", "moe_route_tc.cu", "moe_dispatch.cu", "moe_quant.cu", "moe_gemm.cu", "moe_combine.cu",
-           "moe_kv.cu", "moe_peak.cu"]
+           "moe_kv.cu", "moe_peak.cu",
+           "moe_ffn_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "-I" + INCLUDE]

@@ -53,6 +53,7 @@ moe_status check_cfg(const moe_config* c) {
   if (c->mx_scale_mode != 0 && c->mx_scale_mode != 1) return MOE_ERR_INVALID_ARG;
   if (c->act_global_mode != 0 && c->act_global_mode != 1) return MOE_ERR_INVALID_ARG;
   if (c->act_global_mode == 1 && c->fmt != MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;  // MXFP8 has no global
+  if (c->ffn_schedule != 0 && c->ffn_schedule != 1) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -178,13 +179,6 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g1.hq_scales = hs;
   g1.status = status;
   g1.num_sms = sms;
-  mark(ev, 3, st);
-  if (launch_gemm(g1, st, true) != cudaSuccess) return MOE_ERR_CUDA;
-
-  mark(ev, 4, st);
-  if (h_row_pass(c) &&
-      launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, act_static, st, true) != cudaSuccess)
-    return MOE_ERR_CUDA;
 
   GemmLaunch g2{};
   g2.cfg = &c;
@@ -206,6 +200,24 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g2.y_out = y;
   g2.status = status;
   g2.num_sms = sms;
+
+  mark(ev, 3, st);
+  if (ffn_fused(c)) {
+    // decode batches: GEMM1, the h quantisation and GEMM2 in one launch (its
+    // time is the GEMM1 stage; the h and GEMM2 stages are empty)
+    if (launch_ffn_decode(g1, g2, at<int32_t>(ws, L.ffn_sync), act_static, hq, hs, hg, 0, st, true) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    mark(ev, 4, st);
+    mark(ev, 5, st);
+    return MOE_OK;
+  }
+  if (launch_gemm(g1, st, true) != cudaSuccess) return MOE_ERR_CUDA;
+
+  mark(ev, 4, st);
+  if (h_row_pass(c) &&
+      launch_quant_h(c, h, idx, offsets, perm, seg, hq, hs, hg, act_static, st, true) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
   mark(ev, 5, st);
   if (launch_gemm(g2, st, true) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -221,11 +233,13 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, int32_t* count
   RowTile* tiles = at<RowTile>(ws, L.tiles);
   int32_t* rtb = at<int32_t>(ws, L.rt_base);
   if (dispatch_fits_one_cta(c))
-    return cuda_status(launch_dispatch_small(c, idx, counts, offsets, perm, pair_pos, seg, tiles, rtb, status, st, pdl));
+    return cuda_status(launch_dispatch_small(c, idx, counts, offsets, perm, pair_pos, seg, tiles, rtb, status,
+                                             at<int32_t>(ws, L.ffn_sync), st, pdl));
   uint32_t* bm = at<uint32_t>(ws, L.bitmap);
   int32_t* chunk_counts = reinterpret_cast<int32_t*>(bm + (size_t)c.E * ((c.T + 31) / 32));
   if (launch_dispatch(c, idx, bm, chunk_counts, st, pdl) != cudaSuccess ||
-      launch_scan_plan(c, chunk_counts, counts, nullptr, offsets, seg, tiles, rtb, status, st, true) != cudaSuccess ||
+      launch_scan_plan(c, chunk_counts, counts, nullptr, offsets, seg, tiles, rtb, status, at<int32_t>(ws, L.ffn_sync),
+                       st, true) != cudaSuccess ||
       launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st, true) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -269,6 +283,7 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
   L->seg_start = take((E + 1) * 4);
   L->tiles = take(max_row_tiles(c) * sizeof(RowTile));
   L->rt_base = take((E + 1) * 4);
+  L->ffn_sync = take(ffn_sync_ints(c) * 4);
   L->xq_codes = take(R * code_bytes(c.fmt, c.H));
   L->xq_scales = take(act_scale_bytes(R, c.H / bs, tile_rows(c)));
   L->xq_global = take(R * 4);
@@ -352,7 +367,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_
   cudaStream_t st = (cudaStream_t)stream;
   if (launch_scan_plan(*cfg, nullptr, nullptr, offsets_dev, nullptr, at<int32_t>(ws_dev, L.seg_start),
                        at<RowTile>(ws_dev, L.tiles), at<int32_t>(ws_dev, L.rt_base),
-                       at<uint32_t>(ws_dev, L.status), st, false) != cudaSuccess)
+                       at<uint32_t>(ws_dev, L.status), at<int32_t>(ws_dev, L.ffn_sync), st, false) != cudaSuccess)
     return MOE_ERR_CUDA;
   return ffn_core(*cfg, sms, (const __nv_bfloat16*)x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, gate, up,
                   down, act_static_scales, y_perm_dev, ws_dev, st);
@@ -418,9 +433,13 @@ moe_status moe_forward_kernel_count(const moe_config* cfg, int* count) {
   int n = router_uses_tc(c) ? 3 : 2;         // router: (norms,) logits, top-k
   n += dispatch_fits_one_cta(c) ? 1 : 3;      // dispatch: one CTA, or bitmap + scan + scatter
   n += 1;                                     // x quantisation
-  n += 1;                                     // GEMM1
-  n += h_row_pass(c) ? 1 : 0;                 // h quantisation (else inside GEMM1)
-  n += 2;                                     // GEMM2, combine
+  if (ffn_fused(c)) {
+    n += 2;                                   // the fused expert FFN, combine
+  } else {
+    n += 1;                                   // GEMM1
+    n += h_row_pass(c) ? 1 : 0;               // h quantisation (else inside GEMM1)
+    n += 2;                                   // GEMM2, combine
+  }
   *count = n;
   return MOE_OK;
 }
@@ -580,6 +599,74 @@ moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qweight* g
   g1.wait_limit = limit_cycles;
   g1.withhold_loads = 1;
   return cuda_status(launch_gemm(g1, (cudaStream_t)stream, false));
+}
+
+moe_status moe_selftest_dependency_wait(const moe_config* cfg, const moe_qweight* gate, const moe_qweight* up,
+                                        const moe_qweight* down, void* ws_dev, size_t ws_bytes, int64_t limit_cycles,
+                                        void* stream) {
+  moe_status s = check_cfg(cfg);
+  if (s == MOE_OK && tile_rows(*cfg) != kNTDecode) s = MOE_ERR_UNSUPPORTED_SHAPE;  // the fused kernel's shapes only
+  if (s == MOE_OK) s = check_qw(cfg, gate);
+  if (s == MOE_OK) s = check_qw(cfg, up);
+  if (s == MOE_OK) s = check_qw(cfg, down);
+  if (s == MOE_OK) s = check_ws(cfg, ws_dev, ws_bytes);
+  if (s == MOE_OK && (limit_cycles < 1000 || limit_cycles > 4000000000LL)) s = MOE_ERR_INVALID_ARG;
+  int sms = 0;
+  if (s == MOE_OK) s = device_check(&sms);
+  if (s != MOE_OK) return s;
+  const moe_config& c = *cfg;
+  moe_ws_layout L;
+  ws_layout(c, &L);
+  const int64_t hb = code_bytes(c.fmt, c.H), fb = code_bytes(c.fmt, c.F);
+  uint8_t* hq = at<uint8_t>(ws_dev, L.hq_codes);
+  uint8_t* hs = at<uint8_t>(ws_dev, L.hq_scales);
+  float* hg = at<float>(ws_dev, L.hq_global);
+  CUtensorMap mg, mu, md, mx, mh;
+  if (!make_map(&mg, gate->codes, (int64_t)c.E * c.F, hb, 128) ||
+      !make_map(&mu, up->codes, (int64_t)c.E * c.F, hb, 128) ||
+      !make_map(&md, down->codes, (int64_t)c.E * c.H, fb, 128) ||
+      !make_map(&mx, at<uint8_t>(ws_dev, L.xq_codes), L.R, hb, b_box_rows(c)) || !make_map(&mh, hq, L.R, fb, b_box_rows(c)))
+    return MOE_ERR_CUDA;
+  GemmLaunch g1{}, g2{};
+  g1.cfg = g2.cfg = &c;
+  g1.gated = true;
+  g1.tmA0 = &mg;
+  g1.tmA1 = &mu;
+  g1.tmB = &mx;
+  g1.sfA0 = (const uint8_t*)gate->scales;
+  g1.sfA1 = (const uint8_t*)up->scales;
+  g1.sfB = at<uint8_t>(ws_dev, L.xq_scales);
+  g1.gA0 = gate->global_scale;
+  g1.gA1 = up->global_scale;
+  g1.gB = at<float>(ws_dev, L.xq_global);
+  g1.NA = c.F;
+  g1.K = c.H;
+  g1.h_out = at<__nv_bfloat16>(ws_dev, L.h_bf16);
+  g1.hq_codes = hq;
+  g1.hq_scales = hs;
+  g2.gated = false;
+  g2.tmA0 = g2.tmA1 = &md;
+  g2.tmB = &mh;
+  g2.sfA0 = g2.sfA1 = (const uint8_t*)down->scales;
+  g2.sfB = hs;
+  g2.gA0 = g2.gA1 = down->global_scale;
+  g2.gB = hg;
+  g2.NA = c.H;
+  g2.K = c.F;
+  g2.y_out = at<float>(ws_dev, L.y_perm);
+  for (GemmLaunch* g : {&g1, &g2}) {
+    g->tiles = at<RowTile>(ws_dev, L.tiles);
+    g->rt_base = at<int32_t>(ws_dev, L.rt_base);
+    g->E = c.E;
+    g->status = at<uint32_t>(ws_dev, L.status);
+    g->num_sms = sms;
+    g->wait_limit = limit_cycles;
+  }
+  // the counters are zeroed as the tile-plan kernel does (the self-test runs on its own)
+  if (cudaMemsetAsync(at<int32_t>(ws_dev, L.ffn_sync), 0, ffn_sync_ints(c) * 4, (cudaStream_t)stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(launch_ffn_decode(g1, g2, at<int32_t>(ws_dev, L.ffn_sync), nullptr, hq, hs, hg, 1,
+                                       (cudaStream_t)stream, false));
 }
 
 moe_status moe_poll_device_status(void* ws_dev, void* stream) {

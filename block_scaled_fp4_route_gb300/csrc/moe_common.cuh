@@ -49,6 +49,7 @@ enum : uint32_t {
   ST_TIMEOUT_MMA = 1u << 1,
   ST_TIMEOUT_EPILOGUE = 1u << 2,
   ST_TIMEOUT_DRAIN = 1u << 3,
+  ST_TIMEOUT_DEPEND = 1u << 4,  // a down tile of the fused decode FFN waited too long for its h rows
 };
 
 // ----------------------------------------------------------------------------

@@ -85,12 +85,15 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
                                                     const int32_t* __restrict__ offsets_in, int E,
                                                     int32_t* __restrict__ offsets_out, int32_t* __restrict__ seg_start,
                                                     RowTile* __restrict__ tiles, int32_t* __restrict__ rt_base,
-                                                    uint32_t* __restrict__ status, int nt) {
+                                                    uint32_t* __restrict__ status, int nt,
+                                                    int32_t* __restrict__ sync, int nsync) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
   pdl_wait();
   pdl_trigger();
   if (status && e == 0) *status = 0u;
+  // the fused decode FFN's completion counts start at zero
+  for (int i = e; i < nsync; i += blockDim.x) sync[i] = 0;
   int c = 0;
   if (e < E) {
     if (chunk_counts) {
@@ -175,7 +178,7 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
                                                          int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos,
                                                          int32_t* __restrict__ seg_start, RowTile* __restrict__ tiles,
                                                          int32_t* __restrict__ rt_base, uint32_t* __restrict__ status,
-                                                         int nt) {
+                                                         int nt, int32_t* __restrict__ sync, int nsync) {
   extern __shared__ uint32_t sbm[];  // [E][W] bitmaps, then the ids [T*k], then the offsets [E]
   __shared__ int sh[32];
   const int W = (T + 31) / 32;
@@ -185,6 +188,8 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
   pdl_wait();
   pdl_trigger();
   if (status && threadIdx.x == 0) *status = 0u;
+  // the fused decode FFN's completion counts start at zero
+  for (int i = threadIdx.x; i < nsync; i += blockDim.x) sync[i] = 0;
   for (int i = threadIdx.x; i < E * W; i += blockDim.x) sbm[i] = 0u;
   for (int p = threadIdx.x; p < P; p += blockDim.x) sidx[p] = idx[p];
   __syncthreads();
@@ -254,7 +259,7 @@ bool dispatch_fits_one_cta(const moe_config& c) {
 
 cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32_t* counts, int32_t* offsets,
                                   int32_t* perm, int32_t* pair_pos, int32_t* seg_start, RowTile* tiles,
-                                  int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
+                                  int32_t* rt_base, uint32_t* status, int32_t* sync, cudaStream_t st, bool pdl) {
   if (!dispatch_fits_one_cta(c)) return cudaErrorNotSupported;
   const size_t smem = ((size_t)c.E * ((c.T + 31) / 32) + (size_t)c.T * c.k + c.E) * 4;
   static PerDeviceOnce attr;
@@ -264,7 +269,8 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
   });
   if (e != cudaSuccess) return e;
   return launch_k(k_dispatch_small, dim3(1), dim3(1024), smem, st, pdl, idx, c.T, c.k, c.E, counts, offsets, perm,
-                  pair_pos, seg_start, tiles, rt_base, status, tile_rows(c));
+                  pair_pos, seg_start, tiles, rt_base, status, tile_rows(c), sync,
+                  sync ? (int)ffn_sync_ints(c) : 0);
 }
 
 int dispatch_chunks(const moe_config& c) { return (c.T + kChunkTokens - 1) / kChunkTokens; }
@@ -284,9 +290,10 @@ cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, con
 
 cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, int32_t* counts_out,
                              const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
-                             int32_t* rt_base, uint32_t* status, cudaStream_t st, bool pdl) {
+                             int32_t* rt_base, uint32_t* status, int32_t* sync, cudaStream_t st, bool pdl) {
   return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, chunk_counts, dispatch_chunks(c), counts_out,
-                  offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status, tile_rows(c));
+                  offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status, tile_rows(c), sync,
+                  sync ? (int)ffn_sync_ints(c) : 0);
 }
 
 }  // namespace moe

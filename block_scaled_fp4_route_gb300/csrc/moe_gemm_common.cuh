@@ -1,0 +1,147 @@
+// Pieces shared by the decode expert GEMM (moe_gemm.cu) and the fused decode
+// expert FFN (moe_ffn_decode.cu): the 64-row-tile configuration, the kernel
+// arguments, the soft cap and SiLU of the gated epilogue, and the mapping of a
+// tile index to (expert, weight block, row tile).
+#pragma once
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// internal linkage: every translation unit that includes this gets its own copy
+namespace {
+
+template <int FMT, bool GATED>
+struct Cfg {
+  static constexpr int NA = 2;                              // weight blocks per tile
+  static constexpr int ROWS = GATED ? 128 : 256;            // output features per tile
+  static constexpr int NT = kNTDecode;                      // token rows per tile
+  static constexpr int ACC_BUFS = 2;                        // TMEM accumulator buffers
+  static constexpr int EPI_WARPS = 4;                       // one warp per TMEM lane quadrant
+  static constexpr int THREADS = (4 + EPI_WARPS) * 32;
+  static constexpr int STAGES = FMT == MOE_FMT_NVFP4 ? 4 : 5;
+  static constexpr int A_BYTES = 128 * 128;
+  static constexpr int B_BYTES = NT * 128;
+  static constexpr int SF_ATOMS = FMT == MOE_FMT_NVFP4 ? 4 : 1;  // 512-byte atoms per operand per stage
+  static constexpr int SF_BYTES = SF_ATOMS * 512;
+  static constexpr int RAW_STAGE = NA * A_BYTES + B_BYTES + (NA + 1) * SF_BYTES;
+  static constexpr int STAGE_BYTES = (RAW_STAGE + 1023) / 1024 * 1024;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int RTB_BYTES = (kMaxE + 1) * 4;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + BAR_BYTES + RTB_BYTES + 1024;
+  static constexpr int ELEMS_PER_STAGE = FMT == MOE_FMT_NVFP4 ? 256 : 128;  // 128 bytes of codes
+  static constexpr int BLOCK = FMT == MOE_FMT_NVFP4 ? 16 : 32;
+  static constexpr int ACC_COLS = NT;            // one accumulator: 128 lanes x N columns
+  static constexpr int ACC_BUF = NA * ACC_COLS;  // both weight blocks of one tile
+  static constexpr int SF_COLS_OP = SF_ATOMS * 4;
+  static constexpr int SF_COLS_STAGE = (NA + 1) * SF_COLS_OP;
+  static constexpr int TMEM_SF = ACC_BUFS * ACC_BUF;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(TMEM_SF + STAGES * SF_COLS_STAGE <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM <= 232448, "shared memory budget");
+  static_assert(16 * STAGES + 64 <= BAR_BYTES, "barrier area");
+};
+
+struct GemmArgs {
+  const uint8_t* sfA0;
+  const uint8_t* sfA1;
+  const uint8_t* sfB;
+  const float* gA0;
+  const float* gA1;
+  const float* gB;
+  const RowTile* tiles;
+  const int32_t* rt_base;
+  int E;
+  int NA;  // weight rows per expert (= output features; also the output row stride)
+  int K;   // reduction length in elements
+  float cap;
+  float inv_cap;  // fp32(1 / cap), 0 when cap == 0
+  __nv_bfloat16* h_out;  // NVFP4: bf16 h (quantised by a row pass: its global spans the row)
+  uint8_t* hq_codes;     // MXFP8: h codes and scales written by the epilogue
+  uint8_t* hq_scales;
+  int mx_mode;
+  float* y_out;
+  uint32_t* status;
+  long long limit;
+  int withhold_loads;
+};
+
+// tanh for the soft cap c * tanh(v / c), in fp32 to a few ulp: below 0.5 the
+// odd Taylor series of tanh through the x^15 term (alternating, so the
+// truncation error is under the first dropped term, 9e-9 relative at 0.5);
+// above, 1 - 2 / (e^{2|x|} + 1), which has no cancellation there, with the
+// hardware base-2 exponential and reciprocal.
+__device__ __forceinline__ float tanh_soft(float x) {
+  const float ax = fabsf(x);
+  if (ax < 0.5f) {
+    const float x2 = x * x;
+    float p = -929569.0f / 638512875.0f;
+    p = fmaf(p, x2, 21844.0f / 6081075.0f);
+    p = fmaf(p, x2, -1382.0f / 155925.0f);
+    p = fmaf(p, x2, 62.0f / 2835.0f);
+    p = fmaf(p, x2, -17.0f / 315.0f);
+    p = fmaf(p, x2, 2.0f / 15.0f);
+    p = fmaf(p, x2, -1.0f / 3.0f);
+    return fmaf(x * x2, p, x);
+  }
+  const float e = ex2_approx(2.8853900817779268f * ax);  // e^{2|x|}; +inf for large |x|
+  return copysignf(1.0f - 2.0f * rcp_approx(e + 1.0f), x);
+}
+
+// silu(g) = g / (1 + e^{-g}), with the hardware base-2 exponential and
+// reciprocal (a few ulp; -0 for large negative g, g for large positive g).
+__device__ __forceinline__ float silu(float g) {
+  return g * rcp_approx(1.0f + ex2_approx(-1.4426950408889634f * g));
+}
+
+// Tile t -> (expert e, weight-row block mt, row tile index rt) in the order
+// expert, mt, token block.  rtb[e] is the first row tile of expert e.
+__device__ __forceinline__ void map_tile(int t, int MT, const int32_t* rtb, int E, int& mt, int& rt) {
+  int lo = 0, hi = E;  // rtb[lo]*MT <= t < rtb[hi]*MT
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (rtb[mid] * MT <= t) lo = mid;
+    else hi = mid;
+  }
+  const int nrt = rtb[lo + 1] - rtb[lo];
+  const int l = t - rtb[lo] * MT;
+  mt = l / nrt;
+  rt = rtb[lo] + l % nrt;
+}
+
+// A tile descriptor through L2 (it may be read before this grid's dependency
+// wait, when this SM's L1 could still hold an older copy).
+__device__ __forceinline__ RowTile load_tile(const RowTile* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  return RowTile{v.x, v.y, v.z, v.w};
+}
+
+inline GemmArgs gemm_args(const GemmLaunch& g) {
+  GemmArgs a;
+  a.sfA0 = g.sfA0;
+  a.sfA1 = g.sfA1;
+  a.sfB = g.sfB;
+  a.gA0 = g.gA0;
+  a.gA1 = g.gA1;
+  a.gB = g.gB;
+  a.tiles = g.tiles;
+  a.rt_base = g.rt_base;
+  a.E = g.E;
+  a.NA = g.NA;
+  a.K = g.K;
+  a.cap = g.cfg->swiglu_cap;
+  a.inv_cap = a.cap > 0.0f ? 1.0f / a.cap : 0.0f;
+  a.h_out = g.h_out;
+  a.hq_codes = g.hq_codes;
+  a.hq_scales = g.hq_scales;
+  a.mx_mode = g.cfg->mx_scale_mode;
+  a.y_out = g.y_out;
+  a.status = g.status;
+  a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock
+  a.withhold_loads = g.withhold_loads;
+  return a;
+}
+
+}  // namespace
+
+}  // namespace moe

@@ -103,7 +103,13 @@ typedef enum { MOE_SCALES_ROWMAJOR = 0, MOE_SCALES_TILED = 1 } moe_scale_layout;
  *   bias_in_weights: 0 (default) = the router bias steers selection only and
  *     the weights normalise the unbiased sigmoid scores; 1 = weights
  *     normalise the biased keys.
- *   routed_scale: multiplies the normalised routing weights (default 1). */
+ *   routed_scale: multiplies the normalised routing weights (default 1).
+ *   ffn_schedule: how the expert FFN runs for decode batches (64-row token
+ *     tiles, T * k < 64 * E): 0 (default) = from 64 pairs (T * k >= 64) one
+ *     persistent kernel for GEMM1, the h quantisation and GEMM2, a down
+ *     tile starting as soon as its h rows exist, separate kernels below;
+ *     1 = separate kernels always.  The results are the same bit for bit.
+ *     Prefill batches always use separate kernels. */
 typedef struct {
   int T, H, E, k, F;
   moe_format fmt;
@@ -112,6 +118,7 @@ typedef struct {
   int mx_scale_mode;
   int bias_in_weights;
   float routed_scale;
+  int ffn_schedule;
 } moe_config;
 
 /* One quantised expert matrix for all E experts (device pointers).
@@ -242,8 +249,9 @@ MOE_API moe_status moe_forward(const moe_config* cfg, const void* x_dev, const v
                        void* ws_dev, size_t ws_bytes, void* stream);
 
 /* Number of kernels one moe_forward call launches for this configuration
- * (2 router + 1 or 3 dispatch + x quantisation + GEMM1 + h quantisation
- * unless GEMM1 did it + GEMM2 + combine).  Host-only; no device is touched.
+ * (2 or 3 router + 1 or 3 dispatch + x quantisation + either the fused
+ * decode FFN, or GEMM1 + h quantisation unless GEMM1 did it + GEMM2; +
+ * combine).  Host-only; no device is touched.
  * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE as moe_forward's checks. */
 MOE_API moe_status moe_forward_kernel_count(const moe_config* cfg, int* count);
 
@@ -350,9 +358,23 @@ MOE_API moe_status moe_bench_mma_peak(moe_format fmt, int64_t mmas_per_cta, unsi
 MOE_API moe_status moe_selftest_bounded_wait(const moe_config* cfg, const moe_qweight* gate, const moe_qweight* up,
                                              void* ws_dev, size_t ws_bytes, int64_t limit_cycles, void* stream);
 
+/* Test hook for the fused decode FFN's dependency waits (decode batches,
+ * 64-row tiles; a moe_forward or moe_expert_ffn must have run on the
+ * workspace): launches the fused kernel with its gate/up tiles' completion
+ * reports withheld and every bounded wait limited to limit_cycles (1000 ..
+ * 4e9) SM cycles, so that the down tiles' waits for their h rows run out and
+ * the kernel exits with a timeout bit in the workspace status word
+ * (moe_poll_device_status: MOE_ERR_DEVICE_TIMEOUT).  The device stays
+ * usable; the workspace's y rows are unspecified afterwards. */
+MOE_API moe_status moe_selftest_dependency_wait(const moe_config* cfg, const moe_qweight* gate,
+                                                const moe_qweight* up, const moe_qweight* down, void* ws_dev,
+                                                size_t ws_bytes, int64_t limit_cycles, void* stream);
+
 /* Byte offsets of the layer's intermediates inside the workspace, for
  * inspection by tests (all buffers in padded expert-row order: each expert's
- * rows start at a multiple of tile_rows = NT).  R = padded row capacity.  The
+ * rows start at a multiple of tile_rows = NT).  R = padded row capacity.
+ * ffn_sync: the fused decode FFN's counters (per row tile a completion count
+ * and a ready flag, a tile counter, per padded row the |h| maximum).  The
  * activation block scales (xq_scales, hq_scales) use one 512-byte atom per
  * NT-row tile and 4 scale columns: row r, column c at
  *   ((r/NT)*(C/4) + c/4)*512 + (r%NT%32)*16 + (r%NT/32)*4 + c%4.
@@ -362,7 +384,7 @@ typedef struct {
   int64_t R;
   int64_t tile_rows; /* token rows per expert tile: 64 (decode) or 128 */
   size_t status, logits, topk_idx, topk_w, counts, offsets, perm, pair_pos, bitmap, seg_start,
-      tiles, rt_base, xq_codes, xq_scales, xq_global, h_bf16, hq_codes, hq_scales, hq_global,
+      tiles, rt_base, ffn_sync, xq_codes, xq_scales, xq_global, h_bf16, hq_codes, hq_scales, hq_global,
       y_perm, total;
 } moe_ws_layout;
 MOE_API moe_status moe_workspace_layout(const moe_config* cfg, moe_ws_layout* layout);

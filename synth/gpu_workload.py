@@ -17,7 +17,7 @@ def workload(spec) -> dict:
 
 class GpuWorkload:
     def __init__(self, spec, torch, device="cuda", cap=10.0, mx_scale_mode=0, chunk_experts=8,
-                 with_weights=True, act_static=None, bias_in_weights=0, routed_scale=1.0):
+                 with_weights=True, act_static=None, bias_in_weights=0, routed_scale=1.0, ffn_schedule=0):
         import block_scaled_fp4_route_gb300 as moe
         self.torch = torch
         self.moe = moe
@@ -30,7 +30,8 @@ class GpuWorkload:
         self.route_opts = dict(bias_in_weights=bool(bias_in_weights), routed_scale=float(routed_scale))
         self.cfg = moe.make_config(T, H, E, k, F, w["fmt"], swiglu_cap=cap, mx_scale_mode=mx_scale_mode,
                                    act_global_mode=0 if act_static is None else 1,
-                                   bias_in_weights=int(bias_in_weights), routed_scale=routed_scale)
+                                   bias_in_weights=int(bias_in_weights), routed_scale=routed_scale,
+                                   ffn_schedule=ffn_schedule)
         self.x = synth.dev_x(w, torch, device)
         self.w_router = synth.dev_router_weight(w, torch, device)
         self.bias = torch.from_numpy(synth.router_bias(w)).to(device)

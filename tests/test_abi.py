@@ -69,7 +69,7 @@ def test_workspace_size_and_layout():
     (dict(T=0), 2), (dict(T=70000), 2), (dict(k=0), 2), (dict(k=33), 2), (dict(E=4, k=8), 2),
     (dict(E=2000), 2), (dict(H=4608 + 128), 2), (dict(F=128), 2), (dict(fmt="mxfp8", F=128 + 64), 2),
     (dict(swiglu_cap=-1.0), 1), (dict(mx_scale_mode=2), 1), (dict(act_global_mode=2), 1),
-    (dict(fmt="mxfp8", act_global_mode=1), 1),
+    (dict(fmt="mxfp8", act_global_mode=1), 1), (dict(ffn_schedule=2), 1),
 ])
 def test_config_validation(kw, status):
     with pytest.raises(moe.MoeError) as ei:
@@ -134,9 +134,15 @@ def test_argument_validation_without_a_device():
 
 def test_forward_kernel_count():
     # router (2 for decode batches, 3 with tensor-core logits) + dispatch (1 for decode batches, else 3)
-    # + x quant + GEMM1 + h quant (unless GEMM1 quantises h) + GEMM2 + combine
-    assert moe.moe_forward_kernel_count(cfg()) == 8
-    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=192)) == 7
+    # + x quant + (decode batches: the fused expert FFN | GEMM1 + h quant (unless GEMM1 quantises h)
+    # + GEMM2) + combine
+    assert moe.moe_forward_kernel_count(cfg()) == 6
+    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=192)) == 6
+    assert moe.moe_forward_kernel_count(cfg(ffn_schedule=1)) == 8
+    assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=192, ffn_schedule=1)) == 7
+    assert moe.moe_forward_kernel_count(cfg(T=1024)) == 9         # tensor-core router, 3 dispatch kernels, fused
+    assert moe.moe_forward_kernel_count(cfg(T=7)) == 8            # 56 pairs: separate kernels
+    assert moe.moe_forward_kernel_count(cfg(T=8)) == 6            # 64 pairs: fused
     assert moe.moe_forward_kernel_count(cfg(T=4096)) == 11
     assert moe.moe_forward_kernel_count(cfg(fmt="mxfp8", T=16384)) == 10
     assert moe.moe_forward_kernel_count(cfg(T=4096, E=376)) == 10  # E % 16 != 0: CUDA-core router

@@ -18,11 +18,12 @@ FMT_NVFP4, FMT_MXFP8 = 0, 1
 SCALES_ROWMAJOR, SCALES_TILED = 0, 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
-          4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_ARCH", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_DEVICE_TIMEOUT"}
+          4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_ARCH", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_DEVICE_TIMEOUT",
+          8: "MOE_ERR_BOUNDS"}
 
 EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
-            "moe_route_noalloc", "moe_route_noalloc_poll_status", "moe_fake_quantize", "moe_kv_quantize_mxfp8", "moe_bench_mma_peak", "moe_selftest_bounded_wait", "moe_selftest_dependency_wait", "moe_forward_kernel_count",
+            "moe_route_noalloc", "moe_route_noalloc_poll_status", "moe_fake_quantize", "moe_kv_quantize_mxfp8", "moe_bench_mma_peak", "moe_selftest_bounded_wait", "moe_selftest_dependency_wait", "moe_debug_bounds_status", "moe_forward_kernel_count",
             "moe_status_string"]
 
 
@@ -52,16 +53,27 @@ class moe_ws_layout(ctypes.Structure):
     _fields_ = [("R", ctypes.c_int64), ("tile_rows", ctypes.c_int64)] + [(f, ctypes.c_size_t) for f in _LAYOUT_FIELDS]
 
 
-_lib = None
+_libs = {}
 _lock = threading.Lock()
+_debug_bounds = False
 
 
-def lib():
-    """Build (if stale) and load libmoe.so; raises if that is not possible."""
-    global _lib
+def use_debug_bounds_build(on: bool = True):
+    """Route every entry point of this module to the bounds-checked build
+    (libmoe_debug.so: kernels check the indices they derive from data and skip
+    out-of-range accesses, reported by moe_debug_bounds_status) or back to the
+    normal build."""
+    global _debug_bounds
+    _debug_bounds = bool(on)
+
+
+def lib(debug_bounds=None):
+    """Build (if stale) and load libmoe.so (or the bounds-checked build);
+    raises if that is not possible."""
+    db = _debug_bounds if debug_bounds is None else bool(debug_bounds)
     with _lock:
-        if _lib is None:
-            path = _build.build()
+        if db not in _libs:
+            path = _build.build(debug_bounds=db)
             L = ctypes.CDLL(path)
             P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
             cfgp = ctypes.POINTER(moe_config)
@@ -90,15 +102,16 @@ def lib():
             L.moe_workspace_layout.argtypes = [cfgp, ctypes.POINTER(moe_ws_layout)]
             L.moe_status_string.argtypes = [ctypes.c_int]
             L.moe_status_string.restype = ctypes.c_char_p
+            L.moe_debug_bounds_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
             for n in EXPORTED[:-1]:
                 getattr(L, n).restype = ctypes.c_int
-            _lib = L
-        return _lib
+            _libs[db] = L
+        return _libs[db]
 
 
 def library_path() -> str:
-    """Path of the in-tree libmoe.so (built by lib() when stale)."""
-    return _build.LIB
+    """Path of the in-tree library the entry points use (built by lib() when stale)."""
+    return _build.LIB_DEBUG if _debug_bounds else _build.LIB
 
 
 def _check(fn: str, st: int):
@@ -309,6 +322,16 @@ def moe_pack_scales(rowmajor, rows, scale_cols, tiled, stream=None):
 def moe_poll_device_status(ws, stream=None) -> int:
     """Synchronises the stream; returns the status code (0 = no timeout)."""
     return int(lib().moe_poll_device_status(_ptr(ws), _stream(stream)))
+
+
+def moe_debug_bounds_status(stream=None, with_site=False):
+    """(status, checked[, site]): synchronises the stream and reads / clears the index-check flags
+    of the bounds-checked build (status 8 = MOE_ERR_BOUNDS: a check failed and its access was
+    skipped; site = the source line of a failed check); checked = 0 for the normal build, which
+    has no checks."""
+    c, site = ctypes.c_int(0), ctypes.c_int(0)
+    st = int(lib().moe_debug_bounds_status(_stream(stream), ctypes.byref(c), ctypes.byref(site)))
+    return (st, c.value, site.value) if with_site else (st, c.value)
 
 
 def moe_status_string(status: int) -> str:

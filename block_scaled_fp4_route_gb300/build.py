@@ -17,6 +17,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libmoe.so")
+# the bounds-checked variant (-DMOE_DEBUG_BOUNDS): its kernels check the
+# indices they derive from data and skip out-of-range accesses, flagging them
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libmoe_debug.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["moe_api.cu", "moe_route.cu", "moe_route_tc.cu", "moe_dispatch.cu", "moe_quant.cu", "moe_gemm.cu", "moe_combine.cu",
@@ -48,17 +52,21 @@ def _key(cc: str, defines=()) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug_bounds: bool = False) -> str:
+    """Compile libmoe.so (or, with debug_bounds, the bounds-checked
+    libmoe_debug.so) unless its stamp matches the sources and flags."""
+    out_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug_bounds else (BUILD, LIB)
+    defines = ["-DMOE_DEBUG_BOUNDS"] if debug_bounds else []
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    key = _key(cc)
-    stamp = LIB + ".key"
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read().strip() == key:
-        return LIB
+    key = _key(cc, defines)
+    stamp = lib + ".key"
+    if not force and os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read().strip() == key:
+        return lib
 
     def one(src):
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -68,16 +76,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"link of libmoe.so failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
     with open(stamp, "w") as fh:
         fh.write(key + "\n")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

@@ -2,10 +2,19 @@
 // layout, TMA descriptors, and the chaining of the kernels on the caller's
 // stream.  Allocates no device memory.
 #include <mutex>
+#include <vector>
 
 #include "moe_common.cuh"
 
 namespace moe {
+
+#ifdef MOE_DEBUG_BOUNDS
+static std::vector<BoundsReader>& bounds_readers() {
+  static std::vector<BoundsReader> v;
+  return v;
+}
+void register_bounds_reader(BoundsReader r) { bounds_readers().push_back(r); }
+#endif
 
 namespace {
 
@@ -409,9 +418,12 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   int32_t* pair_pos = at<int32_t>(ws_dev, L.pair_pos);
   float* y = at<float>(ws_dev, L.y_perm);
   mark(ev, 0, st);
-  // the router's first kernel clears the status word of the call
+  // the router's first kernel clears the status word of the call.  It is
+  // launched behind whatever precedes it on the stream (a previous layer's
+  // combine, in a serving loop) and waits for it before its first access, so
+  // its launch overlaps that kernel's tail.
   if (launch_router(c, (const __nv_bfloat16*)x_dev, (const __nv_bfloat16*)w_router_dev, bias_dev,
-                    at<float>(ws_dev, L.logits), idx, w, at<uint32_t>(ws_dev, L.status), st, false) != cudaSuccess)
+                    at<float>(ws_dev, L.logits), idx, w, at<uint32_t>(ws_dev, L.status), st, true) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(ev, 1, st);
   s = dispatch_impl(c, idx, counts, offsets, perm, pair_pos, ws_dev, nullptr, st, true);
@@ -669,6 +681,27 @@ moe_status moe_selftest_dependency_wait(const moe_config* cfg, const moe_qweight
                                        (cudaStream_t)stream, false));
 }
 
+moe_status moe_debug_bounds_status(void* stream, int* checked, int* site) {
+  if (!checked) return MOE_ERR_INVALID_ARG;
+  if (site) *site = 0;
+#ifdef MOE_DEBUG_BOUNDS
+  *checked = 1;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t any = 0;
+  for (BoundsReader r : bounds_readers()) {
+    uint32_t v = 0;
+    if (r(&v) != cudaSuccess) return MOE_ERR_CUDA;
+    any = v > any ? v : any;
+  }
+  if (site) *site = (int)any;
+  return any ? MOE_ERR_BOUNDS : MOE_OK;
+#else
+  (void)stream;
+  *checked = 0;
+  return MOE_OK;
+#endif
+}
+
 moe_status moe_poll_device_status(void* ws_dev, void* stream) {
   if (!ws_dev) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = (cudaStream_t)stream;
@@ -693,6 +726,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "a device-side bounded wait ran out";
+    case MOE_ERR_BOUNDS: return "an index check of the bounds-checked build failed (the access was skipped)";
   }
   return "unknown status";
 }

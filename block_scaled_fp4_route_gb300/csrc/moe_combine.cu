@@ -33,7 +33,11 @@ __global__ void __launch_bounds__(kCombThreads) k_combine(const float* __restric
     float4 v[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (j0 + i < k) v[i] = __ldcs(reinterpret_cast<const float4*>(y + (int64_t)pos[j0 + i] * H) + c);
+      if (j0 + i < k) {
+        v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (MOE_IN_BOUNDS((unsigned)pos[j0 + i] < (unsigned)(gridDim.x * k)))
+          v[i] = __ldcs(reinterpret_cast<const float4*>(y + (int64_t)pos[j0 + i] * H) + c);
+      }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       if (j0 + i < k) {

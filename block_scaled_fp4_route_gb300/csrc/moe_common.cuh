@@ -53,6 +53,45 @@ enum : uint32_t {
 };
 
 // ----------------------------------------------------------------------------
+// Bounds-checked build (-DMOE_DEBUG_BOUNDS): the indices the kernels derive
+// from data (pair positions, padded activation rows, canonical pair rows,
+// row-tile indices) are checked before the accesses they address.  A failed
+// check skips the access and sets this translation unit's device flag, which
+// moe_debug_bounds_status reads and clears; nothing traps.  Without the macro
+// MOE_IN_BOUNDS(cond) is `true` and the condition is not evaluated.
+// ----------------------------------------------------------------------------
+#ifdef MOE_DEBUG_BOUNDS
+namespace {
+__device__ uint32_t g_bounds_flag;  // one per translation unit
+}  // namespace
+// the flag holds the largest source line of a failed check (0: none)
+__device__ __forceinline__ bool bounds_check(bool ok, uint32_t line) {
+  if (!ok) atomicMax(&g_bounds_flag, line);
+  return ok;
+}
+#define MOE_IN_BOUNDS(cond) (::moe::bounds_check((cond), __LINE__))
+// host: every translation unit registers a reader of its flag
+using BoundsReader = cudaError_t (*)(uint32_t* value);
+void register_bounds_reader(BoundsReader r);
+namespace {
+inline cudaError_t read_and_clear_bounds_flag(uint32_t* v) {
+  cudaError_t e = cudaMemcpyFromSymbol(v, g_bounds_flag, sizeof(uint32_t));
+  if (e == cudaSuccess && *v != 0u) {
+    const uint32_t zero = 0u;
+    e = cudaMemcpyToSymbol(g_bounds_flag, &zero, sizeof(uint32_t));
+  }
+  return e;
+}
+struct BoundsRegistrar {
+  BoundsRegistrar() { register_bounds_reader(read_and_clear_bounds_flag); }
+};
+const BoundsRegistrar g_bounds_registrar;
+}  // namespace
+#else
+#define MOE_IN_BOUNDS(cond) (true)
+#endif
+
+// ----------------------------------------------------------------------------
 // TILED block-scale layout (see moe.h): 512-byte atoms of 128 rows x 4 scale
 // columns; inside an atom row r sits at lane r%32, 4-byte word (r/32)%4.
 // ----------------------------------------------------------------------------

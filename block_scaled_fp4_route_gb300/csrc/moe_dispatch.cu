@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ offsets_out, int32_t* __restrict__ seg_start,
                                                     RowTile* __restrict__ tiles, int32_t* __restrict__ rt_base,
                                                     uint32_t* __restrict__ status, int nt,
-                                                    int32_t* __restrict__ sync, int nsync) {
+                                                    int32_t* __restrict__ sync, int nsync, int max_tiles) {
   __shared__ int sh[32];
   const int e = threadIdx.x;
   pdl_wait();
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
       t.row = seg + nt * i;
       t.n_valid = min(nt, c - nt * i);
       t.canon = off + nt * i;
-      tiles[rt0 + i] = t;
+      if (MOE_IN_BOUNDS(rt0 + i < max_tiles)) tiles[rt0 + i] = t;
     }
   }
   if (e == 0) rt_base[E] = rtot;
@@ -156,10 +156,13 @@ __global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __res
       v &= v - 1;
       int t = (w0 + i) * 32 + b;
       int j = 0;
-      while (j < k && idx[t * k + j] != e) ++j;
+      if (MOE_IN_BOUNDS(t < T))
+        while (j < k && idx[t * k + j] != e) ++j;
       int p = base + rank;
-      perm[p] = t * k + j;
-      pair_pos[t * k + j] = p;
+      if (MOE_IN_BOUNDS(t < T && j < k && p < T * k)) {
+        perm[p] = t * k + j;
+        pair_pos[t * k + j] = p;
+      }
       ++rank;
     }
   }
@@ -221,7 +224,7 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
       tl.row = seg + nt * i;
       tl.n_valid = min(nt, c - nt * i);
       tl.canon = off + nt * i;
-      tiles[rt0 + i] = tl;
+      if (MOE_IN_BOUNDS(rt0 + i < (P + nt - 1) / nt + E)) tiles[rt0 + i] = tl;
     }
   }
   if (e == 0) {
@@ -243,8 +246,10 @@ __global__ void __launch_bounds__(1024) k_dispatch_small(const int32_t* __restri
     int rank = __popc(bm[t >> 5] & ((1u << (t & 31)) - 1u));
     for (int i = 0; i < (t >> 5); ++i) rank += __popc(bm[i]);
     const int pos = soff[ee] + rank;
-    perm[pos] = p;
-    pair_pos[p] = pos;
+    if (MOE_IN_BOUNDS(pos < P)) {
+      perm[pos] = p;
+      pair_pos[p] = pos;
+    }
   }
 }
 
@@ -293,7 +298,7 @@ cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, i
                              int32_t* rt_base, uint32_t* status, int32_t* sync, cudaStream_t st, bool pdl) {
   return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, chunk_counts, dispatch_chunks(c), counts_out,
                   offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status, tile_rows(c), sync,
-                  sync ? (int)ffn_sync_ints(c) : 0);
+                  sync ? (int)ffn_sync_ints(c) : 0, (int)max_row_tiles(c));
 }
 
 }  // namespace moe

@@ -143,7 +143,7 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
   // the tile plan is read before the dependency wait, as in k_moe_gemm
   for (int i = threadIdx.x; i <= a1.E; i += blockDim.x) s_rtb[i] = __ldcg(a1.rt_base + i);
   tc_fence_before();
-  __syncthreads();
+  const bool plan_ok = plan_ok_sync(s_rtb, a1.E, a1.max_tiles);
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   if (warp != 0) pdl_wait();
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
   const int E = a1.E;
   const int MT1 = (a1.NA + C::ROWS - 1) / C::ROWS;    // gate/up tiles per row tile (F / 128)
   const int MT2 = (a2.NA + C2::ROWS - 1) / C2::ROWS;  // down tiles per row tile (H / 256)
-  const int nrt = s_rtb[E];
+  const int nrt = plan_ok ? s_rtb[E] : 0;
   const int total1 = nrt * MT1;
   const int total = total1 + nrt * MT2;
   const int KB1 = a1.K / C::ELEMS_PER_STAGE, KB2 = a2.K / C::ELEMS_PER_STAGE;
@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
       // tiles are claimed one ahead: the next index is requested when a tile
       // starts and read when it ends, so the counter's round trip does not
       // stall the loads
-      int claimed = atomicAdd(sy.next_tile, 1);
+      // (a CTA that runs no tile, e.g. one whose plan failed its check in the
+      // bounds-checked build, takes no index from the counter)
+      int claimed = total > 0 ? atomicAdd(sy.next_tile, 1) : 0;
       for (int i = 0; ok; ++i) {
         // pass the claimed tile on (the slot is free once the MMA and the
         // epilogue have read the index kSchedDepth tiles back)
@@ -461,15 +463,16 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
               const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
               const uint32_t sc = m != 0.0f ? mx_scale_code(m, a1.mx_mode) : 0u;
               const uint32_t code = m != 0.0f ? e4m3_encode(__fmul_rn(v, exp2i(127 - (int)sc))) : 0u;
-              if (valid) a1.hq_codes[row * a1.NA + f] = (uint8_t)code;
-              if (valid && lane == 0)
-                a1.hq_scales[act_scale_offset(row, f >> 5, a1.NA >> 5, C::NT)] = (uint8_t)sc;
+              const bool ok = valid && MOE_IN_BOUNDS(row < a1.R);
+              if (ok) a1.hq_codes[row * a1.NA + f] = (uint8_t)code;
+              if (ok && lane == 0) a1.hq_scales[act_scale_offset(row, f >> 5, a1.NA >> 5, C::NT)] = (uint8_t)sc;
             } else {
-              if (valid) a1.h_out[row * a1.NA + f] = hb;
+              const bool ok = valid && MOE_IN_BOUNDS(row < a1.R);
+              if (ok) a1.h_out[row * a1.NA + f] = hb;
               // the row's |h| maximum over this warp's 32 features, for the
               // row pass (non-negative floats order like their bits)
               const uint32_t m = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(__bfloat162float(hb))));
-              if (valid && lane == 0 && !sy.act_static) atomicMax(sy.h_amax + row, m);
+              if (ok && lane == 0 && !sy.act_static) atomicMax(sy.h_amax + row, m);
             }
           }
           // the next chunk moves to the front (register moves, no indexing)
@@ -506,6 +509,7 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
           for (int idx = threadIdx.x - 128; idx < rt.n_valid * nb; idx += 128) {
             const int n = idx / nb, b = idx - n * nb;
             const int64_t row = (int64_t)rt.row + n;
+            if (!MOE_IN_BOUNDS(row < a1.R)) continue;
             const float G = stat ? __fdiv_rn(1.0f, sg) : nvfp4_G(__uint_as_float(__ldcg(sy.h_amax + row)));
             if (b == 0) sy.hq_global[row] = stat ? sg : __fdiv_rn(1.0f, G);
             float v[16];
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
           for (int j = 0; j < 16; ++j) {
             const int n = ch * 16 + j;
             const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
-            if (n < col_hi) {
+            if (n < col_hi && MOE_IN_BOUNDS(rt.canon + n < a2.P)) {
               float* yrow = a2.y_out + (int64_t)(rt.canon + n) * a2.NA;
               yrow[f] = __uint_as_float(r0[ch][j]) * (sA0 * gb);
               if (second) yrow[f + 128] = __uint_as_float(r1[ch][j]) * (sA1 * gb);

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
   // producer waits after it has requested its first weight stages.
   for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = __ldcg(a.rt_base + i);
   tc_fence_before();
-  __syncthreads();
+  const bool plan_ok = plan_ok_sync(s_rtb, a.E, a.max_tiles);
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // warp 0 stays out: a wait taken by some of its lanes would hold the
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
   if (warp != 0) pdl_wait();
 
   const int MT = (a.NA + C::ROWS - 1) / C::ROWS;
-  const int total = s_rtb[a.E] * MT;
+  const int total = plan_ok ? s_rtb[a.E] * MT : 0;
   const int KB = a.K / C::ELEMS_PER_STAGE;
   const int64_t atoms_per_row = (a.K / C::BLOCK) / 4;  // scale atoms per 128 weight rows or per token tile
 
@@ -350,10 +350,11 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
             const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
             const uint32_t sc = m != 0.0f ? mx_scale_code(m, a.mx_mode) : 0u;
             const uint32_t code = m != 0.0f ? e4m3_encode(__fmul_rn(v, exp2i(127 - (int)sc))) : 0u;
-            if (valid) a.hq_codes[row * a.NA + f] = (uint8_t)code;
-            if (valid && lane == 0) a.hq_scales[act_scale_offset(row, f >> 5, a.NA >> 5, C::NT)] = (uint8_t)sc;
+            const bool ok = valid && MOE_IN_BOUNDS(row < a.R);
+            if (ok) a.hq_codes[row * a.NA + f] = (uint8_t)code;
+            if (ok && lane == 0) a.hq_scales[act_scale_offset(row, f >> 5, a.NA >> 5, C::NT)] = (uint8_t)sc;
           } else {
-            if (valid) a.h_out[row * a.NA + f] = hb;
+            if (valid && MOE_IN_BOUNDS(row < a.R)) a.h_out[row * a.NA + f] = hb;
           }
         }
       };
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
           for (int j = 0; j < 16; ++j) {
             const int n = col_lo + ch * 16 + j;
             const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
-            if (n < col_hi) {
+            if (n < col_hi && MOE_IN_BOUNDS(rt.canon + n < a.P)) {
               float* yrow = a.y_out + (int64_t)(rt.canon + n) * a.NA;
               yrow[f] = __uint_as_float(r0[ch][j]) * (sA0 * gb);
               if (second) yrow[f + 128] = __uint_as_float(r1[ch][j]) * (sA1 * gb);
@@ -483,6 +484,7 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
     if (!valid) return;  // no warp-collective operation in the gated epilogue
     const bool capped = a.cap > 0.0f;
     const int64_t row = (int64_t)rt.row + n;
+    if (!MOE_IN_BOUNDS(row < a.R)) return;
     const int f0 = mt * ROWS + 64 * hc;  // first feature of this thread's share
     // two 32-feature blocks (one MXFP8 scale block each), one unrolled
 #pragma unroll 1
@@ -542,7 +544,9 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
     // y rows are written feature-contiguously: each 32 x 32 (token x
     // feature) group of the warp is transposed with xor shuffles, then
     // lane L stores feature L of one token row per instruction
-    const int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile
+    int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile
+    // (warp-uniform: the quadrant's rows are stored only if all are in range)
+    if (!MOE_IN_BOUNDS((int64_t)rt.canon + q * 32 + (nv > 32 ? 32 : nv) <= a.P)) nv = 0;
     float* ybase = a.y_out + ((int64_t)rt.canon + q * 32) * a.NA + mt * ROWS + 64 * hc + lane;
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch)
@@ -634,7 +638,7 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
   // the tile plan is read before the dependency wait, as in k_moe_gemm
   for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_rtb[i] = __ldcg(a.rt_base + i);
   tc_fence_before();
-  __syncthreads();
+  const bool plan_ok = plan_ok_sync(s_rtb, a.E, a.max_tiles);
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // warp 0 stays out: a wait taken by some of its lanes would hold the
@@ -642,7 +646,7 @@ __global__ void __launch_bounds__(CfgTM<FMT, GATED>::THREADS, 1)
   if (warp != 0) pdl_wait();
 
   const int MT = (a.NA + C::ROWS - 1) / C::ROWS;
-  const int total = s_rtb[a.E] * MT;
+  const int total = plan_ok ? s_rtb[a.E] * MT : 0;
   const int KB = a.K / C::ELEMS_PER_STAGE;
   const int64_t atoms_per_row = (a.K / C::BLOCK) / 4;  // scale atoms per 128 rows over K
 

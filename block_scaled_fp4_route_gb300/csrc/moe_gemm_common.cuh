@@ -64,7 +64,31 @@ struct GemmArgs {
   uint32_t* status;
   long long limit;
   int withhold_loads;
+  int64_t R;      // padded activation rows (h / x rows are below R)
+  int64_t P;      // pairs (canonical y rows are below P)
+  int max_tiles;  // capacity of the row-tile list
 };
+
+// The tile plan's row-tile prefix rtb[0..E] must be non-decreasing and end at
+// most at max_tiles.  Checked build: every thread of the CTA checks a share
+// after the plan is in shared memory (this replaces the __syncthreads that
+// follows the load), and a plan that fails runs no tile in any role.  Normal
+// build: the barrier only.
+__device__ __forceinline__ bool plan_ok_sync(const int32_t* s_rtb, int E, int max_tiles) {
+#ifdef MOE_DEBUG_BOUNDS
+  __syncthreads();  // every thread's share of the plan is in shared memory
+  int bad = 0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) bad |= s_rtb[i + 1] < s_rtb[i];
+  if (threadIdx.x == 0) bad |= s_rtb[0] != 0 || s_rtb[E] > max_tiles;
+  return MOE_IN_BOUNDS(!__syncthreads_or(bad));
+#else
+  (void)s_rtb;
+  (void)E;
+  (void)max_tiles;
+  __syncthreads();
+  return true;
+#endif
+}
 
 // tanh for the soft cap c * tanh(v / c), in fp32 to a few ulp: below 0.5 the
 // odd Taylor series of tanh through the x^15 term (alternating, so the
@@ -139,6 +163,9 @@ inline GemmArgs gemm_args(const GemmLaunch& g) {
   a.status = g.status;
   a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock
   a.withhold_loads = g.withhold_loads;
+  a.R = padded_rows(*g.cfg);
+  a.P = (int64_t)g.cfg->T * g.cfg->k;
+  a.max_tiles = (int)max_row_tiles(*g.cfg);
   return a;
 }
 

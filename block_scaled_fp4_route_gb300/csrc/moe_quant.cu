@@ -186,7 +186,8 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ pair_pos,
                                                        const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                       uint8_t* scales, float* glob, const float* act_static, int nt) {
+                                                       uint8_t* scales, float* glob, const float* act_static, int nt,
+                                                       int E, int64_t R) {
   __shared__ float red[32];
   __shared__ int64_t dst[kMaxK];
   __shared__ float sg[kMaxK];
@@ -198,11 +199,32 @@ __global__ void __launch_bounds__(kQThreads) k_quant_x(const __nv_bfloat16* __re
   if (threadIdx.x < k) {
     const int pid = t * k + threadIdx.x;
     const int e = idx[pid];
-    dst[threadIdx.x] = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
-    if (act_static) sg[threadIdx.x] = act_static[2 * e];
+    dst[threadIdx.x] = -1;
+    if (MOE_IN_BOUNDS((unsigned)e < (unsigned)E)) {
+      const int64_t d = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
+      if (MOE_IN_BOUNDS(d >= 0 && d < R)) dst[threadIdx.x] = d;
+      if (act_static) sg[threadIdx.x] = act_static[2 * e];
+    }
   }
   __syncthreads();
-  quant_row_encode<FMT>(v, m, H, mx_mode, k, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
+  int ndst = k;
+#ifdef MOE_DEBUG_BOUNDS
+  // drop the destinations that failed their check (their rows are not written)
+  __shared__ int s_ndst;
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int j = 0; j < k; ++j)
+      if (dst[j] >= 0) {
+        dst[n] = dst[j];
+        sg[n] = sg[j];
+        ++n;
+      }
+    s_ndst = n;
+  }
+  __syncthreads();
+  ndst = s_ndst;
+#endif
+  quant_row_encode<FMT>(v, m, H, mx_mode, ndst, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
 }
 
 // h: one CTA per canonical pair position p; row = its padded row.
@@ -212,7 +234,8 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
                                                        const int32_t* __restrict__ offsets,
                                                        const int32_t* __restrict__ perm,
                                                        const int32_t* __restrict__ seg_start, uint8_t* codes,
-                                                       uint8_t* scales, float* glob, const float* act_static, int nt) {
+                                                       uint8_t* scales, float* glob, const float* act_static, int nt,
+                                                       int E, int64_t R, int P) {
   __shared__ float red[32];
   __shared__ int64_t dst[1];
   __shared__ float sg[1];
@@ -221,13 +244,23 @@ __global__ void __launch_bounds__(kQThreads) k_quant_h(const __nv_bfloat16* __re
   // completed before the previous kernel's threads passed their own
   // dependency wait: looked up (through L2) before this one's.
   if (threadIdx.x == 0) {
-    const int e = __ldcg(idx + __ldcg(perm + p));
-    dst[0] = (int64_t)__ldcg(seg_start + e) + (p - __ldcg(offsets + e));
-    if (act_static) sg[0] = act_static[2 * e + 1];
+    dst[0] = -1;
+    const int pid = __ldcg(perm + p);
+    if (MOE_IN_BOUNDS((unsigned)pid < (unsigned)P)) {
+      const int e = __ldcg(idx + pid);
+      if (MOE_IN_BOUNDS((unsigned)e < (unsigned)E)) {
+        const int64_t d = (int64_t)__ldcg(seg_start + e) + (p - __ldcg(offsets + e));
+        if (MOE_IN_BOUNDS(d >= 0 && d < R)) dst[0] = d;
+        if (act_static) sg[0] = act_static[2 * e + 1];
+      }
+    }
   }
   pdl_wait();
   pdl_trigger();
   __syncthreads();
+#ifdef MOE_DEBUG_BOUNDS
+  if (dst[0] < 0) return;  // the whole CTA: its row failed a check
+#endif
   quant_row_regs<FMT>(h + dst[0] * F, F, mx_mode, 1, dst, act_static ? sg : nullptr, codes, scales, glob, red, nt);
 }
 
@@ -240,31 +273,61 @@ __global__ void __launch_bounds__(256) k_quant_rows_warp(const __nv_bfloat16* __
                                                          const int32_t* __restrict__ perm,
                                                          const int32_t* __restrict__ seg_start, uint8_t* codes,
                                                          uint8_t* scales, float* glob, const float* act_static,
-                                                         int nt) {
+                                                         int nt, int E, int64_t R, int P) {
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_wait();
   pdl_trigger();
   if (r >= rows) return;  // whole warp
-  int64_t dst = 0;
+  int64_t dst = -1;
   float sg = 0.0f;
   const __nv_bfloat16* row;
   int ndst;
   if (is_h) {
-    const int e = idx[perm[r]];
-    dst = (int64_t)seg_start[e] + (r - offsets[e]);
-    if (act_static) sg = act_static[2 * e + 1];
+    const int pid = perm[r];
+    if (MOE_IN_BOUNDS((unsigned)pid < (unsigned)P)) {
+      const int e = idx[pid];
+      if (MOE_IN_BOUNDS((unsigned)e < (unsigned)E)) {
+        const int64_t d = (int64_t)seg_start[e] + (r - offsets[e]);
+        if (MOE_IN_BOUNDS(d >= 0 && d < R)) dst = d;
+        if (act_static) sg = act_static[2 * e + 1];
+      }
+    }
+#ifdef MOE_DEBUG_BOUNDS
+    if (dst < 0) return;  // whole warp (every lane holds the same row)
+#endif
     row = src + dst * K;
     ndst = 1;
   } else {
     if (lane < k) {
       const int pid = r * k + lane;
       const int e = idx[pid];
-      dst = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
-      if (act_static) sg = act_static[2 * e];
+      if (MOE_IN_BOUNDS((unsigned)e < (unsigned)E)) {
+        const int64_t d = (int64_t)seg_start[e] + (pair_pos[pid] - offsets[e]);
+        if (MOE_IN_BOUNDS(d >= 0 && d < R)) dst = d;
+        if (act_static) sg = act_static[2 * e];
+      }
     }
     row = src + (int64_t)r * K;
     ndst = k;
+#ifdef MOE_DEBUG_BOUNDS
+    // drop the destinations that failed their check: lane d takes the d-th
+    // valid one
+    const unsigned ok = __ballot_sync(0xffffffffu, lane < k && dst >= 0);
+    int64_t d2 = -1;
+    float s2 = 0.0f;
+    for (int j = 0; j < 32; ++j) {
+      const int64_t dj = __shfl_sync(0xffffffffu, dst, j);
+      const float sj = __shfl_sync(0xffffffffu, sg, j);
+      if (((ok >> j) & 1u) && lane == __popc(ok & ((1u << j) - 1u))) {
+        d2 = dj;
+        s2 = sj;
+      }
+    }
+    dst = d2;
+    sg = s2;
+    ndst = __popc(ok);
+#endif
   }
   quant_row_warp<FMT>(row, K, mx_mode, ndst, dst, sg, act_static != nullptr, codes, scales, glob, nt);
 }
@@ -394,11 +457,12 @@ cudaError_t launch_quant_x(const moe_config& c, const __nv_bfloat16* x, const in
   if (c.T >= kWarpRowsFrom) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((c.T + 7) / 8), dim3(256), 0, st, pdl, x, c.T, c.H, c.k, 0, c.mx_scale_mode, idx, offsets,
-                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob, act_static, tile_rows(c));
+                    pair_pos, (const int32_t*)nullptr, seg_start, codes, scales, glob, act_static, tile_rows(c), c.E,
+                    padded_rows(c), c.T * c.k);
   }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_x<MOE_FMT_NVFP4> : k_quant_x<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(c.T), dim3(kQThreads), 0, st, pdl, x, c.H, c.k, c.mx_scale_mode, idx, offsets, pair_pos,
-                  seg_start, codes, scales, glob, act_static, tile_rows(c));
+                  seg_start, codes, scales, glob, act_static, tile_rows(c), c.E, padded_rows(c));
 }
 
 cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const int32_t* idx, const int32_t* offsets,
@@ -408,11 +472,12 @@ cudaError_t launch_quant_h(const moe_config& c, const __nv_bfloat16* h, const in
   if (P >= kWarpRowsFromH) {
     auto kw = c.fmt == MOE_FMT_NVFP4 ? k_quant_rows_warp<MOE_FMT_NVFP4> : k_quant_rows_warp<MOE_FMT_MXFP8>;
     return launch_k(kw, dim3((P + 7) / 8), dim3(256), 0, st, pdl, h, P, c.F, c.k, 1, c.mx_scale_mode, idx, offsets,
-                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob, act_static, tile_rows(c));
+                    (const int32_t*)nullptr, perm, seg_start, codes, scales, glob, act_static, tile_rows(c), c.E,
+                    padded_rows(c), P);
   }
   auto kern = c.fmt == MOE_FMT_NVFP4 ? k_quant_h<MOE_FMT_NVFP4> : k_quant_h<MOE_FMT_MXFP8>;
   return launch_k(kern, dim3(P), dim3(kQThreads), 0, st, pdl, h, c.F, c.mx_scale_mode, idx, offsets, perm, seg_start,
-                  codes, scales, glob, act_static, tile_rows(c));
+                  codes, scales, glob, act_static, tile_rows(c), c.E, padded_rows(c), P);
 }
 
 cudaError_t launch_quantize(moe_format fmt, int mx_mode, int src_fp32, const void* src, int64_t rows, int64_t cols,

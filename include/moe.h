@@ -57,7 +57,8 @@ typedef enum {
   MOE_ERR_WORKSPACE_TOO_SMALL = 4,
   MOE_ERR_ARCH = 5,
   MOE_ERR_CUDA = 6,
-  MOE_ERR_DEVICE_TIMEOUT = 7
+  MOE_ERR_DEVICE_TIMEOUT = 7,
+  MOE_ERR_BOUNDS = 8
 } moe_status;
 
 /* Expert weight / activation encodings [CB Checkpoints; TS Checkpoint row;
@@ -347,6 +348,20 @@ MOE_API moe_status moe_poll_device_status(void* ws_dev, void* stream);
  * Allocates nothing. */
 MOE_API moe_status moe_bench_mma_peak(moe_format fmt, int64_t mmas_per_cta, unsigned long long* cycles_dev,
                                       void* status_dev, int* ctas, double* flops_per_mma, void* stream);
+
+/* Index checks of the bounds-checked build.  The library can be built with
+ * MOE_DEBUG_BOUNDS defined (a separate libmoe_debug.so): the indices its
+ * kernels derive from data (pair positions, padded activation rows, canonical
+ * pair rows, row-tile indices) are then checked before the accesses they
+ * address, and a failed check skips the access and sets a device flag
+ * instead of reading or writing out of bounds (nothing traps).  This call
+ * synchronises `stream`, then reads and clears the flags of the current
+ * device: MOE_ERR_BOUNDS if a check failed since the last call, MOE_OK
+ * otherwise.  *checked = 1 in the checked build; in the normal build
+ * *checked = 0 and the call returns MOE_OK without touching the device.
+ * site (nullable): the source line of a failed check, for diagnosis (0 if
+ * none). */
+MOE_API moe_status moe_debug_bounds_status(void* stream, int* checked, int* site);
 
 /* Test hook for the device-side failure detection: launches the gate/up GEMM
  * over the tile plan already in the workspace (a moe_forward or

@@ -188,3 +188,13 @@ def test_kv_quantize_validation_without_a_device():
     assert call(tokens=0) == 0                      # nothing to do, nothing enqueued
     assert call(kv=ok + 8) == 3 and call(codes=ok + 4) == 3 and call(scales=None) == 1
     assert call(slot=ok + 4) == 3                   # int64 slots, 8-byte aligned
+
+
+def test_bounds_checked_build_exports_the_same_symbols():
+    D = moe.lib(debug_bounds=True)
+    for n in declared_functions():
+        assert hasattr(D, n), n
+    c = ctypes.c_int(-1)
+    site = ctypes.c_int(-1)
+    assert moe.lib().moe_debug_bounds_status(None, ctypes.byref(c), ctypes.byref(site)) == 0
+    assert c.value == 0 and site.value == 0

@@ -1,8 +1,10 @@
 """The prefill router (T > 256): tensor-core logits nominate the candidates,
 which are recomputed on CUDA cores.  Checks that the tensor-core logits stay
-far inside the error the candidate margin assumes (2^-11 ||x|| ||w_e||), and
-that routing matches the oracle on small shapes with ragged token and expert
-tiles, with outlier tokens, and through the standalone moe_route call."""
+far inside the error the candidate margin assumes (2^-11 ||x|| ||w_e||; the
+candidates' entries of the scratch hold their recomputed logits, closer
+still), that routing matches the oracle on small shapes with ragged token and
+expert tiles, with outlier tokens, and through the standalone moe_route call,
+and the degenerate case where every expert is a candidate."""
 import numpy as np
 import pytest
 
@@ -70,3 +72,17 @@ def test_tc_router_matches_oracle(name):
     assert np.abs(wts[same] - ro["w"][same]).max() <= parity.W_TOL
     assert np.allclose(wts.sum(1), 1.0, atol=1e-5)
     print(name, "near ties", len(ties))
+
+
+@pytest.mark.parametrize("E", [48, 384])
+def test_tc_router_every_expert_a_candidate(E):
+    # zero tokens and a zero bias: every logit is 0, every key 1/2, so every
+    # expert is a candidate and the ties go to the lowest indices: experts
+    # 0 .. k-1 with weight 1/k each (routed_scale 2: 2/k)
+    spec = dict(T=300, H=512, E=E, k=8, F=256, fmt="nvfp4", seed=65, **U)
+    gw = GpuWorkload(spec, torch, with_weights=False, routed_scale=2.0)
+    gw.x.zero_()
+    gw.bias.zero_()
+    idx, wts = route_gpu(gw)
+    assert (idx == np.arange(8, dtype=np.int32)[None, :]).all()
+    assert np.allclose(wts, 2.0 / 8, rtol=0, atol=1e-7)

@@ -5,8 +5,8 @@ activation quantisation, GEMM1 + capped SwiGLU, h quantisation, GEMM2,
 combine), inputs resident in HBM.  Prints one JSON line.  The line's workload
 is the largest single-GPU configuration (a 16384-token MXFP8 prefill chunk
 with Zipf-skewed expert load); the other configurations (the tiny case, the
-64- and 192-token decode batches, the 4096-token NVFP4 prefill chunk) are
-measured in the same run under `per_workload`.  The tensor-core roofs are the
+1-, 8-, 32-, 64- and 192-token decode batches, the 4096-token NVFP4 prefill
+chunk) are measured in the same run under `per_workload`.  The tensor-core roofs are the
 block-scaled MMA rates measured in the same run (moe_bench_mma_peak).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
@@ -36,8 +36,8 @@ METRIC = ("MoE-layer tokens/s & µs/layer; % HBM roofline (decode) / % FP4-FP8 p
 DEFAULT_WORKLOAD = "prefill16384_mxfp8_zipf"
 # the other configurations, measured beside the line's (timed steps, CPU work
 # kept small): name -> steps
-PER_WORKLOAD = {"tiny_mxfp8": 2000, "decode64_nvfp4": 1000, "decode192_mxfp8_outliers": 500,
-                "prefill4096_nvfp4": 200}
+PER_WORKLOAD = {"tiny_mxfp8": 2000, "decode1_nvfp4": 2000, "decode8_nvfp4": 1000, "decode32_mxfp8": 500,
+                "decode64_nvfp4": 1000, "decode192_mxfp8_outliers": 500, "prefill4096_nvfp4": 200}
 UNIT = "tokens/s"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
 
@@ -60,8 +60,10 @@ def peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the expert-GEMM sources (the traffic figures in profiles/ hold
+    only for the kernels they were captured from)."""
     h = hashlib.sha256()
-    for f in ("moe_gemm.cu", "moe_common.cuh"):
+    for f in ("moe_gemm.cu", "moe_gemm_common.cuh", "moe_ffn_decode.cu", "moe_common.cuh", "moe_quant_dev.cuh"):
         h.update(open(os.path.join(ROOT, "block_scaled_fp4_route_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -291,6 +293,42 @@ def measure_tensor_peaks(moe, torch, gpu_index: int, burst_s: float = 0.1, susta
 
 
 # ----------------------------------------------------------------------------
+# the MXFP8 KV-cache quantiser (moe_kv_quantize_mxfp8)
+# ----------------------------------------------------------------------------
+
+def measure_kv_quant(moe, torch, hbm_gbs: float, tokens=16384, heads=8, head_dim=128, reps=50):
+    """New K rows of a prefill chunk, bf16 [tokens, heads, head_dim], encoded
+    into a paged cache twice their size at a seeded permutation of slots:
+    algorithmic bytes = 2 (bf16 in) + 1 + 1/32 (codes and E8M0 scales out) per
+    element; the inputs (34 MB in, 17 MB out) fit in L2, so an L2 flush
+    buffer is written between the timed launches."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    kv = torch.randn((tokens, heads, head_dim), device="cuda", generator=g).to(torch.bfloat16)
+    slots = torch.randperm(2 * tokens, device="cuda", generator=g)[:tokens].to(torch.int64)
+    codes = torch.empty((2 * tokens, heads, head_dim), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((2 * tokens, heads, head_dim // 32), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        moe.moe_kv_quantize_mxfp8(kv, codes, scales, slots=slots)
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        moe.moe_kv_quantize_mxfp8(kv, codes, scales, slots=slots)
+        b.record(st)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e-3)
+    sec = float(np.median(times))
+    n = tokens * heads * head_dim
+    alg = n * (2 + 1 + 1 / 32)
+    return {"tokens": tokens, "heads": heads, "head_dim": head_dim, "slot_map": "seeded permutation into 2x slots",
+            "us": sec * 1e6, "gbs": alg / sec / 1e9, "hbm_frac": alg / sec / 1e9 / hbm_gbs,
+            "algorithmic_bytes": alg, "l2": "256 MB flush buffer written before each timed launch", "reps": reps}
+
+
+# ----------------------------------------------------------------------------
 # one workload on the GPU
 # ----------------------------------------------------------------------------
 
@@ -329,9 +367,14 @@ def stage_times(moe, torch, gw, n: int) -> dict:
 
 
 def ffn_fused(gw) -> bool:
-    """Decode batches (64-row tiles) run GEMM1, the h quantisation and GEMM2
-    as one kernel by default (moe_config.ffn_schedule 0)."""
-    return gw.layout["tile_rows"] == 64 and gw.cfg.ffn_schedule == 0
+    """Whether this configuration runs GEMM1, the h quantisation and GEMM2 as
+    the fused decode kernel (the library decides: its forward then launches
+    fewer kernels than with ffn_schedule = 1)."""
+    moe = gw.moe
+    c = gw.cfg
+    sep = moe.make_config(c.T, c.H, c.E, c.k, c.F, c.fmt, c.swiglu_cap, c.mx_scale_mode, c.bias_in_weights,
+                          c.routed_scale, c.act_global_mode, ffn_schedule=1)
+    return moe.moe_forward_kernel_count(c) < moe.moe_forward_kernel_count(sep)
 
 
 def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, hbm_gbs: float, tpeak: float):
@@ -426,8 +469,12 @@ def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str
     stage_ms = stage_times(moe, torch, gw, min(steps, n_prof))
     tpk = tensor_peaks[w["fmt"]]
     roof = rooflines(w, gw, n_touched, ms_per_step, stage_ms, hbm_gbs, tpk)
+    if ffn_fused(gw):   # one kernel between the x quantisation and the combine
+        ffn_ms = stage_ms.pop("gemm1_gate_up_swiglu") + stage_ms.pop("quant_h") + stage_ms.pop("gemm2_down")
+        stage_ms = {"router": stage_ms["router"], "dispatch": stage_ms["dispatch"], "quant_x": stage_ms["quant_x"],
+                    "expert_ffn_fused": ffn_ms, "combine": stage_ms["combine"]}
     res = {"workload": name, "T": w["T"], "fmt": w["fmt"], "touched_experts": n_touched, "steps": steps,
-           "launch": how, "ffn": "fused decode kernel" if ffn_fused(gw) else "separate kernels", "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+           "launch": how, "ffn_schedule": "fused decode kernel" if ffn_fused(gw) else "separate kernels", "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
            "tokens_per_s": job_tokens_per_s(w["T"], steps, world, ms), "stage_ms": stage_ms,
            "roofline": roof, "clocks": clocks.summary(),
            "gpu_launches": moe.moe_forward_kernel_count(gw.cfg) * steps}
@@ -626,7 +673,7 @@ def main():
                                       pk["hbm_gbs"], gpu_index, n_prof=50, ffn_schedule=args.ffn_schedule)
             rl = r["roofline"]
             per[nm] = {"T": r["T"], "fmt": r["fmt"], "touched_experts": r["touched_experts"], "steps": n_steps,
-                       "ffn": r["ffn"],
+                       "ffn_schedule": r["ffn_schedule"],
                        "us_per_layer": r["us_per_layer"], "tokens_per_s": r["tokens_per_s"],
                        "bound": rl["layer"]["bound"], "layer_frac": rl["layer"]["frac"],
                        "stage_ms": r["stage_ms"], "clocks": r["clocks"]}
@@ -637,6 +684,10 @@ def main():
             del g2w
             torch.cuda.empty_cache()
 
+    kv = None
+    if world == 1 and not args.no_per_workload:
+        kv = measure_kv_quant(moe, torch, pk["hbm_gbs"])
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -644,12 +695,13 @@ def main():
                 "config": {"workload": args.workload, "T": T, "H": w["H"], "E": w["E"], "k": k, "F": w["F"],
                            "fmt": w["fmt"], "touched_experts": main_res["touched_experts"],
                            "parallelism": f"replicas{world}", "launch": main_res["launch"],
-                           "ffn": main_res["ffn"],
+                           "ffn_schedule": main_res["ffn_schedule"],
                            "l2": "inputs larger than L2: the touched expert weights of one step "
                                  f"({gemm_bytes(w, main_res['touched_experts'])[0] / 1e9:.2f} GB read by GEMM1 "
                                  "alone) against a 129 MB L2; no flush"},
                 "layer": layer, "roofline": roofline, "tensor_peaks": mma, "cpu_baseline": cpu, "e2e": e2e,
-                "per_workload": per, "clocks": main_res["clocks"], "gpu_launches": main_res["gpu_launches"]}
+                "per_workload": per, "kv_cache_quant_mxfp8": kv, "clocks": main_res["clocks"],
+                "gpu_launches": main_res["gpu_launches"]}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

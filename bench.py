@@ -72,18 +72,19 @@ def kernel_source_sha() -> str:
 # algorithmic bytes of one launch of each expert GEMM
 # ----------------------------------------------------------------------------
 
-def gemm_bytes(w: dict, n_touched: int, h_quantised_in_gemm1: bool = False):
+def gemm_bytes(w: dict, n_touched: int, h_quantised_in_gemm1: bool = False, y_compact: bool = True):
     """Algorithmic HBM bytes of GEMM1 (gate+up) and GEMM2 (down) per launch:
     the encoded weights of the touched experts (each read once), the encoded
     activations read and the output written (GEMM1: bf16 h, or its MXFP8
-    codes and scales when the epilogue quantises h; GEMM2: fp32 y)."""
+    codes and scales when the epilogue quantises h; GEMM2: y rows, fp16 codes
+    plus an exponent byte per 32 features, or fp32)."""
     H, F, P = w["H"], w["F"], w["T"] * w["k"]
     nv = w["fmt"] == "nvfp4"
     bpe = 0.5 + 1 / 16 if nv else 1 + 1 / 32          # bytes per element incl. block scales
     glob = 4 if nv else 0
     h_out = P * F * (bpe if h_quantised_in_gemm1 else 2)
     g1 = n_touched * (2 * (F * H * bpe + glob)) + P * (H * bpe + glob) + h_out
-    g2 = n_touched * (H * F * bpe + glob) + P * (F * bpe + glob) + P * H * 4
+    g2 = n_touched * (H * F * bpe + glob) + P * (F * bpe + glob) + P * H * (2 + 1 / 32 if y_compact else 4)
     return g1, g2
 
 
@@ -373,7 +374,7 @@ def ffn_fused(gw) -> bool:
     moe = gw.moe
     c = gw.cfg
     sep = moe.make_config(c.T, c.H, c.E, c.k, c.F, c.fmt, c.swiglu_cap, c.mx_scale_mode, c.bias_in_weights,
-                          c.routed_scale, c.act_global_mode, ffn_schedule=1)
+                          c.routed_scale, c.act_global_mode, ffn_schedule=1, y_format=c.y_format)
     return moe.moe_forward_kernel_count(c) < moe.moe_forward_kernel_count(sep)
 
 
@@ -383,13 +384,20 @@ def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, h
     tensor-core rate (tpeak, TFLOP/s); `bound` is the roof that binds by
     arithmetic intensity.  Where one fused kernel runs both GEMMs (decode
     batches) its roof ("ffn") counts the bytes and flops of both and the
-    separate GEMM entries are absent."""
-    g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"])
+    separate GEMM entries are absent.  The layer's algorithmic bytes are the
+    touched experts' encoded weights, the router weights, x and the output:
+    the intermediates (x codes, h, y) are the implementation's traffic, which
+    one fused kernel per layer could keep on chip; each GEMM's own roof counts
+    the activations it reads and writes."""
+    g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"],
+                                    gw.cfg.y_format == gw.moe.Y_FP16E)
     g1_flops, g2_flops = gemm_flops(w)
     g1_s, g2_s = stage_ms["gemm1_gate_up_swiglu"] / 1e3, stage_ms["gemm2_down"] / 1e3
     balance = tpeak * 1e12 / (hbm_gbs * 1e9)        # flop per byte at which the two roofs meet
     T, H = w["T"], w["H"]
-    layer_bytes = g1_bytes + g2_bytes + w["E"] * H * 2 + T * H * 4
+    nv = w["fmt"] == "nvfp4"
+    per_expert = 3 * (w["F"] * H * (0.5 + 1 / 16 if nv else 1 + 1 / 32) + (4 if nv else 0))
+    layer_bytes = n_touched * per_expert + w["E"] * H * 2 + T * H * 4
     layer_flops = g1_flops + g2_flops + 2.0 * T * H * w["E"]
     step_s = ms_per_step / 1e3
 
@@ -415,14 +423,15 @@ def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, h
 
 
 def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str, tensor_peaks: dict, hbm_gbs: float,
-                     gpu_index: int, dist=None, world: int = 1, n_prof: int = 200, ffn_schedule: int = 0):
+                     gpu_index: int, dist=None, world: int = 1, n_prof: int = 200, ffn_schedule: int = 0,
+                     y_format: str = "fp16e"):
     """Set up one seeded workload, time `steps` forwards (CUDA-graph replays
     of captured calls, or eager calls) between events on the launching
     stream, with the SM clock sampled, plus per-stage event times."""
     import synth
     from synth.gpu_workload import GpuWorkload
     w = synth.WORKLOADS[name]
-    gw = GpuWorkload(name, torch, ffn_schedule=ffn_schedule)
+    gw = GpuWorkload(name, torch, ffn_schedule=ffn_schedule, y_format=y_format)
     st = torch.cuda.current_stream()
     for _ in range(warmup):
         gw.forward()
@@ -474,7 +483,8 @@ def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str
         stage_ms = {"router": stage_ms["router"], "dispatch": stage_ms["dispatch"], "quant_x": stage_ms["quant_x"],
                     "expert_ffn_fused": ffn_ms, "combine": stage_ms["combine"]}
     res = {"workload": name, "T": w["T"], "fmt": w["fmt"], "touched_experts": n_touched, "steps": steps,
-           "launch": how, "ffn_schedule": "fused decode kernel" if ffn_fused(gw) else "separate kernels", "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+           "launch": how, "ffn_schedule": "fused decode kernel" if ffn_fused(gw) else "separate kernels",
+           "y_format": y_format, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
            "tokens_per_s": job_tokens_per_s(w["T"], steps, world, ms), "stage_ms": stage_ms,
            "roofline": roof, "clocks": clocks.summary(),
            "gpu_launches": moe.moe_forward_kernel_count(gw.cfg) * steps}
@@ -497,6 +507,9 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other configurations")
     ap.add_argument("--no-tensor-peak", action="store_true",
                     help="skip the MMA-rate measurement (tensor roofs from the bf16 rate x nominal ratio)")
+    ap.add_argument("--y-format", default="fp16e", choices=["fp16e", "fp32"],
+                    help="moe_config.y_format: the expert outputs between the down GEMM and the combine as fp16 "
+                         "codes with an exponent per 32 features (default) or fp32")
     ap.add_argument("--ffn-schedule", type=int, default=0, choices=[0, 1],
                     help="moe_config.ffn_schedule: 0 = decode batches run the expert FFN as one fused kernel, "
                          "1 = separate kernels")
@@ -541,7 +554,8 @@ def main():
     w = synth.WORKLOADS[args.workload]
     T, k = w["T"], w["k"]
     gw, main_res = measure_workload(moe, torch, args.workload, args.steps, args.warmup, args.launch, tpeak,
-                                    pk["hbm_gbs"], gpu_index, dist, world, ffn_schedule=args.ffn_schedule)
+                                    pk["hbm_gbs"], gpu_index, dist, world, ffn_schedule=args.ffn_schedule,
+                                    y_format=args.y_format)
     st = torch.cuda.current_stream()
     ms_per_step = main_res["ms_per_step"]
     value = main_res["tokens_per_s"]
@@ -670,7 +684,8 @@ def main():
             if nm == args.workload:
                 continue
             g2w, r = measure_workload(moe, torch, nm, n_steps, max(args.warmup, 5), args.launch, tpeak,
-                                      pk["hbm_gbs"], gpu_index, n_prof=50, ffn_schedule=args.ffn_schedule)
+                                      pk["hbm_gbs"], gpu_index, n_prof=50, ffn_schedule=args.ffn_schedule,
+                                      y_format=args.y_format)
             rl = r["roofline"]
             per[nm] = {"T": r["T"], "fmt": r["fmt"], "touched_experts": r["touched_experts"], "steps": n_steps,
                        "ffn_schedule": r["ffn_schedule"],
@@ -695,7 +710,7 @@ def main():
                 "config": {"workload": args.workload, "T": T, "H": w["H"], "E": w["E"], "k": k, "F": w["F"],
                            "fmt": w["fmt"], "touched_experts": main_res["touched_experts"],
                            "parallelism": f"replicas{world}", "launch": main_res["launch"],
-                           "ffn_schedule": main_res["ffn_schedule"],
+                           "ffn_schedule": main_res["ffn_schedule"], "y_format": main_res["y_format"],
                            "l2": "inputs larger than L2: the touched expert weights of one step "
                                  f"({gemm_bytes(w, main_res['touched_experts'])[0] / 1e9:.2f} GB read by GEMM1 "
                                  "alone) against a 129 MB L2; no flush"},

@@ -15,13 +15,15 @@ import threading
 from . import build as _build
 
 FMT_NVFP4, FMT_MXFP8 = 0, 1
+Y_FP32, Y_FP16E = 0, 1
 SCALES_ROWMAJOR, SCALES_TILED = 0, 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
           4: "MOE_ERR_WORKSPACE_TOO_SMALL", 5: "MOE_ERR_ARCH", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_DEVICE_TIMEOUT",
           8: "MOE_ERR_BOUNDS"}
 
-EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_forward",
+EXPORTED = ["moe_workspace_size", "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_y_bytes",
+            "moe_forward",
             "moe_forward_profiled", "moe_quantize", "moe_pack_scales", "moe_poll_device_status", "moe_workspace_layout",
             "moe_route_noalloc", "moe_route_noalloc_poll_status", "moe_fake_quantize", "moe_kv_quantize_mxfp8", "moe_bench_mma_peak", "moe_selftest_bounded_wait", "moe_selftest_dependency_wait", "moe_debug_bounds_status", "moe_forward_kernel_count",
             "moe_status_string"]
@@ -37,7 +39,7 @@ class moe_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("H", ctypes.c_int), ("E", ctypes.c_int), ("k", ctypes.c_int),
                 ("F", ctypes.c_int), ("fmt", ctypes.c_int), ("swiglu_cap", ctypes.c_float),
                 ("act_global_mode", ctypes.c_int), ("mx_scale_mode", ctypes.c_int), ("bias_in_weights", ctypes.c_int),
-                ("routed_scale", ctypes.c_float), ("ffn_schedule", ctypes.c_int)]
+                ("routed_scale", ctypes.c_float), ("ffn_schedule", ctypes.c_int), ("y_format", ctypes.c_int)]
 
 
 class moe_qweight(ctypes.Structure):
@@ -85,6 +87,7 @@ def lib(debug_bounds=None):
             L.moe_dispatch.argtypes = [cfgp, P, P, P, P, P, P, sz, P]
             L.moe_expert_ffn.argtypes = [cfgp, P, P, P, P, P, qwp, qwp, qwp, P, P, P, sz, P]
             L.moe_combine.argtypes = [cfgp, P, P, P, P, P]
+            L.moe_y_bytes.argtypes = [cfgp, ctypes.POINTER(sz)]
             L.moe_forward.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, P, sz, P]
             L.moe_forward_profiled.argtypes = [cfgp, P, P, P, qwp, qwp, qwp, P, P, P, sz, P,
                                                ctypes.POINTER(ctypes.c_void_p)]
@@ -135,16 +138,21 @@ def _stream(stream):
 
 
 def make_config(T, H, E, k, F, fmt, swiglu_cap=10.0, mx_scale_mode=0, bias_in_weights=0, routed_scale=1.0,
-                act_global_mode=0, ffn_schedule=0):
+                act_global_mode=0, ffn_schedule=0, y_format=None):
     """A moe_config: T tokens, hidden H, E experts, top-k, FFN width F; fmt "nvfp4" / "mxfp8" (or
     FMT_*); swiglu_cap c of c*tanh(v/c) (0 = none); mx_scale_mode 0 = OCP floor, 1 = round-up;
     bias_in_weights 0 = the bias steers selection only; act_global_mode 1 = static per-expert NVFP4
     activation globals; ffn_schedule 0 = decode batches run the expert FFN as one fused kernel,
-    1 = separate kernels."""
+    1 = separate kernels; y_format of the expert outputs, "fp16e" (default: fp16 codes with an
+    exponent per 32 features) or "fp32" (or Y_*)."""
     if isinstance(fmt, str):
         fmt = {"nvfp4": FMT_NVFP4, "mxfp8": FMT_MXFP8}[fmt]
+    if y_format is None:
+        y_format = Y_FP16E
+    if isinstance(y_format, str):
+        y_format = {"fp32": Y_FP32, "fp16e": Y_FP16E}[y_format]
     return moe_config(T, H, E, k, F, fmt, swiglu_cap, act_global_mode, mx_scale_mode, bias_in_weights, routed_scale,
-                      ffn_schedule)
+                      ffn_schedule, y_format)
 
 
 def qweight(codes, scales, global_scale=None) -> moe_qweight:
@@ -210,16 +218,37 @@ def moe_dispatch(cfg, topk_idx, counts, offsets, perm, pair_pos, ws, stream=None
 
 def moe_expert_ffn(cfg, x, topk_idx, offsets, perm, pair_pos, gate, up, down, y_perm, ws, stream=None,
                    act_static_scales=None):
-    """Expert FFN of every pair: y_perm fp32 [T * k, H] (out), rows in dispatch order; gate / up /
-    down from qweight(); act_static_scales as for moe_forward."""
+    """Expert FFN of every pair: y_perm (out) the T * k rows in dispatch order in cfg.y_format
+    (moe_y_bytes bytes: fp32 [T * k, H], or fp16 codes then int8 exponents, see y_rows); gate / up
+    / down from qweight(); act_static_scales as for moe_forward."""
     _check("moe_expert_ffn", lib().moe_expert_ffn(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(offsets),
                                                   _ptr(perm), _ptr(pair_pos), ctypes.byref(gate), ctypes.byref(up),
                                                   ctypes.byref(down), _ptr(act_static_scales), _ptr(y_perm),
                                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def moe_y_bytes(cfg) -> int:
+    """Bytes of the T * k expert output rows in cfg.y_format."""
+    n = ctypes.c_size_t(0)
+    _check("moe_y_bytes", lib().moe_y_bytes(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def y_rows(cfg, buf):
+    """Views of a y buffer (a uint8 / any tensor of moe_y_bytes bytes): fp32 [P, H] for Y_FP32,
+    else (codes fp16 [P, H], exponents int8 [P, H / 32]).  Argument marshalling only."""
+    import torch
+    P, H = cfg.T * cfg.k, cfg.H
+    b = buf.view(torch.uint8).reshape(-1)
+    if cfg.y_format == Y_FP32:
+        return b[:P * H * 4].view(torch.float32).view(P, H)
+    return b[:P * H * 2].view(torch.float16).view(P, H), b[P * H * 2:P * H * 2 + P * (H // 32)].view(
+        torch.int8).view(P, H // 32)
+
+
 def moe_combine(cfg, y_perm, topk_w, pair_pos, out, stream=None):
-    """out bf16 [T, H] = sum over slots (in slot order, fp32) of topk_w * y_perm[pair_pos]."""
+    """out bf16 [T, H] = sum over slots (in slot order, fp32) of topk_w * y_perm[pair_pos], y_perm
+    in cfg.y_format."""
     _check("moe_combine", lib().moe_combine(ctypes.byref(cfg), _ptr(y_perm), _ptr(topk_w), _ptr(pair_pos),
                                             _ptr(out), _stream(stream)))
 

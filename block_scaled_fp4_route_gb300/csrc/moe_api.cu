@@ -63,6 +63,7 @@ moe_status check_cfg(const moe_config* c) {
   if (c->act_global_mode != 0 && c->act_global_mode != 1) return MOE_ERR_INVALID_ARG;
   if (c->act_global_mode == 1 && c->fmt != MOE_FMT_NVFP4) return MOE_ERR_INVALID_ARG;  // MXFP8 has no global
   if (c->ffn_schedule != 0 && c->ffn_schedule != 1) return MOE_ERR_INVALID_ARG;
+  if (c->y_format != MOE_Y_FP32 && c->y_format != MOE_Y_FP16E) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -136,7 +137,7 @@ void mark(cudaEvent_t* ev, int i, cudaStream_t st) {
 // GEMM2).
 moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const int32_t* idx, const int32_t* offsets,
                     const int32_t* perm, const int32_t* pair_pos, const moe_qweight* gate, const moe_qweight* up,
-                    const moe_qweight* down, const float* act_static, float* y, void* ws, cudaStream_t st,
+                    const moe_qweight* down, const float* act_static, void* y, void* ws, cudaStream_t st,
                     cudaEvent_t* ev = nullptr) {
   if (c.act_global_mode != 1) act_static = nullptr;
   moe_ws_layout L;
@@ -207,6 +208,7 @@ moe_status ffn_core(const moe_config& c, int sms, const __nv_bfloat16* x, const 
   g2.NA = c.H;
   g2.K = c.F;
   g2.y_out = y;
+  g2.y_exp = y_exponents(c, y);
   g2.status = status;
   g2.num_sms = sms;
 
@@ -300,7 +302,7 @@ void ws_layout(const moe_config& c, moe_ws_layout* L) {
   L->hq_codes = take(R * code_bytes(c.fmt, c.F));
   L->hq_scales = take(act_scale_bytes(R, c.F / bs, tile_rows(c)));
   L->hq_global = take(R * 4);
-  L->y_perm = take(P * c.H * 4);
+  L->y_perm = take(y_bytes(c));
   L->total = off;
 }
 
@@ -359,7 +361,7 @@ moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_dev, int3
 moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
                           const int32_t* offsets_dev, const int32_t* perm_dev, const int32_t* pair_pos_dev,
                           const moe_qweight* gate, const moe_qweight* up, const moe_qweight* down,
-                          const float* act_static_scales, float* y_perm_dev, void* ws_dev, size_t ws_bytes,
+                          const float* act_static_scales, void* y_perm_dev, void* ws_dev, size_t ws_bytes,
                           void* stream) {
   moe_status s = check_cfg(cfg);
   if (s == MOE_OK) s = check_ptrs({x_dev, topk_idx_dev, offsets_dev, perm_dev, pair_pos_dev, y_perm_dev});
@@ -382,7 +384,7 @@ moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_
                   down, act_static_scales, y_perm_dev, ws_dev, st);
 }
 
-moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const float* topk_w_dev,
+moe_status moe_combine(const moe_config* cfg, const void* y_perm_dev, const float* topk_w_dev,
                        const int32_t* pair_pos_dev, void* out_dev, void* stream) {
   moe_status s = check_cfg(cfg);
   if (s == MOE_OK) s = check_ptrs({y_perm_dev, topk_w_dev, pair_pos_dev, out_dev});
@@ -390,6 +392,14 @@ moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const flo
   if (s != MOE_OK) return s;
   return cuda_status(launch_combine(*cfg, y_perm_dev, topk_w_dev, pair_pos_dev, (__nv_bfloat16*)out_dev,
                                     (cudaStream_t)stream, false));
+}
+
+moe_status moe_y_bytes(const moe_config* cfg, size_t* bytes) {
+  moe_status s = check_cfg(cfg);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = (size_t)y_bytes(*cfg);
+  return MOE_OK;
 }
 
 static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const void* w_router_dev,
@@ -416,7 +426,7 @@ static moe_status forward_impl(const moe_config* cfg, const void* x_dev, const v
   int32_t* offsets = at<int32_t>(ws_dev, L.offsets);
   int32_t* perm = at<int32_t>(ws_dev, L.perm);
   int32_t* pair_pos = at<int32_t>(ws_dev, L.pair_pos);
-  float* y = at<float>(ws_dev, L.y_perm);
+  void* y = at<uint8_t>(ws_dev, L.y_perm);
   mark(ev, 0, st);
   // the router's first kernel clears the status word of the call.  It is
   // launched behind whatever precedes it on the stream (a previous layer's
@@ -665,7 +675,8 @@ moe_status moe_selftest_dependency_wait(const moe_config* cfg, const moe_qweight
   g2.gB = hg;
   g2.NA = c.H;
   g2.K = c.F;
-  g2.y_out = at<float>(ws_dev, L.y_perm);
+  g2.y_out = at<uint8_t>(ws_dev, L.y_perm);
+  g2.y_exp = y_exponents(c, g2.y_out);
   for (GemmLaunch* g : {&g1, &g2}) {
     g->tiles = at<RowTile>(ws_dev, L.tiles);
     g->rt_base = at<int32_t>(ws_dev, L.rt_base);

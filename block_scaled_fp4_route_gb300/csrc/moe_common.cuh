@@ -162,6 +162,37 @@ __device__ __forceinline__ int ilog2_ceil(float a) {
   return ef > 0 ? ef - 127 + (m != 0u) : sub;
 }
 
+// MOE_Y_FP16E expert outputs: the exponent of a 32-feature block with
+// absolute maximum amax (its largest value then lands in [2^14, 2^15) of the
+// fp16 range), and the fp16 codes (round to nearest even; the pair form puts
+// the first value in the low half).
+__device__ __forceinline__ int y16_exponent(float amax) {
+  if (amax == 0.0f) return 0;
+  const int e = ilog2_floor(amax) - 14;
+  return e < -110 ? -110 : e;
+}
+__device__ __forceinline__ uint32_t f16x2_encode(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t f16_encode(float v) {
+  uint16_t r;
+  asm("cvt.rn.f16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float f16_value(uint16_t c) {
+  float r;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(r) : "h"(c));
+  return r;
+}
+// Both fp16 values of a 32-bit word (low half first), exactly.
+__device__ __forceinline__ void f16x2_values(uint32_t u, float& lo, float& hi) {
+  asm("{.reg .f16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(u));
+}
+
 // E8M0 scale byte of one MXFP8 block with absolute maximum amax_b > 0.
 __device__ __forceinline__ uint32_t mx_scale_code(float amax_b, int mode) {
   int e = (mode == 0) ? ilog2_floor(amax_b) - 8 : ilog2_ceil(__fdiv_rn(amax_b, 448.0f));

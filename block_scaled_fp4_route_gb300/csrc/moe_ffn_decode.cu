@@ -544,10 +544,30 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
           for (int j = 0; j < 16; ++j) {
             const int n = ch * 16 + j;
             const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
-            if (n < col_hi && MOE_IN_BOUNDS(rt.canon + n < a2.P)) {
-              float* yrow = a2.y_out + (int64_t)(rt.canon + n) * a2.NA;
-              yrow[f] = __uint_as_float(r0[ch][j]) * (sA0 * gb);
-              if (second) yrow[f + 128] = __uint_as_float(r1[ch][j]) * (sA1 * gb);
+            if (n >= col_hi) continue;  // warp-uniform
+            const float v0 = __uint_as_float(r0[ch][j]) * (sA0 * gb);
+            const float v1 = __uint_as_float(r1[ch][j]) * (sA1 * gb);
+            const bool ok = MOE_IN_BOUNDS(rt.canon + n < a2.P);
+            const int64_t prow = (int64_t)rt.canon + n;
+            if (a2.y16) {
+              // the warp's 32 lanes are one 32-feature exponent block
+              int e0, e1 = 0;
+              const uint16_t c0 = y16_lane_code(v0, e0);
+              const uint16_t c1 = second ? y16_lane_code(v1, e1) : (uint16_t)0;
+              if (ok) {
+                uint16_t* yrow = reinterpret_cast<uint16_t*>(a2.y_out) + prow * a2.NA;
+                int8_t* erow = a2.y_exp + prow * (a2.NA >> 5);
+                yrow[f] = c0;
+                if (lane == 0) erow[f >> 5] = (int8_t)e0;
+                if (second) {
+                  yrow[f + 128] = c1;
+                  if (lane == 0) erow[(f + 128) >> 5] = (int8_t)e1;
+                }
+              }
+            } else if (ok) {
+              float* yrow = reinterpret_cast<float*>(a2.y_out) + prow * a2.NA;
+              yrow[f] = v0;
+              if (second) yrow[f + 128] = v1;
             }
           }
         }

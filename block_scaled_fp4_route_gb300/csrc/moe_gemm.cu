@@ -396,10 +396,30 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
           for (int j = 0; j < 16; ++j) {
             const int n = col_lo + ch * 16 + j;
             const float gb = __shfl_sync(0xffffffffu, ch < 2 ? gb_lo : gb_hi, (ch * 16 + j) & 31);
-            if (n < col_hi && MOE_IN_BOUNDS(rt.canon + n < a.P)) {
-              float* yrow = a.y_out + (int64_t)(rt.canon + n) * a.NA;
-              yrow[f] = __uint_as_float(r0[ch][j]) * (sA0 * gb);
-              if (second) yrow[f + 128] = __uint_as_float(r1[ch][j]) * (sA1 * gb);
+            if (n >= col_hi) continue;  // warp-uniform
+            const float v0 = __uint_as_float(r0[ch][j]) * (sA0 * gb);
+            const float v1 = __uint_as_float(r1[ch][j]) * (sA1 * gb);
+            const bool ok = MOE_IN_BOUNDS(rt.canon + n < a.P);
+            const int64_t prow = (int64_t)rt.canon + n;
+            if (a.y16) {
+              // the warp's 32 lanes are one 32-feature exponent block
+              int e0, e1 = 0;
+              const uint16_t c0 = y16_lane_code(v0, e0);
+              const uint16_t c1 = second ? y16_lane_code(v1, e1) : (uint16_t)0;
+              if (ok) {
+                uint16_t* yrow = reinterpret_cast<uint16_t*>(a.y_out) + prow * a.NA;
+                int8_t* erow = a.y_exp + prow * (a.NA >> 5);
+                yrow[f] = c0;
+                if (lane == 0) erow[f >> 5] = (int8_t)e0;
+                if (second) {
+                  yrow[f + 128] = c1;
+                  if (lane == 0) erow[(f + 128) >> 5] = (int8_t)e1;
+                }
+              }
+            } else if (ok) {
+              float* yrow = reinterpret_cast<float*>(a.y_out) + prow * a.NA;
+              yrow[f] = v0;
+              if (second) yrow[f + 128] = v1;
             }
           }
         }
@@ -540,6 +560,23 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
         r1[1][j] = r1[3][j];
       }
     }
+  } else if (a.y16) {
+    // MOE_Y_FP16E: each thread's 64 features of a block are two whole
+    // 32-feature exponent blocks of its own row, encoded and stored by the
+    // thread (64 contiguous bytes per block; no collective operation)
+    const int64_t prow = (int64_t)rt.canon + n;
+    if (!valid || !MOE_IN_BOUNDS(prow < a.P)) return;
+    const int f0 = mt * ROWS + 64 * hc;
+    uint16_t* yrow = reinterpret_cast<uint16_t*>(a.y_out) + prow * a.NA + f0;
+    uint16_t* erow = reinterpret_cast<uint16_t*>(a.y_exp + prow * (a.NA >> 5) + (f0 >> 5));
+    int e0 = y16_block_store(r0[0], r0[1], s0, yrow);
+    int e1 = y16_block_store(r0[2], r0[3], s0, yrow + 32);
+    erow[0] = (uint16_t)((e0 & 0xFF) | ((e1 & 0xFF) << 8));
+    if (second) {
+      e0 = y16_block_store(r1[0], r1[1], s1, yrow + 128);
+      e1 = y16_block_store(r1[2], r1[3], s1, yrow + 160);
+      erow[2] = (uint16_t)((e0 & 0xFF) | ((e1 & 0xFF) << 8));
+    }
   } else {
     // y rows are written feature-contiguously: each 32 x 32 (token x
     // feature) group of the warp is transposed with xor shuffles, then
@@ -547,7 +584,8 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
     int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile
     // (warp-uniform: the quadrant's rows are stored only if all are in range)
     if (!MOE_IN_BOUNDS((int64_t)rt.canon + q * 32 + (nv > 32 ? 32 : nv) <= a.P)) nv = 0;
-    float* ybase = a.y_out + ((int64_t)rt.canon + q * 32) * a.NA + mt * ROWS + 64 * hc + lane;
+    float* ybase = reinterpret_cast<float*>(a.y_out) + ((int64_t)rt.canon + q * 32) * a.NA + mt * ROWS + 64 * hc +
+                   lane;
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch)
 #pragma unroll

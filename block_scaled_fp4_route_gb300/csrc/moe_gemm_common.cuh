@@ -60,7 +60,9 @@ struct GemmArgs {
   uint8_t* hq_codes;     // MXFP8: h codes and scales written by the epilogue
   uint8_t* hq_scales;
   int mx_mode;
-  float* y_out;
+  void* y_out;     // y rows: fp32, or fp16 codes (y16)
+  int8_t* y_exp;   // y16: exponents [P, NA/32]
+  int y16;
   uint32_t* status;
   long long limit;
   int withhold_loads;
@@ -68,6 +70,41 @@ struct GemmArgs {
   int64_t P;      // pairs (canonical y rows are below P)
   int max_tiles;  // capacity of the row-tile list
 };
+
+// One MOE_Y_FP16E block held by one thread: the 32 values lo[0..15],
+// hi[0..15] (fp32 bits) times sc, the same fp32 products the fp32 format
+// stores; their codes go to dst (32 fp16, 64 bytes, 16-byte aligned) and the
+// block's exponent is returned.
+__device__ __forceinline__ int y16_block_store(const uint32_t (&lo)[16], const uint32_t (&hi)[16], float sc,
+                                               uint16_t* dst) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    v[j] = __fmul_rn(__uint_as_float(lo[j]), sc);
+    v[16 + j] = __fmul_rn(__uint_as_float(hi[j]), sc);
+  }
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
+  const int e = y16_exponent(m);
+  const float mul = exp2i(-e);
+  uint32_t pk[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pk[j] = f16x2_encode(__fmul_rn(v[2 * j], mul), __fmul_rn(v[2 * j + 1], mul));
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  return e;
+}
+
+// One MOE_Y_FP16E value per lane of a warp whose 32 lanes hold one 32-feature
+// block of a row (weight-major epilogues): the block's exponent (reduced
+// across the warp; every lane must call) and this lane's code.
+__device__ __forceinline__ uint16_t y16_lane_code(float v, int& e) {
+  const float m = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
+  e = y16_exponent(m);
+  return f16_encode(__fmul_rn(v, exp2i(-e)));
+}
 
 // The tile plan's row-tile prefix rtb[0..E] must be non-decreasing and end at
 // most at max_tiles.  Checked build: every thread of the CTA checks a share
@@ -160,6 +197,8 @@ inline GemmArgs gemm_args(const GemmLaunch& g) {
   a.hq_scales = g.hq_scales;
   a.mx_mode = g.cfg->mx_scale_mode;
   a.y_out = g.y_out;
+  a.y_exp = g.y_exp;
+  a.y16 = y16(*g.cfg) ? 1 : 0;
   a.status = g.status;
   a.limit = g.wait_limit > 0 ? g.wait_limit : 4000000000LL;  // default ~2 s of SM clock
   a.withhold_loads = g.withhold_loads;

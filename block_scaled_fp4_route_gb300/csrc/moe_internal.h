@@ -150,7 +150,8 @@ struct GemmLaunch {
   __nv_bfloat16* h_out;   // gated, NVFP4: bf16 h [R, F]
   uint8_t* hq_codes = nullptr;   // gated, MXFP8: h codes [R, F] and scales, written by the epilogue
   uint8_t* hq_scales = nullptr;
-  float* y_out;           // down:  [P, H]
+  void* y_out;            // down:  y rows [P, H] in the config's y_format (fp32, or fp16 codes)
+  int8_t* y_exp = nullptr; // down, MOE_Y_FP16E: exponents [P, H/32]
   uint32_t* status;
   int num_sms;
   long long wait_limit = 0;  // cycles per bounded wait; 0 = the default (~2 s)
@@ -177,7 +178,18 @@ inline bool ffn_fused(const moe_config& c) {
   return tile_rows(c) == kNTDecode && c.ffn_schedule == 0 && (int64_t)c.T * c.k >= kFusedMinPairs;
 }
 
-cudaError_t launch_combine(const moe_config& c, const float* y, const float* w, const int32_t* pair_pos,
+// y rows of a configuration: bytes, and where the exponents of MOE_Y_FP16E
+// start (after the P*H fp16 codes).
+inline bool y16(const moe_config& c) { return c.y_format == MOE_Y_FP16E; }
+inline int64_t y_bytes(const moe_config& c) {
+  const int64_t P = (int64_t)c.T * c.k;
+  return y16(c) ? P * c.H * 2 + P * (c.H / 32) : P * c.H * 4;
+}
+inline int8_t* y_exponents(const moe_config& c, void* y) {
+  return y16(c) ? reinterpret_cast<int8_t*>(y) + (int64_t)c.T * c.k * c.H * 2 : nullptr;
+}
+
+cudaError_t launch_combine(const moe_config& c, const void* y, const float* w, const int32_t* pair_pos,
                            __nv_bfloat16* out, cudaStream_t st, bool pdl);
 
 }  // namespace moe

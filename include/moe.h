@@ -81,6 +81,21 @@ typedef enum { MOE_FMT_NVFP4 = 0, MOE_FMT_MXFP8 = 1 } moe_format;
  *             as ROWMAJOR when rows%128 == 0 and C%4 == 0. */
 typedef enum { MOE_SCALES_ROWMAJOR = 0, MOE_SCALES_TILED = 1 } moe_scale_layout;
 
+/* Format of the expert outputs y (the rows the down GEMM writes and the
+ * combine reads, before the routing weights apply; the pages do not fix it):
+ *   MOE_Y_FP32:  fp32 [P, H].
+ *   MOE_Y_FP16E: fp16 significands with a power-of-two exponent per 32
+ *     features.  For row p and feature block b (features 32b .. 32b+31),
+ *     amax = max |y| over the block and
+ *       e = 0 if amax = 0, else max(floor(log2 amax) - 14, -110),
+ *       code = fp16_rne(y * 2^-e),   y decoded = code * 2^e,
+ *     so every block's largest value lands in [2^14, 2^15) of the fp16
+ *     range: nothing overflows and each element keeps 11 significant bits
+ *     (|error| <= 2^-11 |y|).  Layout: the fp16 codes [P, H], then the int8
+ *     exponents [P, H/32].  Half the bytes of fp32 between the down GEMM
+ *     and the combine. */
+typedef enum { MOE_Y_FP32 = 0, MOE_Y_FP16E = 1 } moe_y_format;
+
 /* Layer shape and options.
  *   T tokens (1..65536), H hidden, E experts (1..1024), k experts per token
  *   (1..min(E,32)), F expert FFN width.  H and F must be multiples of 256 for
@@ -110,7 +125,11 @@ typedef enum { MOE_SCALES_ROWMAJOR = 0, MOE_SCALES_TILED = 1 } moe_scale_layout;
  *     persistent kernel for GEMM1, the h quantisation and GEMM2, a down
  *     tile starting as soon as its h rows exist, separate kernels below;
  *     1 = separate kernels always.  The results are the same bit for bit.
- *     Prefill batches always use separate kernels. */
+ *     Prefill batches always use separate kernels.
+ *   y_format: moe_y_format of the expert outputs (the buffers that
+ *     moe_expert_ffn writes and moe_combine reads, and the workspace's y
+ *     rows in moe_forward).  MOE_Y_FP16E is the faster choice; a zeroed
+ *     config gets MOE_Y_FP32. */
 typedef struct {
   int T, H, E, k, F;
   moe_format fmt;
@@ -120,6 +139,7 @@ typedef struct {
   int bias_in_weights;
   float routed_scale;
   int ffn_schedule;
+  int y_format;
 } moe_config;
 
 /* One quantised expert matrix for all E experts (device pointers).
@@ -223,20 +243,28 @@ MOE_API moe_status moe_dispatch(const moe_config* cfg, const int32_t* topk_idx_d
  *   gate/up/down quantised weights (see moe_qweight)
  *   act_static_scales fp32 [E, 2] (g_x[e], g_h[e]) when act_global_mode = 1,
  *                else NULL (ignored)
- *   y_perm_dev   fp32 [P, H] (out), row p = perm order. */
+ *   y_perm_dev   (out) the P rows y_p in perm order, in cfg->y_format
+ *                (moe_y_bytes bytes, 16-byte aligned). */
 MOE_API moe_status moe_expert_ffn(const moe_config* cfg, const void* x_dev, const int32_t* topk_idx_dev,
                           const int32_t* offsets_dev, const int32_t* perm_dev,
                           const int32_t* pair_pos_dev, const moe_qweight* gate,
                           const moe_qweight* up, const moe_qweight* down,
-                          const float* act_static_scales, float* y_perm_dev,
+                          const float* act_static_scales, void* y_perm_dev,
                           void* ws_dev, size_t ws_bytes, void* stream);
+
+/* Bytes of the y rows of this configuration in its y_format: P*H*4 (fp32)
+ * or P*H*2 + P*H/32 (fp16 codes, then exponents), P = T*k. */
+MOE_API moe_status moe_y_bytes(const moe_config* cfg, size_t* bytes);
 
 /* Weighted combine [CB MegaMoE: the combine ends the fused unit]:
  *   out[t] = bf16_rne( sum_{j=0..k-1} topk_w[t,j] * y_perm[pair_pos[t,j]] ),
- * summed in fp32 in slot order (deterministic).
- *   y_perm_dev fp32 [P, H]; topk_w_dev fp32 [T, k]; pair_pos_dev int32 [T, k];
- *   out_dev bf16 [T, H] (out). */
-MOE_API moe_status moe_combine(const moe_config* cfg, const float* y_perm_dev, const float* topk_w_dev,
+ * summed in fp32 in slot order (deterministic), y_perm the decoded rows.
+ * For MOE_Y_FP16E each product is fma(topk_w * 2^e, code, sum) (the weight
+ * times a power of two is exact), i.e. the same sum over the decoded values.
+ *   y_perm_dev rows in cfg->y_format (as moe_expert_ffn writes them);
+ *   topk_w_dev fp32 [T, k]; pair_pos_dev int32 [T, k]; out_dev bf16 [T, H]
+ *   (out). */
+MOE_API moe_status moe_combine(const moe_config* cfg, const void* y_perm_dev, const float* topk_w_dev,
                        const int32_t* pair_pos_dev, void* out_dev, void* stream);
 
 /* The whole layer in one call: moe_route, moe_dispatch, moe_expert_ffn and

@@ -274,6 +274,34 @@ def combine(w: np.ndarray, pair_pos: np.ndarray, y: np.ndarray) -> np.ndarray:
     return out
 
 
+def encode_y16(y32: np.ndarray):
+    """The expert outputs y (fp32 rows [n, H]) in the compact exchange format
+    between the down GEMM and the combine.  The pages fix no format for y
+    (the MegaMoE paragraph of the Inkling-2-Small cookbook keeps it inside
+    the fused unit), so this is a reading of the library's own: per row and
+    32-feature block, amax = max |y|; e = floor(log2 amax) - 14, not below
+    -110, and 0 for an all-zero block; code = fp16(y * 2^-e), rounded to
+    nearest even (the block maximum lands in [2^14, 2^15)).
+    Returns (codes uint16 [n, H], exponents int8 [n, H/32])."""
+    y = np.asarray(y32, np.float32)
+    n, H = y.shape
+    b = y.reshape(n, H // 32, 32).astype(np.float64)
+    amax = np.abs(b).max(axis=2)
+    _, ex = np.frexp(amax)                 # amax = m * 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    e = np.where(amax > 0, np.maximum(ex - 1 - 14, -110), 0).astype(np.int32)
+    scaled = b * np.exp2(-e.astype(np.float64))[..., None]      # exact: a power of two
+    codes = scaled.astype(np.float16).view(np.uint16).reshape(n, H)
+    return codes, e.astype(np.int8)
+
+
+def decode_y16(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    """Values of encode_y16's format: code * 2^e (fp64, exact)."""
+    codes = np.asarray(codes, np.uint16)
+    n, H = codes.shape
+    v = codes.view(np.float16).astype(np.float64).reshape(n, H // 32, 32)
+    return (v * np.exp2(np.asarray(exps, np.float64))[..., None]).reshape(n, H)
+
+
 # ----------------------------------------------------------------------------
 # the layer over (a sample of) a seeded workload
 # ----------------------------------------------------------------------------

@@ -17,7 +17,8 @@ def workload(spec) -> dict:
 
 class GpuWorkload:
     def __init__(self, spec, torch, device="cuda", cap=10.0, mx_scale_mode=0, chunk_experts=8,
-                 with_weights=True, act_static=None, bias_in_weights=0, routed_scale=1.0, ffn_schedule=0):
+                 with_weights=True, act_static=None, bias_in_weights=0, routed_scale=1.0, ffn_schedule=0,
+                 y_format=None):
         import block_scaled_fp4_route_gb300 as moe
         self.torch = torch
         self.moe = moe
@@ -31,7 +32,7 @@ class GpuWorkload:
         self.cfg = moe.make_config(T, H, E, k, F, w["fmt"], swiglu_cap=cap, mx_scale_mode=mx_scale_mode,
                                    act_global_mode=0 if act_static is None else 1,
                                    bias_in_weights=int(bias_in_weights), routed_scale=routed_scale,
-                                   ffn_schedule=ffn_schedule)
+                                   ffn_schedule=ffn_schedule, y_format=y_format)
         self.x = synth.dev_x(w, torch, device)
         self.w_router = synth.dev_router_weight(w, torch, device)
         self.bias = torch.from_numpy(synth.router_bias(w)).to(device)
@@ -82,6 +83,11 @@ class GpuWorkload:
         off = self.layout[name]
         item = torch.empty((), dtype=dtype).element_size()
         return self.ws[off:off + count * item].view(dtype)
+
+    def y_raw(self):
+        """The workspace's expert output rows as bytes (moe_y_bytes of the config)."""
+        off = self.layout["y_perm"]
+        return self.ws[off:off + self.moe.moe_y_bytes(self.cfg)]
 
     def routing(self):
         """topk idx / w, counts, offsets, perm, pair_pos, seg_start from the workspace (numpy)."""

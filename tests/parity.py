@@ -65,6 +65,29 @@ def bf16_to_f64(t) -> np.ndarray:
     return t.to(torch.float32).cpu().numpy().astype(np.float64)
 
 
+# the compact y rows keep 11 significant bits: |decoded - y| <= Y16_REL |y|
+Y16_REL = 2.0 ** -11
+
+
+def y_rows_f64(moe, cfg, raw, rows) -> np.ndarray:
+    """fp64 values of the given y rows of a y buffer (bytes, on the device)
+    in cfg.y_format: fp32 as stored, or the fp16 codes decoded with their
+    exponents by the oracle's rule."""
+    import torch
+    import oracle
+    idx = torch.as_tensor(np.asarray(rows, np.int64), device=raw.device)
+    v = moe.y_rows(cfg, raw)
+    if cfg.y_format == moe.Y_FP32:
+        return v[idx].cpu().numpy().astype(np.float64)
+    codes, ex = v
+    return oracle.decode_y16(codes[idx].view(torch.int16).cpu().numpy().view(np.uint16), ex[idx].cpu().numpy())
+
+
+def y_rel(moe, cfg) -> float:
+    """Relative rounding of the y format (0 for fp32)."""
+    return 0.0 if cfg.y_format == moe.Y_FP32 else Y16_REL
+
+
 def out_error(gpu: np.ndarray, ref: np.ndarray):
     err = np.abs(gpu - ref)
     rms = float(np.sqrt(np.mean(ref ** 2)))

@@ -63,13 +63,21 @@ def test_workspace_size_and_layout():
         assert Lm["hq_codes"] == Lm["h_bf16"]
     # larger T needs no less workspace
     assert moe.moe_workspace_size(cfg(T=4096)) > n
+    # the y rows: fp16 codes then one exponent byte per 32 features (default), or fp32
+    P, H = 64 * 8, 4608
+    assert c.y_format == moe.Y_FP16E and moe.moe_y_bytes(c) == P * H * 2 + P * H // 32
+    c32 = cfg(y_format="fp32")
+    assert moe.moe_y_bytes(c32) == P * H * 4
+    L32 = moe.moe_workspace_layout(c32)
+    assert L32["total"] - L32["y_perm"] >= P * H * 4 and L["total"] - L["y_perm"] >= P * H * 2 + P * H // 32
+    assert L32["total"] > L["total"]
 
 
 @pytest.mark.parametrize("kw,status", [
     (dict(T=0), 2), (dict(T=70000), 2), (dict(k=0), 2), (dict(k=33), 2), (dict(E=4, k=8), 2),
     (dict(E=2000), 2), (dict(H=4608 + 128), 2), (dict(F=128), 2), (dict(fmt="mxfp8", F=128 + 64), 2),
     (dict(swiglu_cap=-1.0), 1), (dict(mx_scale_mode=2), 1), (dict(act_global_mode=2), 1),
-    (dict(fmt="mxfp8", act_global_mode=1), 1), (dict(ffn_schedule=2), 1),
+    (dict(fmt="mxfp8", act_global_mode=1), 1), (dict(ffn_schedule=2), 1), (dict(y_format=2), 1),
 ])
 def test_config_validation(kw, status):
     with pytest.raises(moe.MoeError) as ei:

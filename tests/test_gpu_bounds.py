@@ -12,6 +12,8 @@ unchanged."""
 import numpy as np
 import pytest
 
+import parity
+
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
@@ -61,7 +63,7 @@ def test_out_of_range_pair_position_is_flagged_and_skipped(checked_build):
     gw.forward()
     assert moe.moe_debug_bounds_status()[0] == 0
     P = T * k
-    y = gw.ws_view("y_perm", torch.float32, P * H).view(P, H)
+    y = gw.y_raw()
     wts = gw.ws_view("topk_w", torch.float32, P).view(T, k)
     pp = gw.ws_view("pair_pos", torch.int32, P).view(T, k)
     good = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
@@ -77,5 +79,5 @@ def test_out_of_range_pair_position_is_flagged_and_skipped(checked_build):
     rows = [t for t in range(T) if t != 3]
     assert torch.equal(out[rows].view(torch.int16), good[rows].view(torch.int16))
     # token 3 is the sum of its other slot only
-    y3 = y[pp[3, 0].item()].double() * wts[3, 0].double()
-    assert np.allclose(out[3].double().cpu().numpy(), y3.cpu().numpy(), rtol=2 ** -7, atol=1e-6)
+    y3 = parity.y_rows_f64(moe, gw.cfg, y, [pp[3, 0].item()])[0] * float(wts[3, 0])
+    assert np.allclose(out[3].double().cpu().numpy(), y3, rtol=2 ** -7, atol=1e-6)

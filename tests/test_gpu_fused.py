@@ -47,7 +47,7 @@ def run(gw, cfg):
     assert moe.moe_poll_device_status(gw.ws) == 0
     P, H, R, F = gw.w["T"] * gw.w["k"], gw.w["H"], gw.layout["R"], gw.w["F"]
     cb = F // 2 if gw.w["fmt"] == "nvfp4" else F
-    y = gw.ws_view("y_perm", torch.int32, P * H).clone()
+    y = gw.y_raw().clone()
     hq = gw.ws_view("hq_codes", torch.uint8, R * cb).view(R, cb).clone()
     return out, y, hq
 

@@ -200,7 +200,7 @@ def test_staged_calls_equal_forward(name):
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     perm = torch.empty(T * k, dtype=torch.int32, device=dev)
     pp = torch.empty((T, k), dtype=torch.int32, device=dev)
-    y = torch.empty((T * k, H), dtype=torch.float32, device=dev)
+    y = torch.empty(moe.moe_y_bytes(c), dtype=torch.uint8, device=dev)
     out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
     ws = torch.empty_like(gw.ws)
     moe.moe_route(c, gw.x, gw.w_router, gw.bias, idx, wts, ws)
@@ -274,15 +274,17 @@ def check_pair_rows(gw, r, experts, cache, max_rows=256):
     The products of the two encodings are exact, so the GPU's y differs only
     by its fp32 accumulation over F and the epilogue's scale multiply:
     |dy| <= 2^-12 sum_f |h^_f w_of| (the bound of an fp32 sum of F = 2304
-    terms is below 2^-12 even with truncating adds).  (The h codes themselves
-    are checked against the oracle by their flip rate, and the layer output
-    end to end.)"""
+    terms is below 2^-12 even with truncating adds), plus, for the compact y
+    rows, their rounding to 11 significant bits (2^-11 of the fp32 value).
+    (The h codes themselves are checked against the oracle by their flip
+    rate, and the layer output end to end.)"""
     w, k, H, F = gw.w, gw.w["k"], gw.w["H"], gw.w["F"]
     nt = gw.layout["tile_rows"]
     R = gw.layout["R"]
     P = w["T"] * k
     nv = w["fmt"] == "nvfp4"
-    y_all = gw.ws_view("y_perm", torch.float32, P * H).view(P, H)
+    yraw = gw.y_raw()
+    rel = parity.y_rel(moe, gw.cfg)
     cb, bs = (F // 2, 16) if nv else (F, 32)
     hq = gw.ws_view("hq_codes", torch.uint8, R * cb).view(R, cb)
     hs_all = untile_scales(gw.ws_view("hq_scales", torch.uint8, (R // nt) * (F // bs // 4) * 512).cpu().numpy(),
@@ -300,8 +302,9 @@ def check_pair_rows(gw, r, experts, cache, max_rows=256):
             cache[e] = oracle.quantized_expert(w, e)
         wd = oracle.decode(w["fmt"], *cache[e]["down"], per_tensor=True)
         y_ref = h @ wd.T
-        bound = 2.0 ** -12 * (np.abs(h) @ np.abs(wd).T) + 1e-30
-        y_gpu = y_all[torch.from_numpy(ps + lo).cuda()].cpu().numpy().astype(np.float64)
+        acc = 2.0 ** -12 * (np.abs(h) @ np.abs(wd).T)
+        bound = acc + rel * (np.abs(y_ref) + acc) + 1e-30
+        y_gpu = parity.y_rows_f64(moe, gw.cfg, yraw, ps + lo)
         err = np.abs(y_gpu - y_ref)
         assert np.all(err <= bound), f"expert {e}: |dy| above the accumulation bound at {np.argmax(err / bound)}"
         worst = max(worst, float((err / bound).max()))
@@ -312,11 +315,8 @@ def check_combine_rows(gw, r, out_gpu, tokens):
     """The combine on the GPU's own y and weights: out[t] = bf16(sum_j w y)
     within half a bf16 ulp plus the fp32 summation error."""
     k, H = gw.w["k"], gw.w["H"]
-    P = gw.w["T"] * k
-    y_all = gw.ws_view("y_perm", torch.float32, P * H).view(P, H)
     pp = r["pair_pos"][tokens]
-    y = y_all[torch.from_numpy(pp.ravel().astype(np.int64)).cuda()].cpu().numpy().astype(np.float64)
-    y = y.reshape(len(tokens), k, H)
+    y = parity.y_rows_f64(moe, gw.cfg, gw.y_raw(), pp.ravel()).reshape(len(tokens), k, H)
     wt = r["w"][tokens].astype(np.float64)
     ref = np.einsum("tj,tjh->th", wt, y)
     bound = 2.0 ** -8 * np.abs(ref) + 1e-6 * np.einsum("tj,tjh->th", np.abs(wt), np.abs(y)) + 1e-30

@@ -485,3 +485,45 @@ def test_nvfp4_static_global_saturates_at_2688_g():
     dyn = oracle.nvfp4_quantize(x)
     sta = oracle.nvfp4_quantize_static(x, dyn[2])
     assert all(np.array_equal(a, b) for a, b in zip(dyn, sta))
+
+
+def test_y16_format_hand_worked_blocks():
+    # The compact y rows: per 32-feature block e = floor(log2 amax) - 14 and
+    # code = fp16(y * 2^-e).  Worked by hand from the fp16 bit layout (sign,
+    # 5 exponent bits biased by 15, 10 mantissa bits):
+    y = np.zeros((1, 128), np.float32)
+    # block 0: amax 3 -> e = 1 - 14 = -13; 1 -> 2^13 = 0x7000, -0.5 -> -2^12 =
+    # 0xEC00, 3 -> 1.5 * 2^14 = 0x7600
+    y[0, 0], y[0, 1], y[0, 2] = 1.0, -0.5, 3.0
+    # block 1: all zero -> e = 0, codes 0
+    # block 2: amax 1 -> e = -14; 1 + 2^-11 -> 16392, a tie between 16384 and
+    # 16400 -> even: 0x7400; 1 + 3 * 2^-11 -> 16408, a tie -> 16416 = 0x7402
+    y[0, 64], y[0, 65], y[0, 66] = 1.0, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11
+    # block 3: amax 2^-100 -> e clamped at -110: 2^-100 * 2^110 = 2^10 = 0x6400
+    y[0, 96] = 2.0 ** -100
+    codes, ex = oracle.encode_y16(y)
+    assert list(ex[0]) == [-13, 0, -14, -110]
+    assert list(codes[0, :3]) == [0x7000, 0xEC00, 0x7600] and not codes[0, 3:64].any()
+    assert list(codes[0, 64:67]) == [0x7400, 0x7400, 0x7402]
+    assert codes[0, 96] == 0x6400
+    # a large block: amax 1e30, floor(log2) = 99 -> e = 85
+    big = np.full((1, 32), 1e30, np.float32)
+    assert oracle.encode_y16(big)[1][0, 0] == 85
+    dec = oracle.decode_y16(codes, ex)
+    assert dec[0, 0] == 1.0 and dec[0, 1] == -0.5 and dec[0, 2] == 3.0 and dec[0, 96] == 2.0 ** -100
+
+
+def test_y16_format_error_bound_and_range():
+    # every block's maximum lands in [2^14, 2^15) and each value keeps 11
+    # significant bits: |decoded - y| <= 2^-11 |y| (RNE, half an fp16 ulp)
+    rng = np.random.default_rng(11)
+    y = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-30, 30, (64, 1)))).astype(np.float32)
+    y[3, 32:64] = 0.0
+    codes, ex = oracle.encode_y16(y)
+    dec = oracle.decode_y16(codes, ex)
+    y64 = y.astype(np.float64)
+    assert np.all(np.abs(dec - y64) <= 2.0 ** -11 * np.abs(y64))
+    scaled_max = np.abs(codes.view(np.float16).astype(np.float64)).reshape(64, 8, 32).max(2)
+    nz = np.abs(y64).reshape(64, 8, 32).max(2) > 0
+    assert np.all((scaled_max[nz] >= 2.0 ** 14) & (scaled_max[nz] < 2.0 ** 15))
+    assert np.all(ex[~nz] == 0)

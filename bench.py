@@ -68,6 +68,57 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
+def traffic_key(kname: str, w: dict, tile_rows: int) -> str:
+    """Which measured kernel a roof's traffic ratio comes from."""
+    if kname == "ffn":
+        return f"ffn_decode_{w['fmt']}"
+    return f"{kname}_{'token_major' if tile_rows == 128 else 'decode'}_{w['fmt']}"
+
+
+def write_traffic(pairs):
+    """profiles/gemm_traffic.json from ncu captures of small cases: each pair
+    is (the plain bench run's JSON line, the ncu CSV of dram__bytes_read.sum
+    and dram__bytes_write.sum of its GEMM launches).  Per kernel, the mean
+    DRAM bytes per launch over its algorithmic bytes (kernel_bytes) is stored
+    with the GEMM sources' hash; the bench applies the ratio to a full
+    workload's algorithmic bytes (traffic grows with the units processed:
+    touched experts' weights, pairs' activations)."""
+    import csv
+    import synth
+    out = {"source_sha": kernel_source_sha(),
+           "how": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum per launch on small cases; ratio = "
+                  "mean DRAM bytes per launch / algorithmic bytes (bench.py kernel_bytes); the bench multiplies a "
+                  "full workload's algorithmic bytes by the ratio",
+           "ratios": {}}
+    for js, cs in pairs:
+        line = json.loads(open(js).read().strip().splitlines()[-1])
+        cfg = line["config"]
+        w = dict(synth.WORKLOADS[cfg["workload"]])
+        fused = cfg["ffn_schedule"] == "fused decode kernel"
+        kb = kernel_bytes(w, cfg["touched_experts"], fused, cfg.get("y_format", "fp16e") == "fp16e")
+        per = {}
+        rows = list(csv.reader(l for l in open(cs) if l.startswith('"')))
+        hdr = rows[0]
+        ki, ii, mi, vi = (hdr.index(n) for n in ("Kernel Name", "ID", "Metric Name", "Metric Value"))
+        for r in rows[1:]:
+            if r[mi] not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+                continue
+            per.setdefault((r[ki], r[ii]), 0.0)
+            per[(r[ki], r[ii])] += float(r[vi].replace(",", ""))
+        groups = {}
+        for (kn, _), b in per.items():
+            kname = "ffn" if "k_moe_ffn_decode" in kn else ("gemm1" if kn.split("(")[0].endswith("1>") else "gemm2")
+            groups.setdefault(kname, []).append(b)
+        for kname, vals in groups.items():
+            mean = sum(vals) / len(vals)
+            key = traffic_key(kname, w, cfg.get("tile_rows", 128 if not fused else 64))
+            out["ratios"][key] = {"workload": cfg["workload"], "launches": len(vals), "dram_bytes": mean,
+                                  "algorithmic_bytes": kb[kname], "ratio": round(mean / kb[kname], 4)}
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps(out, indent=1))
+
+
 # ----------------------------------------------------------------------------
 # algorithmic bytes of one launch of each expert GEMM
 # ----------------------------------------------------------------------------
@@ -86,6 +137,22 @@ def gemm_bytes(w: dict, n_touched: int, h_quantised_in_gemm1: bool = False, y_co
     g1 = n_touched * (2 * (F * H * bpe + glob)) + P * (H * bpe + glob) + h_out
     g2 = n_touched * (H * F * bpe + glob) + P * (F * bpe + glob) + P * H * (2 + 1 / 32 if y_compact else 4)
     return g1, g2
+
+
+def kernel_bytes(w: dict, n_touched: int, fused: bool, y_compact: bool = True) -> dict:
+    """Algorithmic bytes per launch of the kernels whose roofs the bench
+    reports: gemm1 and gemm2 (separate kernels; GEMM1 writes MXFP8 h codes in
+    its epilogue, NVFP4 h as bf16), or ffn (the fused decode kernel: both
+    GEMMs' bytes without the h round trip, which stays in L2)."""
+    mx = w["fmt"] == "mxfp8"
+    g1, g2 = gemm_bytes(w, n_touched, mx, y_compact)
+    if not fused:
+        return {"gemm1": g1, "gemm2": g2}
+    P, F = w["T"] * w["k"], w["F"]
+    bpe = 1 + 1 / 32 if mx else 0.5 + 1 / 16
+    h_write = P * F * (bpe if mx else 2)             # GEMM1's h out (MXFP8 codes + scales, or bf16)
+    h_read = P * (F * bpe + (0 if mx else 4))        # GEMM2's encoded h in
+    return {"ffn": g1 + g2 - h_write - h_read}
 
 
 def gemm_flops(w: dict):
@@ -389,8 +456,8 @@ def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, h
     the intermediates (x codes, h, y) are the implementation's traffic, which
     one fused kernel per layer could keep on chip; each GEMM's own roof counts
     the activations it reads and writes."""
-    g1_bytes, g2_bytes = gemm_bytes(w, n_touched, gw.layout["hq_codes"] == gw.layout["h_bf16"],
-                                    gw.cfg.y_format == gw.moe.Y_FP16E)
+    fused = ffn_fused(gw)
+    kb = kernel_bytes(w, n_touched, fused, gw.cfg.y_format == gw.moe.Y_FP16E)
     g1_flops, g2_flops = gemm_flops(w)
     g1_s, g2_s = stage_ms["gemm1_gate_up_swiglu"] / 1e3, stage_ms["gemm2_down"] / 1e3
     balance = tpeak * 1e12 / (hbm_gbs * 1e9)        # flop per byte at which the two roofs meet
@@ -408,17 +475,10 @@ def rooflines(w: dict, gw, n_touched: int, ms_per_step: float, stage_ms: dict, h
                 "frac": (f / sec / 1e12 / tpeak) if tensor_bound else (b / sec / 1e9 / hbm_gbs),
                 "algorithmic_bytes": b, "flops": f}
 
-    if ffn_fused(gw):
-        # the fused kernel's h round trip stays on chip or in L2 (its
-        # algorithmic bytes are GEMM1's input and GEMM2's weights and output)
-        P, F = w["T"] * w["k"], w["F"]
-        nv = w["fmt"] == "nvfp4"
-        bpe = 0.5 + 1 / 16 if nv else 1 + 1 / 32
-        h_write = P * F * (2 if nv else bpe)             # GEMM1's h out (bf16, or MXFP8 codes + scales)
-        h_read = P * (F * bpe + (4 if nv else 0))        # GEMM2's encoded h in
-        ffn = roof(g1_bytes + g2_bytes - h_write - h_read, g1_flops + g2_flops, g1_s)
+    if fused:
+        ffn = roof(kb["ffn"], g1_flops + g2_flops, g1_s)
         return {"ffn": ffn, "layer": roof(layer_bytes, layer_flops, step_s), "machine_balance_flop_per_byte": balance}
-    return {"gemm1": roof(g1_bytes, g1_flops, g1_s), "gemm2": roof(g2_bytes, g2_flops, g2_s),
+    return {"gemm1": roof(kb["gemm1"], g1_flops, g1_s), "gemm2": roof(kb["gemm2"], g2_flops, g2_s),
             "layer": roof(layer_bytes, layer_flops, step_s), "machine_balance_flop_per_byte": balance}
 
 
@@ -484,7 +544,8 @@ def measure_workload(moe, torch, name: str, steps: int, warmup: int, launch: str
                     "expert_ffn_fused": ffn_ms, "combine": stage_ms["combine"]}
     res = {"workload": name, "T": w["T"], "fmt": w["fmt"], "touched_experts": n_touched, "steps": steps,
            "launch": how, "ffn_schedule": "fused decode kernel" if ffn_fused(gw) else "separate kernels",
-           "y_format": y_format, "ms_per_step": ms_per_step, "us_per_layer": ms_per_step * 1e3,
+           "y_format": y_format, "tile_rows": int(gw.layout["tile_rows"]), "ms_per_step": ms_per_step,
+           "us_per_layer": ms_per_step * 1e3,
            "tokens_per_s": job_tokens_per_s(w["T"], steps, world, ms), "stage_ms": stage_ms,
            "roofline": roof, "clocks": clocks.summary(),
            "gpu_launches": moe.moe_forward_kernel_count(gw.cfg) * steps}
@@ -507,6 +568,9 @@ def main():
     ap.add_argument("--no-per-workload", action="store_true", help="skip the other configurations")
     ap.add_argument("--no-tensor-peak", action="store_true",
                     help="skip the MMA-rate measurement (tensor roofs from the bf16 rate x nominal ratio)")
+    ap.add_argument("--write-traffic", nargs="+", metavar="JSON,CSV",
+                    help="write profiles/gemm_traffic.json from plain-run JSON lines and their ncu DRAM-byte CSVs "
+                         "(no GPU needed), then exit")
     ap.add_argument("--y-format", default="fp16e", choices=["fp16e", "fp32"],
                     help="moe_config.y_format: the expert outputs between the down GEMM and the combine as fp16 "
                          "codes with an exponent per 32 features (default) or fp32")
@@ -516,6 +580,9 @@ def main():
     ap.add_argument("--launch", default="graph", choices=["graph", "eager"],
                     help="timed steps as CUDA-graph replays of captured moe_forward calls (default) or eager calls")
     args = ap.parse_args()
+    if args.write_traffic:
+        write_traffic([tuple(p.split(",")) for p in args.write_traffic])
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
@@ -634,12 +701,15 @@ def main():
     # decode batches the fused expert FFN) ----
     kname = "ffn" if "ffn" in main_res["roofline"] else "gemm1"
     g1 = main_res["roofline"][kname]
-    traffic = None
+    tkey = traffic_key(kname, w, main_res["tile_rows"])
+    traffic, traffic_note = None, None
     if os.path.exists(TRAFFIC_FILE):
         tr = json.load(open(TRAFFIC_FILE))
-        ent = tr.get(args.workload, {}).get(kname)
+        ent = tr.get("ratios", {}).get(tkey)
         if ent and tr.get("source_sha") == kernel_source_sha():
-            traffic = ent
+            traffic = ent["ratio"] * g1["algorithmic_bytes"]
+            traffic_note = (f"DRAM bytes of {tkey} measured by ncu on {ent['workload']} ({ent['ratio']:.4f} x its "
+                            "algorithmic bytes), scaled to this launch's algorithmic bytes")
     tensor_bound = g1["bound"] == "tensor"
     hbm = {"achieved": g1["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": g1["hbm_frac"],
            "algorithmic_bytes": g1["algorithmic_bytes"], "peak_source": pk["source"]}
@@ -652,7 +722,8 @@ def main():
     roofline = {"bound": "tensor" if tensor_bound else "hbm",
                 "kernel": "ffn_decode_fused" if kname == "ffn" else "gemm1_gate_up_swiglu",
                 "achieved": top["achieved"], "peak": top["peak"], "unit": top["unit"], "frac": top["frac"],
-                "traffic": traffic, "peak_source": top["peak_source"], "hbm": hbm, "tensor": tensor,
+                "traffic": traffic, "traffic_note": traffic_note, "peak_source": top["peak_source"], "hbm": hbm,
+                "tensor": tensor,
                 "gemm2": main_res["roofline"].get("gemm2"), "layer": main_res["roofline"]["layer"],
                 "machine_balance_flop_per_byte": main_res["roofline"]["machine_balance_flop_per_byte"]}
     layer = {"us_per_layer": ms_per_step * 1e3, "step_us": step_dist, "stage_ms": main_res["stage_ms"]}
@@ -711,6 +782,7 @@ def main():
                            "fmt": w["fmt"], "touched_experts": main_res["touched_experts"],
                            "parallelism": f"replicas{world}", "launch": main_res["launch"],
                            "ffn_schedule": main_res["ffn_schedule"], "y_format": main_res["y_format"],
+                           "tile_rows": main_res["tile_rows"],
                            "l2": "inputs larger than L2: the touched expert weights of one step "
                                  f"({gemm_bytes(w, main_res['touched_experts'])[0] / 1e9:.2f} GB read by GEMM1 "
                                  "alone) against a 129 MB L2; no flush"},

@@ -34,7 +34,10 @@ namespace moe {
 namespace {
 
 constexpr float kTcGamma = 1.0f / 2048.0f;        // assumed |l_tc - l| / (||x|| ||w_e||) bound
-constexpr float kKeySlack = 1.0f / 1048576.0f;   // fp32 sigmoid and bias-add rounding of A_e
+// the approximate keys' own arithmetic: a sigmoid from __expf and a
+// reciprocal (|error| below 2^-22 of the key: s(1-s) times the exponential's
+// relative error, plus the two roundings) and the fp32 bias add
+constexpr float kKeySlack = 1.0f / 262144.0f;
 constexpr float kNormInflate = 1.0f + 1.0f / 1024.0f;  // fp32 sum-of-squares rounding -> upper bound
 
 // ---------------------------------------------------------------------------
@@ -236,14 +239,19 @@ struct Kahan {
 // of exact two-sums, so every lane returns the same value.  Error at most
 // (31 + 2 + 1) u sum|x w|, u = 2^-24.  The NC experts share the loads of x
 // and their loads are issued together.
+// The products go straight from the bf16 halves of each word into an fp32
+// fused multiply-add (fma.rn.f32.bf16: the bf16 operands are exact in fp32,
+// the product is exact, one rounding per add), lower element first: the
+// same chain as unpacking both to fp32 and using fmaf, without the unpacking.
 __device__ __forceinline__ void slot_fma(const uint4& xa, const uint4& wa, float& p) {
   const uint32_t xv[4] = {xa.x, xa.y, xa.z, xa.w};
   const uint32_t wv[4] = {wa.x, wa.y, wa.z, wa.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    p = __fmaf_rn(__uint_as_float(xv[j] << 16), __uint_as_float(wv[j] << 16), p);
-    p = __fmaf_rn(__uint_as_float(xv[j] & 0xFFFF0000u), __uint_as_float(wv[j] & 0xFFFF0000u), p);
-  }
+  for (int j = 0; j < 4; ++j)
+    asm("{\n.reg .b16 xl, xh, wl, wh;\nmov.b32 {xl, xh}, %1;\nmov.b32 {wl, wh}, %2;\n"
+        "fma.rn.f32.bf16 %0, xl, wl, %0;\nfma.rn.f32.bf16 %0, xh, wh, %0;\n}"
+        : "+f"(p)
+        : "r"(xv[j]), "r"(wv[j]));
 }
 
 template <int NC>
@@ -332,11 +340,10 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
     const uint4 u = *reinterpret_cast<const uint4*>(xr + i);
     const uint32_t v[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float a = __uint_as_float(v[j] << 16), b = __uint_as_float(v[j] & 0xFFFF0000u);
-      ss = fmaf(a, a, ss);
-      ss = fmaf(b, b, ss);
-    }
+    for (int j = 0; j < 4; ++j)
+      asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %1;\nfma.rn.f32.bf16 %0, l, l, %0;\nfma.rn.f32.bf16 %0, h, h, %0;\n}"
+          : "+f"(ss)
+          : "r"(v[j]));
   }
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float xn = sqrtf(ss) * kNormInflate;
@@ -349,7 +356,7 @@ __global__ void __launch_bounds__(kSelWarps * 32) k_router_select(
     lov[i] = -INFINITY;
     hiv[i] = -INFINITY;
     if (e < E) {
-      const float a = __fadd_rn(router_sigmoid(ltv[i]), bias[e]);
+      const float a = __fadd_rn(__frcp_rn(__fadd_rn(1.0f, __expf(-ltv[i]))), bias[e]);
       const float m = 0.25f * kTcGamma * xn * wnorm[e] + kKeySlack;
       lov[i] = a - m;
       hiv[i] = a + m;

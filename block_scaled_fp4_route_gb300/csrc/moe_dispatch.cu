@@ -97,7 +97,16 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
   int c = 0;
   if (e < E) {
     if (chunk_counts) {
-      for (int ch = 0; ch < nch; ++ch) c += chunk_counts[(int64_t)ch * E + e];
+      // eight chunk counts requested at a time (integer sums: any order)
+      int ch = 0;
+      for (; ch + 8 <= nch; ch += 8) {
+        int v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = chunk_counts[(int64_t)(ch + i) * E + e];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c += v[i];
+      }
+      for (; ch < nch; ++ch) c += chunk_counts[(int64_t)ch * E + e];
       if (counts_out) counts_out[e] = c;
     } else {
       c = offsets_in[e + 1] - offsets_in[e];
@@ -275,7 +284,7 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
   if (e != cudaSuccess) return e;
   return launch_k(k_dispatch_small, dim3(1), dim3(1024), smem, st, pdl, idx, c.T, c.k, c.E, counts, offsets, perm,
                   pair_pos, seg_start, tiles, rt_base, status, tile_rows(c), sync,
-                  sync ? (int)ffn_sync_ints(c) : 0);
+                  sync && ffn_fused(c) ? (int)ffn_sync_ints(c) : 0);
 }
 
 int dispatch_chunks(const moe_config& c) { return (c.T + kChunkTokens - 1) / kChunkTokens; }
@@ -296,9 +305,11 @@ cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, con
 cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, int32_t* counts_out,
                              const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
                              int32_t* rt_base, uint32_t* status, int32_t* sync, cudaStream_t st, bool pdl) {
+  // the counters exist for the fused decode FFN only
+  const int nsync = sync && ffn_fused(c) ? (int)ffn_sync_ints(c) : 0;
   return launch_k(k_scan_plan, dim3(1), dim3(1024), 0, st, pdl, chunk_counts, dispatch_chunks(c), counts_out,
-                  offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status, tile_rows(c), sync,
-                  sync ? (int)ffn_sync_ints(c) : 0, (int)max_row_tiles(c));
+                  offsets_in, c.E, offsets_out, seg_start, tiles, rt_base, status, tile_rows(c), sync, nsync,
+                  (int)max_row_tiles(c));
 }
 
 }  // namespace moe

@@ -251,7 +251,7 @@ moe_status dispatch_impl(const moe_config& c, const int32_t* idx, int32_t* count
   if (launch_dispatch(c, idx, bm, chunk_counts, st, pdl) != cudaSuccess ||
       launch_scan_plan(c, chunk_counts, counts, nullptr, offsets, seg, tiles, rtb, status, at<int32_t>(ws, L.ffn_sync),
                        st, true) != cudaSuccess ||
-      launch_dispatch_scatter(c, idx, bm, offsets, perm, pair_pos, st, true) != cudaSuccess)
+      launch_dispatch_scatter(c, idx, bm, chunk_counts, offsets, perm, pair_pos, st, true) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -80,7 +80,7 @@ __device__ int block_exclusive_scan(int v, int* total, int* sh) {
 // counts (if non-null) or offsets_in -> offsets_out, seg_start, tile list.
 // The pair counts come from per-chunk counts (summed here and written to
 // counts_out), or from offsets_in.
-__global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ chunk_counts, int nch,
+__global__ void __launch_bounds__(1024) k_scan_plan(int32_t* __restrict__ chunk_counts, int nch,
                                                     int32_t* __restrict__ counts_out,
                                                     const int32_t* __restrict__ offsets_in, int E,
                                                     int32_t* __restrict__ offsets_out, int32_t* __restrict__ seg_start,
@@ -97,16 +97,24 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
   int c = 0;
   if (e < E) {
     if (chunk_counts) {
-      // eight chunk counts requested at a time (integer sums: any order)
+      // eight chunk counts requested at a time; each is replaced by the
+      // expert's pairs in the chunks before it (the scatter's chunk base)
       int ch = 0;
       for (; ch + 8 <= nch; ch += 8) {
         int v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = chunk_counts[(int64_t)(ch + i) * E + e];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) c += v[i];
+        for (int i = 0; i < 8; ++i) {
+          chunk_counts[(int64_t)(ch + i) * E + e] = c;
+          c += v[i];
+        }
       }
-      for (; ch < nch; ++ch) c += chunk_counts[(int64_t)ch * E + e];
+      for (; ch < nch; ++ch) {
+        const int v = chunk_counts[(int64_t)ch * E + e];
+        chunk_counts[(int64_t)ch * E + e] = c;
+        c += v;
+      }
       if (counts_out) counts_out[e] = c;
     } else {
       c = offsets_in[e + 1] - offsets_in[e];
@@ -140,40 +148,35 @@ __global__ void __launch_bounds__(1024) k_scan_plan(const int32_t* __restrict__ 
   if (e == 0) rt_base[E] = rtot;
 }
 
-__global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __restrict__ idx, int T, int k,
+// One thread per pair (t, j), e = idx[t, j]: its position in the dispatch
+// order is offsets[e] + the expert's pairs in the 256-token chunks before
+// t's (chunk_base, from the tile-plan kernel) + the expert's tokens before t
+// inside the chunk (popcounts of at most 8 bitmap words).  Every pair is
+// independent, so a hot expert's pairs spread over the whole grid.
+__global__ void __launch_bounds__(kDThreads) k_disp_scatter(const int32_t* __restrict__ idx, int T, int k, int E,
                                                             const uint32_t* __restrict__ bitmap,
+                                                            const int32_t* __restrict__ chunk_base,
                                                             const int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ perm, int32_t* __restrict__ pair_pos) {
-  __shared__ int sh[32];
-  const int e = blockIdx.x;
   const int W = (T + 31) / 32;
-  const int wpt = (W + blockDim.x - 1) / blockDim.x;
+  const int64_t P = (int64_t)T * k;
+  const int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  const int w0 = threadIdx.x * wpt;
-  int c = 0;
-  for (int i = 0; i < wpt; ++i)
-    if (w0 + i < W) c += __popc(bitmap[(int64_t)e * W + w0 + i]);
-  int tot;
-  int rank = block_exclusive_scan(c, &tot, sh);
-  const int base = offsets[e];
-  for (int i = 0; i < wpt; ++i) {
-    if (w0 + i >= W) break;
-    uint32_t v = bitmap[(int64_t)e * W + w0 + i];
-    while (v) {
-      int b = __ffs(v) - 1;
-      v &= v - 1;
-      int t = (w0 + i) * 32 + b;
-      int j = 0;
-      if (MOE_IN_BOUNDS(t < T))
-        while (j < k && idx[t * k + j] != e) ++j;
-      int p = base + rank;
-      if (MOE_IN_BOUNDS(t < T && j < k && p < T * k)) {
-        perm[p] = t * k + j;
-        pair_pos[t * k + j] = p;
-      }
-      ++rank;
-    }
+  if (p >= P) return;
+  const int t = (int)(p / k);
+  const int e = idx[p];
+  if (!MOE_IN_BOUNDS((unsigned)e < (unsigned)E)) return;
+  const int ch = t / kChunkTokens;
+  const int wt = t >> 5;
+  const uint32_t* bm = bitmap + (int64_t)e * W;
+  int rank = 0;
+  for (int w = ch * (kChunkTokens / 32); w < wt; ++w) rank += __popc(bm[w]);
+  rank += __popc(bm[wt] & ((1u << (t & 31)) - 1u));
+  const int64_t pos = (int64_t)offsets[e] + chunk_base[(int64_t)ch * E + e] + rank;
+  if (MOE_IN_BOUNDS(pos >= 0 && pos < P)) {
+    perm[pos] = (int32_t)p;
+    pair_pos[p] = (int32_t)pos;
   }
 }
 
@@ -296,13 +299,14 @@ cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, uint32_t* b
 }
 
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
-                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st,
-                                    bool pdl) {
-  return launch_k(k_disp_scatter, dim3(c.E), dim3(kDThreads), 0, st, pdl, idx, c.T, c.k, bitmap, offsets, perm,
-                  pair_pos);
+                                    const int32_t* chunk_base, const int32_t* offsets, int32_t* perm,
+                                    int32_t* pair_pos, cudaStream_t st, bool pdl) {
+  const int64_t P = (int64_t)c.T * c.k;
+  return launch_k(k_disp_scatter, dim3((unsigned)((P + kDThreads - 1) / kDThreads)), dim3(kDThreads), 0, st, pdl,
+                  idx, c.T, c.k, c.E, bitmap, chunk_base, offsets, perm, pair_pos);
 }
 
-cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, int32_t* counts_out,
+cudaError_t launch_scan_plan(const moe_config& c, int32_t* chunk_counts, int32_t* counts_out,
                              const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
                              int32_t* rt_base, uint32_t* status, int32_t* sync, cudaStream_t st, bool pdl) {
   // the counters exist for the fused decode FFN only

@@ -79,9 +79,11 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t row_bytes,
 int dispatch_chunks(const moe_config& c);
 cudaError_t launch_dispatch(const moe_config& c, const int32_t* idx, uint32_t* bitmap, int32_t* chunk_counts,
                             cudaStream_t st, bool pdl);
+// chunk_base: the chunk counts after launch_scan_plan replaced them by each
+// expert's pairs in the earlier chunks
 cudaError_t launch_dispatch_scatter(const moe_config& c, const int32_t* idx, const uint32_t* bitmap,
-                                    const int32_t* offsets, int32_t* perm, int32_t* pair_pos, cudaStream_t st,
-                                    bool pdl);
+                                    const int32_t* chunk_base, const int32_t* offsets, int32_t* perm,
+                                    int32_t* pair_pos, cudaStream_t st, bool pdl);
 // Whole dispatch + tile plan in one CTA when the token bitmaps fit in shared
 // memory (decode batches); returns cudaErrorNotSupported otherwise.
 bool dispatch_fits_one_cta(const moe_config& c);
@@ -92,8 +94,9 @@ cudaError_t launch_dispatch_small(const moe_config& c, const int32_t* idx, int32
 // offsets_in when chunk_counts == nullptr) -> offsets_out (optional),
 // seg_start [E+1], tiles, rt_base [E+1] (first row tile of each expert; the
 // total at E); zeroes *status when given, and the fused decode FFN's
-// completion counts (sync, 2 * max_row_tiles int32) when given
-cudaError_t launch_scan_plan(const moe_config& c, const int32_t* chunk_counts, int32_t* counts_out,
+// counters (sync) when given and that kernel runs.  chunk_counts (if given)
+// are replaced by each expert's pairs in the chunks before (launch_dispatch_scatter).
+cudaError_t launch_scan_plan(const moe_config& c, int32_t* chunk_counts, int32_t* counts_out,
                              const int32_t* offsets_in, int32_t* offsets_out, int32_t* seg_start, RowTile* tiles,
                              int32_t* rt_base, uint32_t* status, int32_t* sync, cudaStream_t st, bool pdl);
 

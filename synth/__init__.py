@@ -71,6 +71,9 @@ WORKLOADS = {
     # GB resident, touched weights still far above the L2 size)
     "profile_decode16_nvfp4_e96": dict(T=16, H=4608, E=96, k=8, F=2304, fmt="nvfp4", seed=21,
                                        outlier_frac=0.0, bias="uniform"),
+    # one token: 8 touched experts, one wave of 144 gate/up and 144 down tiles
+    "profile_decode1_nvfp4_e64": dict(T=1, H=4608, E=64, k=8, F=2304, fmt="nvfp4", seed=24,
+                                      outlier_frac=0.0, bias="uniform"),
     "profile_prefill2048_mxfp8_e64": dict(T=2048, H=4608, E=64, k=8, F=2304, fmt="mxfp8", seed=22,
                                           outlier_frac=0.0, bias="uniform"),
     "profile_prefill2048_nvfp4_e64": dict(T=2048, H=4608, E=64, k=8, F=2304, fmt="nvfp4", seed=23,

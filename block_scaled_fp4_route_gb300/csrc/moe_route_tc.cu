@@ -69,13 +69,23 @@ __global__ void __launch_bounds__(256) k_router_prep(const __nv_bfloat16* __rest
 }
 
 // ---------------------------------------------------------------------------
-// Logits tile: 128 tokens (MMA M, TMEM lanes) x up to 128 experts (MMA N,
+// Logits tile: 128 tokens (MMA M, TMEM lanes) x up to NE experts (MMA N,
 // TMEM columns) x all of H.  Warp 0: TMA producer; warp 1: MMA issuer; warp 2:
 // TMEM allocator; warps 4..7: epilogue (warp w reads lane quadrant w % 4).
+// NE = 128 (six stages), or 192 for large batches (five stages): each token
+// tile is then read by fewer CTAs, and 128 token tiles x 2 expert tiles fill
+// the GPU in under two waves where 128 x 3 take three.
 // ---------------------------------------------------------------------------
-constexpr int kRtStages = 6;
-constexpr int kRtBox = 128 * 128;  // one operand per stage: 128 rows x 64 bf16
-constexpr int kRtSmem = kRtStages * 2 * kRtBox + 256 + 1024;
+constexpr int kRtBox = 128 * 128;  // the token operand per stage: 128 rows x 64 bf16
+template <int NE>
+struct RtCfg {
+  static constexpr int STAGES = NE == 128 ? 6 : 5;
+  static constexpr int BOXW = NE * 128;                    // the expert operand per stage
+  static constexpr int STAGE = kRtBox + BOXW;
+  static constexpr int SMEM = STAGES * STAGE + 256 + 1024;
+  static constexpr int TMEM_COLS = NE <= 128 ? 128 : 256;  // a power of two
+  static_assert(SMEM <= 232448, "router tile shared memory");
+};
 
 __device__ __forceinline__ uint32_t idesc_bf16(uint32_t N) {
   // fp32 accumulator, bf16 A and B, both K-major, M = 128
@@ -90,20 +100,23 @@ __device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bd
       : "memory");
 }
 
+template <int NE>
 __global__ void __launch_bounds__(256, 1) k_router_tc(const __grid_constant__ CUtensorMap tmx,
                                                      const __grid_constant__ CUtensorMap tmw,
                                                      float* __restrict__ lt, int T, int E, int H,
                                                      uint32_t* status, long long limit) {
+  using R = RtCfg<NE>;
+  constexpr int kRtStages = R::STAGES;
   extern __shared__ uint8_t rt_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rt_smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * 2 * kRtBox);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRtStages * R::STAGE);
   uint64_t* empty = full + kRtStages;
   uint64_t* done = empty + kRtStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e0 = blockIdx.x * 128, t0 = blockIdx.y * 128;
-  const int N = min(128, E - e0);  // a multiple of 16
+  const int e0 = blockIdx.x * NE, t0 = blockIdx.y * 128;
+  const int N = min(NE, E - e0);  // a multiple of 16
   const int KB = H / 64;
 
   if (threadIdx.x == 0) {
@@ -116,7 +129,7 @@ __global__ void __launch_bounds__(256, 1) k_router_tc(const __grid_constant__ CU
     fence_barrier_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, R::TMEM_COLS);
     tmem_relinquish();
   }
   if (threadIdx.x == 32) {
@@ -139,8 +152,8 @@ __global__ void __launch_bounds__(256, 1) k_router_tc(const __grid_constant__ CU
           ok = false;
           break;
         }
-        uint8_t* sA = smem + stage * 2 * kRtBox;
-        mbar_expect_tx(&full[stage], 2 * kRtBox);
+        uint8_t* sA = smem + stage * R::STAGE;
+        mbar_expect_tx(&full[stage], R::STAGE);
         armed |= 1u << stage;
         armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
         tma_load_2d(sA, &tmx, &full[stage], kb * 128, t0);
@@ -168,7 +181,7 @@ __global__ void __launch_bounds__(256, 1) k_router_tc(const __grid_constant__ CU
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&full[stage], phase, abort_flag, status, ST_TIMEOUT_MMA, limit)) break;
         tc_fence_after();
-        uint8_t* sA = smem + stage * 2 * kRtBox;
+        uint8_t* sA = smem + stage * R::STAGE;
         const uint64_t da = sdesc_sw128(smem_u32(sA));
         const uint64_t db = sdesc_sw128(smem_u32(sA + kRtBox));
 #pragma unroll
@@ -211,7 +224,7 @@ __global__ void __launch_bounds__(256, 1) k_router_tc(const __grid_constant__ CU
   pdl_trigger();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, R::TMEM_COLS);
   }
 }
 
@@ -479,22 +492,36 @@ cudaError_t launch_router_tc(const moe_config& c, const __nv_bfloat16* x, const 
                 : c.E <= 512 ? k_router_select<16> : k_router_select<32>;
   static_assert(32 * 32 >= kMaxE, "selection experts per lane");
   cudaError_t ea = once_per_device(attr, [] {
-    cudaError_t r = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
+    cudaError_t r = cudaFuncSetAttribute(k_router_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RtCfg<128>::SMEM);
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(k_router_tc<192>, cudaFuncAttributeMaxDynamicSharedMemorySize, RtCfg<192>::SMEM);
     for (auto kern : {k_router_select<4>, k_router_select<8>, k_router_select<16>, k_router_select<32>})
       if (r == cudaSuccess)
         r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSelWarps * 3 * kMaxE * 4);
     return r;
   });
   if (ea != cudaSuccess) return ea;
+  // 192-expert tiles once 128-expert tiles would take more than two waves
+  int dev = 0, sms = 0;
+  cudaError_t ea2 = cudaGetDevice(&dev);
+  if (ea2 == cudaSuccess) ea2 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (ea2 != cudaSuccess) return ea2;
+  const bool wide = (int64_t)((c.T + 127) / 128) * ((c.E + 127) / 128) > 2 * (int64_t)sms;
+  const int ne = wide ? 192 : 128;
   CUtensorMap tmx, tmw;
-  if (!make_map(&tmx, x, c.T, (int64_t)c.H * 2, 128) || !make_map(&tmw, wr, c.E, (int64_t)c.H * 2, 128))
+  if (!make_map(&tmx, x, c.T, (int64_t)c.H * 2, 128) || !make_map(&tmw, wr, c.E, (int64_t)c.H * 2, ne))
     return cudaErrorInvalidValue;
   float* lt = scratch;
   float* wnorm = scratch + (size_t)c.T * c.E;
   cudaError_t e = launch_k(k_router_prep, dim3((c.E + 7) / 8), dim3(256), 0, st, pdl, wr, c.E, c.H, wnorm, status);
   if (e != cudaSuccess) return e;
-  e = launch_k(k_router_tc, dim3((c.E + 127) / 128, (c.T + 127) / 128), dim3(256), kRtSmem, st, true, tmx, tmw, lt,
-               c.T, c.E, c.H, status, 4000000000LL);
+  if (wide)
+    e = launch_k(k_router_tc<192>, dim3((c.E + 191) / 192, (c.T + 127) / 128), dim3(256), RtCfg<192>::SMEM, st, true,
+                 tmx, tmw, lt, c.T, c.E, c.H, status, 4000000000LL);
+  else
+    e = launch_k(k_router_tc<128>, dim3((c.E + 127) / 128, (c.T + 127) / 128), dim3(256), RtCfg<128>::SMEM, st, true,
+                 tmx, tmw, lt, c.T, c.E, c.H, status, 4000000000LL);
   if (e != cudaSuccess) return e;
   return launch_k(select, dim3((c.T + kSelWarps - 1) / kSelWarps), dim3(kSelWarps * 32), sel_smem, st, true,
                   x, wr, (const float*)lt, (const float*)wnorm, bias, c.T, c.H, c.E, c.k, c.bias_in_weights,

@@ -26,6 +26,9 @@ TC_SMALL = {
     # two expert tiles (128 + 32), 2% outlier tokens (x20): wide candidate sets
     "tc_outliers_mxfp8": dict(T=520, H=384, E=160, k=6, F=128, fmt="mxfp8", seed=17, outlier_frac=0.02,
                               bias="uniform"),
+    # more than two waves of 128-expert tiles: 192-expert tiles (192 + 192 +
+    # 16, the last one partial), 102 token tiles (the last one 72 rows)
+    "tc_wide_nvfp4": dict(T=13000, H=256, E=400, k=8, F=256, fmt="nvfp4", seed=18, **U),
 }
 
 

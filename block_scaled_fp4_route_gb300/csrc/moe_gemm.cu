@@ -510,28 +510,36 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
 #pragma unroll 1
     for (int b = 0; b < 2; ++b) {
       uint32_t pk[16];  // 32 bf16 h values
+      float mh = 0.0f;  // their largest |h| before the bf16 rounding
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
         const int c = j >> 4, jj = j & 15;
-        float g0 = __uint_as_float(r0[c][jj]) * s0, g1 = __uint_as_float(r0[c][jj + 1]) * s0;
-        float u0 = __uint_as_float(r1[c][jj]) * s1, u1 = __uint_as_float(r1[c][jj + 1]) * s1;
+        // MXFP8 has no global scales (s0 = s1 = 1)
+        float g0 = __uint_as_float(r0[c][jj]), g1 = __uint_as_float(r0[c][jj + 1]);
+        float u0 = __uint_as_float(r1[c][jj]), u1 = __uint_as_float(r1[c][jj + 1]);
+        if constexpr (FMT == MOE_FMT_NVFP4) {
+          g0 *= s0;
+          g1 *= s0;
+          u0 *= s1;
+          u1 *= s1;
+        }
         if (capped) {
           g0 = a.cap * tanh_soft(g0 * a.inv_cap);
           g1 = a.cap * tanh_soft(g1 * a.inv_cap);
           u0 = a.cap * tanh_soft(u0 * a.inv_cap);
           u1 = a.cap * tanh_soft(u1 * a.inv_cap);
         }
-        const __nv_bfloat162 hv = __floats2bfloat162_rn(silu(g0) * u0, silu(g1) * u1);
+        const float h0 = silu(g0) * u0, h1 = silu(g1) * u1;
+        if constexpr (FMT == MOE_FMT_MXFP8) mh = fmaxf(mh, fmaxf(fabsf(h0), fabsf(h1)));
+        const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
         pk[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
       }
       const int f = f0 + 32 * b;
       if constexpr (FMT == MOE_FMT_MXFP8) {
         // the block's 32 features are this thread's: amax, E8M0 scale and
-        // E4M3 codes in registers
-        float m = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          m = fmaxf(m, fmaxf(fabsf(__uint_as_float(pk[i] << 16)), fabsf(__uint_as_float(pk[i] & 0xFFFF0000u))));
+        // E4M3 codes in registers.  The largest |bf16(h)| is bf16(largest
+        // |h|): rounding to nearest even is monotone and symmetric.
+        const float m = __bfloat162float(__float2bfloat16_rn(mh));
         uint32_t sc = 0, q[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         if (m != 0.0f) {
           sc = mx_scale_code(m, a.mx_mode);

@@ -455,8 +455,8 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
             const int64_t row = (int64_t)rt.row + n;
             float g = __uint_as_float(r0[0][j]) * (sA0 * gb);
             float u = __uint_as_float(r1[0][j]) * (sA1 * gb);
-            g = capped ? a1.cap * tanh_soft(g * a1.inv_cap) : g;
-            u = capped ? a1.cap * tanh_soft(u * a1.inv_cap) : u;
+            g = capped ? cap_soft(g, a1.cap, a1.inv_cap) : g;
+            u = capped ? cap_soft(u, a1.cap, a1.inv_cap) : u;
             const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * u);
             if constexpr (FMT == MOE_FMT_MXFP8) {
               const float v = __bfloat162float(hb);

@@ -340,8 +340,8 @@ __global__ void __launch_bounds__(Cfg<FMT, GATED>::THREADS, 1)
           const int64_t row = (int64_t)rt.row + n;
           float g = __uint_as_float(c0[j]) * (sA0 * gb);
           float u = __uint_as_float(c1[j]) * (sA1 * gb);
-          g = capped ? a.cap * tanh_soft(g * a.inv_cap) : g;
-          u = capped ? a.cap * tanh_soft(u * a.inv_cap) : u;
+          g = capped ? cap_soft(g, a.cap, a.inv_cap) : g;
+          u = capped ? cap_soft(u, a.cap, a.inv_cap) : u;
           const __nv_bfloat16 hb = __float2bfloat16_rn(silu(g) * u);
           if constexpr (FMT == MOE_FMT_MXFP8) {
             // the warp's 32 lanes are one 32-feature block of this token
@@ -524,10 +524,10 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
           u1 *= s1;
         }
         if (capped) {
-          g0 = a.cap * tanh_soft(g0 * a.inv_cap);
-          g1 = a.cap * tanh_soft(g1 * a.inv_cap);
-          u0 = a.cap * tanh_soft(u0 * a.inv_cap);
-          u1 = a.cap * tanh_soft(u1 * a.inv_cap);
+          g0 = cap_soft(g0, a.cap, a.inv_cap);
+          g1 = cap_soft(g1, a.cap, a.inv_cap);
+          u0 = cap_soft(u0, a.cap, a.inv_cap);
+          u1 = cap_soft(u1, a.cap, a.inv_cap);
         }
         const float h0 = silu(g0) * u0, h1 = silu(g1) * u1;
         if constexpr (FMT == MOE_FMT_MXFP8) mh = fmaxf(mh, fmaxf(fabsf(h0), fabsf(h1)));

@@ -149,6 +149,23 @@ __device__ __forceinline__ float tanh_soft(float x) {
   return copysignf(1.0f - 2.0f * rcp_approx(e + 1.0f), x);
 }
 
+// The soft cap c * tanh(v / c) (inv_c = fp32(1 / c)): with x = v inv_c below
+// 0.5 it is c x + (c x) x^2 P(x^2), and c x differs from v by at most
+// |v| 2^-24 (inv_c is rounded once), so it is evaluated as fma(v x^2, P, v):
+// one multiply fewer than scaling tanh_soft's result.
+__device__ __forceinline__ float cap_soft(float v, float c, float inv_c) {
+  const float x = v * inv_c;
+  if (fabsf(x) < 0.5f) {
+    const float x2 = x * x;
+    float p = 0.0172414667904377f;
+    p = fmaf(p, x2, -0.05304548144340515f);
+    p = fmaf(p, x2, 0.13325878977775574f);
+    p = fmaf(p, x2, -0.333331435918808f);
+    return fmaf(v * x2, p, v);
+  }
+  return c * tanh_soft(x);
+}
+
 // silu(g) = g / (1 + e^{-g}), with the hardware base-2 exponential and
 // reciprocal (a few ulp; -0 for large negative g, g for large positive g).
 __device__ __forceinline__ float silu(float g) {

@@ -486,6 +486,29 @@ __device__ __forceinline__ void store_rows32(float* base, int stride, int nv, co
     if (i < nv) base[(int64_t)i * stride] = __uint_as_float(i < 16 ? lo[i] : hi[i - 16]);
 }
 
+// 4 x 4 transpose of 16-byte chunks within each group of four lanes: on
+// entry lane 4g + j holds chunks 0..3 of its row (v[4c .. 4c + 3] = chunk c),
+// on exit chunk j of rows 4g .. 4g + 3 (v[4r .. 4r + 3] = chunk j of row
+// 4g + r).  Two rounds, as in warp_transpose32, four words per chunk.
+__device__ __forceinline__ void quad_transpose4x4(uint32_t (&v)[16], int lane) {
+#pragma unroll
+  for (int m = 2; m >= 1; m >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c & m) continue;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t& a = v[4 * c + w];
+        uint32_t& b = v[4 * (c | m) + w];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, up ? a : b, m);
+        if (up) a = recv;
+        else b = recv;
+      }
+    }
+  }
+}
+
 // Token-major epilogue after the TMEM copy: r0 / r1 hold this thread's 64
 // columns of weight block 0 / 1 (token row n of the tile, features
 // 64 hc .. 64 hc + 63 of each block); s0 / s1 the global scales.  Gated:
@@ -569,21 +592,41 @@ __device__ __forceinline__ void tm_epilogue_math(const GemmArgs& a, uint32_t (&r
       }
     }
   } else if (a.y16) {
-    // MOE_Y_FP16E: each thread's 64 features of a block are two whole
-    // 32-feature exponent blocks of its own row, encoded and stored by the
-    // thread (64 contiguous bytes per block; no collective operation)
+    // MOE_Y_FP16E: each thread's 64 features of a weight block are two whole
+    // 32-feature exponent blocks of its own row, encoded by the thread (no
+    // exchange for the exponent).  A block's codes are 64 bytes, four 16-byte
+    // chunks; the four lanes of each group of four swap chunks (a 4 x 4
+    // transpose) so that each store instruction writes whole 64-byte blocks
+    // of eight rows instead of one 16-byte quarter of 32 rows.
     const int64_t prow = (int64_t)rt.canon + n;
-    if (!valid || !MOE_IN_BOUNDS(prow < a.P)) return;
+    const bool row_ok = valid && MOE_IN_BOUNDS(prow < a.P);
+    int nv = rt.n_valid - q * 32;  // token rows of this quadrant in the tile (warp-uniform)
+    if (!MOE_IN_BOUNDS((int64_t)rt.canon + q * 32 + (nv > 32 ? 32 : nv) <= a.P)) nv = 0;
+    if (nv <= 0) return;
     const int f0 = mt * ROWS + 64 * hc;
-    uint16_t* yrow = reinterpret_cast<uint16_t*>(a.y_out) + prow * a.NA + f0;
+    const int g4 = lane & ~3;  // first row of this lane's group within the quadrant
+    uint16_t* ybase = reinterpret_cast<uint16_t*>(a.y_out) + ((int64_t)rt.canon + q * 32 + g4) * a.NA + f0 +
+                      8 * (lane & 3);
     uint16_t* erow = reinterpret_cast<uint16_t*>(a.y_exp + prow * (a.NA >> 5) + (f0 >> 5));
-    int e0 = y16_block_store(r0[0], r0[1], s0, yrow);
-    int e1 = y16_block_store(r0[2], r0[3], s0, yrow + 32);
-    erow[0] = (uint16_t)((e0 & 0xFF) | ((e1 & 0xFF) << 8));
-    if (second) {
-      e0 = y16_block_store(r1[0], r1[1], s1, yrow + 128);
-      e1 = y16_block_store(r1[2], r1[3], s1, yrow + 160);
-      erow[2] = (uint16_t)((e0 & 0xFF) | ((e1 & 0xFF) << 8));
+    uint32_t pk[16];
+    int eb[2];
+#pragma unroll
+    for (int wb = 0; wb < 2; ++wb) {
+      if (wb == 1 && !second) break;
+      uint32_t(&ra)[4][16] = wb == 0 ? r0 : r1;
+      const float sc = wb == 0 ? s0 : s1;
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        eb[b] = y16_block_codes(ra[2 * b], ra[2 * b + 1], sc, pk);
+        quad_transpose4x4(pk, lane);
+        uint16_t* dst = ybase + 128 * wb + 32 * b;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          if (g4 + r < nv)
+            *reinterpret_cast<uint4*>(dst + (int64_t)r * a.NA) =
+                make_uint4(pk[4 * r], pk[4 * r + 1], pk[4 * r + 2], pk[4 * r + 3]);
+      }
+      if (row_ok) erow[2 * wb] = (uint16_t)((eb[0] & 0xFF) | ((eb[1] & 0xFF) << 8));
     }
   } else {
     // y rows are written feature-contiguously: each 32 x 32 (token x

@@ -73,10 +73,10 @@ struct GemmArgs {
 
 // One MOE_Y_FP16E block held by one thread: the 32 values lo[0..15],
 // hi[0..15] (fp32 bits) times sc, the same fp32 products the fp32 format
-// stores; their codes go to dst (32 fp16, 64 bytes, 16-byte aligned) and the
-// block's exponent is returned.
-__device__ __forceinline__ int y16_block_store(const uint32_t (&lo)[16], const uint32_t (&hi)[16], float sc,
-                                               uint16_t* dst) {
+// stores; their codes go to pk (32 fp16, two per word, in feature order) and
+// the block's exponent is returned.
+__device__ __forceinline__ int y16_block_codes(const uint32_t (&lo)[16], const uint32_t (&hi)[16], float sc,
+                                               uint32_t (&pk)[16]) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -88,12 +88,8 @@ __device__ __forceinline__ int y16_block_store(const uint32_t (&lo)[16], const u
   for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(v[j]));
   const int e = y16_exponent(m);
   const float mul = exp2i(-e);
-  uint32_t pk[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) pk[j] = f16x2_encode(__fmul_rn(v[2 * j], mul), __fmul_rn(v[2 * j + 1], mul));
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
   return e;
 }
 

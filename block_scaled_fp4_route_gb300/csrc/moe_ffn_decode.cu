@@ -51,6 +51,13 @@ __device__ __forceinline__ int ld_acquire(const int32_t* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ int ld_relaxed(const int32_t* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// after a relaxed read that saw a release store: together an acquire
+__device__ __forceinline__ void fence_acquire_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void st_release(int32_t* p, int v) {
   asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -107,7 +114,9 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = abort_flag + 1;  // the epilogue's "this tile completed its row tile"
   volatile int* ring = last_flag + 1;        // [kSchedDepth] tile indices (-1: no more tiles)
-  static_assert(16 * C::STAGES + 8 * 5 + 16 * kSchedDepth + 4 * (3 + kSchedDepth) <= C::BAR_BYTES, "barrier area");
+  volatile int* ring_nv = ring + kSchedDepth;  // [kSchedDepth] their token rows (n_valid)
+  static_assert(16 * C::STAGES + 8 * 5 + 16 * kSchedDepth + 4 * (3 + 2 * kSchedDepth) <= C::BAR_BYTES,
+                "barrier area");
   int32_t* s_rtb = reinterpret_cast<int32_t*>(smem + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -165,9 +174,12 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
     if (g1) map_tile(t, MT1, s_rtb, E, mt, rti);
     else map_tile(t - total1, MT2, s_rtb, E, mt, rti);
   };
-  // h rows of row tile rti ready for the down GEMM (acquire)
+  // h rows of row tile rti ready for the down GEMM (acquire; relaxed: a hint)
   auto h_ready = [&](int rti) {
     return FMT == MOE_FMT_NVFP4 ? ld_acquire(sy.ready + rti) != 0 : ld_acquire(sy.done1 + rti) >= MT1;
+  };
+  auto h_ready_relaxed = [&](int rti) {
+    return FMT == MOE_FMT_NVFP4 ? ld_relaxed(sy.ready + rti) != 0 : ld_relaxed(sy.done1 + rti) >= MT1;
   };
 
   if (warp == 0) {
@@ -185,11 +197,25 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
       bool prev_done = false;  // pdl_wait returned
       int held_stage[C::STAGES], held_kb[C::STAGES];
       // tiles are claimed one ahead: the next index is requested when a tile
-      // starts and read when it ends, so the counter's round trip does not
-      // stall the loads
+      // starts, and its descriptor (and, for a down tile, a first look at its
+      // row tile's flag) is read halfway through the tile, so that neither
+      // the counter's round trip nor a global load sits between the last
+      // stage of one tile and the first stage of the next
       // (a CTA that runs no tile, e.g. one whose plan failed its check in the
       // bounds-checked build, takes no index from the counter)
       int claimed = total > 0 ? atomicAdd(sy.next_tile, 1) : 0;
+      bool c_have = false, c_g1 = false, c_ready = false;
+      int c_mt = 0, c_rti = 0;
+      RowTile c_rt{};
+      auto fetch_claimed = [&]() {
+        if (claimed < total) {
+          tile_of(claimed, c_g1, c_mt, c_rti);
+          c_rt = load_tile(a1.tiles + c_rti);
+          // relaxed: a hint only; a tile found ready is acquired with a fence
+          c_ready = !c_g1 && !sy.withhold_arrivals && h_ready_relaxed(c_rti);
+        }
+        c_have = true;
+      };
       for (int i = 0; ok; ++i) {
         // pass the claimed tile on (the slot is free once the MMA and the
         // epilogue have read the index kSchedDepth tiles back)
@@ -199,15 +225,17 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
           ok = false;
           break;
         }
+        if (!c_have) fetch_claimed();
         const int t = claimed < total ? claimed : -1;
+        const bool g1 = c_g1;
+        const int mt = c_mt, rti = c_rti;
+        const RowTile rt = c_rt;
         ring[slot] = t;
+        ring_nv[slot] = t >= 0 ? rt.n_valid : 0;
         mbar_arrive(&sched_full[slot]);
         if (t < 0) break;
         claimed = atomicAdd(sy.next_tile, 1);
-        bool g1;
-        int mt, rti;
-        tile_of(t, g1, mt, rti);
-        const RowTile rt = load_tile((g1 ? a1 : a2).tiles + rti);
+        c_have = false;
         const GemmArgs& a = g1 ? a1 : a2;
         const CUtensorMap* mA0 = g1 ? &tmG : &tmD;
         const CUtensorMap* mA1 = g1 ? &tmU : &tmD;
@@ -226,9 +254,11 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
         const uint8_t* sfa1 = a.sfA1 + (int64_t)(arow1 >> 7) * apr * 512;
         const uint8_t* sfb = a.sfB + (int64_t)(rt.row / C::NT) * apr * 512;
         const uint32_t bytes = C::NA * C::A_BYTES + N * 128 + (C::NA + 1) * C::SF_BYTES;
-        bool tok = g1 ? prev_done : false;  // may the token part go out now
-        if (!g1 && !sy.withhold_arrivals) tok = h_ready(rti);
-        if (!g1 && tok) fence_proxy_async_global();
+        bool tok = g1 ? prev_done : c_ready;  // may the token part go out now
+        if (!g1 && tok) {
+          fence_acquire_gpu();  // with the relaxed read of the flag: an acquire
+          fence_proxy_async_global();
+        }
         int nh = 0;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, status, ST_TIMEOUT_PRODUCER, limit)) {
@@ -291,6 +321,7 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
             }
             nh = 0;
           }
+          if (!c_have && kb == KB / 2) fetch_claimed();
         }
       }
       if (!prev_done) pdl_wait();
@@ -318,12 +349,13 @@ __global__ void __launch_bounds__(Cfg<FMT, true>::THREADS, 1)
           break;
         }
         const int t = ring[slot];
+        const int nv = ring_nv[slot];
         mbar_arrive(&sched_empty[slot]);
         if (t < 0) break;
         bool g1;
         int mt, rti;
         tile_of(t, g1, mt, rti);
-        const uint32_t N = (uint32_t)((a1.tiles[rti].n_valid + 15) & ~15);
+        const uint32_t N = (uint32_t)((nv + 15) & ~15);
         const int KB = g1 ? KB1 : KB2;
         const int buf = it % C::ACC_BUFS;
         const uint32_t use = (uint32_t)(it / C::ACC_BUFS) & 1u;

@@ -61,11 +61,13 @@ void ws_layout(const moe_config& c, moe_ws_layout* L);
 // for it on the device.
 // Router: logits + top-k + weights.  `scratch` holds router_scratch_floats(c)
 // floats; `status` (nullable) is cleared by the router's first kernel.
+// `fixed_scratch`: the caller's scratch is the static array of
+// moe_route_noalloc, whose documented bound keeps the original split counts.
 cudaError_t launch_router(const moe_config& c, const __nv_bfloat16* x, const __nv_bfloat16* wr,
                           const float* bias, float* scratch, int32_t* idx, float* w, uint32_t* status,
-                          cudaStream_t st, bool pdl);
-size_t router_scratch_floats(const moe_config& c);
-int router_splits(const moe_config& c);
+                          cudaStream_t st, bool pdl, bool fixed_scratch = false);
+size_t router_scratch_floats(const moe_config& c, bool fixed_scratch = false);
+int router_splits(const moe_config& c, bool fixed_scratch = false);
 // Prefill router (tensor-core logits, exact re-check of the candidates).
 bool router_uses_tc(const moe_config& c);
 size_t router_tc_scratch_floats(const moe_config& c);
